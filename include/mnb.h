@@ -1,0 +1,209 @@
+/*
+ * mnb.h — C ABI of the GB300 (sm_103a) weight-only INT4 blockwise MatMul in
+ * the ONNX com.microsoft::MatMulNBits form.
+ *
+ * Operation (page "Qwen3 CPU Inference Critical Path", section "Exact kernel
+ * inventory", row com.microsoft::MatMulNBits v1; section "Prepared weight-only
+ * plan"):
+ *
+ *   Y[m,n] = sum_k A[m,k] * (q[n,k] - z[n,k/bs]) * s[n,k/bs] + bias[n]
+ *
+ * for 0 <= m < M, 0 <= n < N, 0 <= k < K, bs = block_size, with the 4-bit
+ * codes q and zero points z unsigned (0..15) and z = 8 when no zero points
+ * are given. Weights stay compressed: no call expands them to a dense matrix.
+ *
+ * Conventions for every call:
+ *  - Every pointer argument is a DEVICE pointer unless its comment says HOST.
+ *    The caller owns and allocates every buffer; the library allocates no
+ *    device memory in any call.
+ *  - Calls that take a stream are asynchronous on it (NULL = legacy default
+ *    stream). A returned MNB_OK means the work was validated and enqueued.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    rejected call enqueues nothing and touches no buffer. No call ever falls
+ *    back to a CPU path. MNB_ERR_CUDA reports a failed launch or copy;
+ *    mnb_last_error_string() then describes it (per calling thread).
+ *  - No exception crosses this boundary.
+ */
+#ifndef MNB_H
+#define MNB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MNB_API __attribute__((visibility("default")))
+#else
+#define MNB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *mnb_stream_t;
+
+typedef enum {
+  MNB_OK = 0,
+  MNB_ERR_NULL = -1,        /* a required pointer is NULL                 */
+  MNB_ERR_SHAPE = -2,       /* M, N or K out of range                     */
+  MNB_ERR_BLOCKSIZE = -3,   /* block_size not a power of two in [16, 256] */
+  MNB_ERR_DTYPE = -4,       /* unknown dtype or unsupported combination   */
+  MNB_ERR_ALIGN = -5,       /* a pointer breaks its alignment rule        */
+  MNB_ERR_ALIAS = -6,       /* the output overlaps an input               */
+  MNB_ERR_CUDA = -7,        /* a CUDA launch or copy failed               */
+  MNB_ERR_UNSUPPORTED = -8, /* valid request the library cannot serve     */
+  MNB_ERR_DEVICE = -9       /* current device is not an sm_103 GPU        */
+} mnb_status;
+
+typedef enum { MNB_F32 = 0, MNB_BF16 = 1 } mnb_dtype;
+
+/* Path selection for mnb_matmul_path (the crossover sweep forces a path). */
+typedef enum {
+  MNB_PATH_AUTO = 0, /* small-M kernel for M <= 16, tensor-core GEMM above */
+  MNB_PATH_GEMV = 1, /* split-K decode kernel (M <= 16)                    */
+  MNB_PATH_GEMM = 2  /* TMA + tcgen05/TMEM prefill kernel (any M)          */
+} mnb_path;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MNB_API const char *mnb_status_string(int status);
+
+/* Description of the last failing call on the calling thread (static buffer
+ * owned by the library, valid until the thread's next failing call). */
+MNB_API const char *mnb_last_error_string(void);
+
+/* Library ABI version: (major << 16) | minor. */
+MNB_API int mnb_version(void);
+
+/*
+ * Sizes in bytes of the three prepacked buffers for an N x K weight
+ * (section "Prepared weight-only plan": packed constant storage aligned for
+ * the selected kernel). HOST outputs; zp_bytes is 0 when has_zero_points is
+ * 0. The packed layout pads N up to a multiple of 16 and K up to a multiple
+ * of 64 with zero codes; for N % 16 == 0 and K % 64 == 0 the packed codes
+ * take exactly the N*K/2 bytes of the input.
+ * Errors: MNB_ERR_NULL (an output pointer), MNB_ERR_SHAPE (N or K < 1),
+ * MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE.
+ */
+MNB_API mnb_status mnb_prepacked_sizes(int64_t N, int64_t K, int block_size,
+                                       mnb_dtype scale_dtype,
+                                       int has_zero_points,
+                                       size_t *packed_b_bytes,
+                                       size_t *packed_scales_bytes,
+                                       size_t *packed_zp_bytes);
+
+/*
+ * Offline re-layout of one MatMulNBits weight into the prepacked form the
+ * kernels stream with 128-bit loads (run once per weight; section "Prepared
+ * weight-only plan" and section "Phase Q1", item "plan-owned packed weights
+ * reused by every token").
+ *
+ *  B            uint8 [N, nb, bs/2], nb = ceil(K/bs): element k of row n is
+ *               byte (k mod bs)/2 of block k/bs, even k in the low nibble
+ *               (the MatMulNBits "packed UINT8 storage").
+ *  scales       [N, nb] in scale_dtype (fp32, or bf16 as raw 16-bit words).
+ *  zero_points  uint8 [N, ceil(nb/2)], even block in the low nibble, or NULL
+ *               (every zero point is 8; packed_zp is then not written).
+ *  packed_b, packed_scales, packed_zp: outputs of the sizes given by
+ *               mnb_prepacked_sizes, 16-byte aligned.
+ * The re-layout is lossless for every code with k < K; the storage padding
+ * nibbles past K in the last block are not kept. Inputs need only byte
+ * (B, zero_points) or element (scales) alignment. The last kernel it
+ * enqueues is empty (see mnb_set_programmatic_launch).
+ * Errors: MNB_ERR_NULL, MNB_ERR_SHAPE, MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE,
+ * MNB_ERR_ALIGN (a packed output not 16-byte aligned), MNB_ERR_ALIAS (an
+ * output overlaps an input or another output), MNB_ERR_CUDA.
+ */
+MNB_API mnb_status mnb_prepack(const uint8_t *B, const void *scales,
+                               const uint8_t *zero_points, int64_t N,
+                               int64_t K, int block_size,
+                               mnb_dtype scale_dtype, void *packed_b,
+                               void *packed_scales, void *packed_zp,
+                               mnb_stream_t stream);
+
+/*
+ * Inverse of mnb_prepack: writes B [N, nb, bs/2] (padding nibbles past K set
+ * to 0), scales [N, nb] and, when packed_zp is not NULL, zero_points
+ * [N, ceil(nb/2)] (an unused high nibble of an odd nb set to 0). Used to
+ * prove the re-layout lossless. Same error rules as mnb_prepack.
+ */
+MNB_API mnb_status mnb_unprepack(const void *packed_b,
+                                 const void *packed_scales,
+                                 const void *packed_zp, int64_t N, int64_t K,
+                                 int block_size, mnb_dtype scale_dtype,
+                                 uint8_t *B, void *scales,
+                                 uint8_t *zero_points, mnb_stream_t stream);
+
+/*
+ * Y = A * dequant(B)^T + bias on the prepacked weight.
+ *
+ *  A            [M, K] row-major in a_dtype (fp32 or bf16), element-aligned.
+ *  packed_b     prepacked codes from mnb_prepack (16-byte aligned).
+ *  scales       prepacked scales from mnb_prepack, in scale_dtype.
+ *  zero_points  prepacked zero points from mnb_prepack, or NULL for the
+ *               default zero point 8 (must match how the weight was packed).
+ *  bias         fp32 [N] or NULL.
+ *  Y            [M, N] row-major in a_dtype; bf16 results are rounded to
+ *               nearest even from the fp32 accumulator. Must not overlap
+ *               any input.
+ *  M >= 1, N >= 1, K >= 1, each below 2^31; block_size a power of two in
+ *  [16, 256], matching the prepacked weight.
+ * Accumulation is fp32. Results are bitwise reproducible for a given device,
+ * shape and path (every split-K reduction runs in a fixed order).
+ * Errors: MNB_ERR_NULL, MNB_ERR_SHAPE, MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE,
+ * MNB_ERR_ALIGN, MNB_ERR_ALIAS, MNB_ERR_UNSUPPORTED (no kernel for this
+ * combination), MNB_ERR_DEVICE, MNB_ERR_CUDA.
+ */
+MNB_API mnb_status mnb_matmul(const void *A, const void *packed_b,
+                              const void *scales, const void *zero_points,
+                              const float *bias, int64_t M, int64_t N,
+                              int64_t K, int block_size, void *Y,
+                              mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                              mnb_stream_t stream);
+
+/* mnb_matmul with the kernel path forced (MNB_PATH_GEMV needs M <= 16,
+ * else MNB_ERR_UNSUPPORTED). */
+MNB_API mnb_status mnb_matmul_path(const void *A, const void *packed_b,
+                                   const void *scales, const void *zero_points,
+                                   const float *bias, int64_t M, int64_t N,
+                                   int64_t K, int block_size, void *Y,
+                                   mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                   mnb_path path, mnb_stream_t stream);
+
+/*
+ * mnb_matmul for callers whose activations and results live in HOST memory:
+ * copies A_host [M, K] into the caller's device buffer A_dev, runs the
+ * product into Y_dev, and copies Y_dev back into Y_host [M, N], all
+ * enqueued on stream (page-locked host buffers make the copies
+ * asynchronous; pageable ones make them synchronous with the host). The
+ * host buffers must stay valid until the stream reaches this point.
+ * Errors: as mnb_matmul; MNB_ERR_NULL also for the host buffers.
+ */
+MNB_API mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,
+                                        const void *packed_b,
+                                        const void *scales,
+                                        const void *zero_points,
+                                        const float *bias, int64_t M,
+                                        int64_t N, int64_t K, int block_size,
+                                        void *Y_dev, void *Y_host,
+                                        mnb_dtype a_dtype,
+                                        mnb_dtype scale_dtype,
+                                        mnb_stream_t stream);
+
+/*
+ * Programmatic dependent launch (on by default): each matmul kernel lets the
+ * next kernel on the stream launch early and starts streaming its own
+ * (constant) prepacked weights before the previous kernel has finished; it
+ * reads A, and writes Y, only after that kernel's results are visible. The
+ * packed buffers must therefore have been written before the previous
+ * kernel on the stream started; mnb_prepack guarantees this by ending with
+ * an empty kernel. Pass 0 to launch every kernel in plain stream order.
+ * Process-wide setting.
+ */
+MNB_API void mnb_set_programmatic_launch(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MNB_H */

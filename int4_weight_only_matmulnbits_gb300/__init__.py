@@ -1,0 +1,16 @@
+"""GB300 (sm_103a) weight-only INT4 blockwise MatMul, MatMulNBits form.
+
+The computation lives in the C-ABI library libmnb.so (include/mnb.h); this
+package is its thin Python binding plus the seeded workload generators. The
+library is loaded on first use and its absence is an error.
+"""
+from .binding import (EXPORTS, MnbError, PackedWeight, load, library_path,
+                      mnb_matmul, mnb_matmul_from_host, mnb_prepack,
+                      mnb_prepacked_sizes, mnb_set_programmatic_launch,
+                      mnb_unprepack, mnb_version, status_string)
+from ._build import build_library
+
+__all__ = ["EXPORTS", "MnbError", "PackedWeight", "build_library", "load",
+           "library_path", "mnb_matmul", "mnb_matmul_from_host", "mnb_prepack",
+           "mnb_prepacked_sizes", "mnb_set_programmatic_launch", "mnb_unprepack",
+           "mnb_version", "status_string"]

@@ -1,0 +1,216 @@
+"""Thin ctypes binding of libmnb.so (include/mnb.h), same names as the C ABI.
+
+Argument marshalling only: tensors are turned into device pointers, outputs
+are allocated with torch (device memory is plumbing here), and every
+computation runs in the library's CUDA kernels. A missing library raises
+immediately; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+MNB_OK = 0
+MNB_F32, MNB_BF16 = 0, 1
+MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2}
+
+# Every entry point include/mnb.h declares.
+EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
+           "mnb_prepacked_sizes", "mnb_prepack", "mnb_unprepack", "mnb_matmul",
+           "mnb_matmul_path", "mnb_matmul_from_host",
+           "mnb_set_programmatic_launch")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MnbError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {status_string(status)}"
+        if detail:
+            msg += f" [{detail}]"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load libmnb.so and declare its signatures. Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{path} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            _build.build_library()
+        lib = ctypes.CDLL(path)
+        p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        lib.mnb_status_string.argtypes = [i32]
+        lib.mnb_status_string.restype = ctypes.c_char_p
+        lib.mnb_last_error_string.argtypes = []
+        lib.mnb_last_error_string.restype = ctypes.c_char_p
+        lib.mnb_version.argtypes = []
+        lib.mnb_version.restype = i32
+        lib.mnb_prepacked_sizes.argtypes = [i64, i64, i32, i32, i32,
+                                            ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                            ctypes.POINTER(sz)]
+        lib.mnb_prepacked_sizes.restype = i32
+        lib.mnb_prepack.argtypes = [p, p, p, i64, i64, i32, i32, p, p, p, p]
+        lib.mnb_prepack.restype = i32
+        lib.mnb_unprepack.argtypes = [p, p, p, i64, i64, i32, i32, p, p, p, p]
+        lib.mnb_unprepack.restype = i32
+        lib.mnb_matmul.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32, i32, p]
+        lib.mnb_matmul.restype = i32
+        lib.mnb_matmul_path.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32,
+                                        i32, i32, p]
+        lib.mnb_matmul_path.restype = i32
+        lib.mnb_matmul_from_host.argtypes = [p, p, p, p, p, p, i64, i64, i64, i32,
+                                             p, p, i32, i32, p]
+        lib.mnb_matmul_from_host.restype = i32
+        lib.mnb_set_programmatic_launch.argtypes = [i32]
+        lib.mnb_set_programmatic_launch.restype = None
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().mnb_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != MNB_OK:
+        detail = load().mnb_last_error_string().decode()
+        raise MnbError(status, where, detail)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return MNB_F32
+    if dt == torch.bfloat16:
+        return MNB_BF16
+    raise TypeError(f"unsupported dtype {dt}: fp32 or bf16")
+
+
+@dataclass
+class PackedWeight:
+    """Caller-owned prepacked buffers of one N x K MatMulNBits weight."""
+    packed_b: torch.Tensor
+    packed_scales: torch.Tensor
+    packed_zp: torch.Tensor | None
+    N: int
+    K: int
+    block_size: int
+    scale_dtype: torch.dtype
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.packed_b, self.packed_scales, self.packed_zp) if t is not None)
+
+
+def mnb_version() -> int:
+    return load().mnb_version()
+
+
+def mnb_set_programmatic_launch(enable: bool) -> None:
+    load().mnb_set_programmatic_launch(1 if enable else 0)
+
+
+def mnb_prepacked_sizes(N: int, K: int, block_size: int, scale_dtype: torch.dtype,
+                        has_zero_points: bool) -> tuple[int, int, int]:
+    b, s, z = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().mnb_prepacked_sizes(N, K, block_size, _dtype_code(scale_dtype),
+                                      int(has_zero_points), ctypes.byref(b),
+                                      ctypes.byref(s), ctypes.byref(z)),
+           "mnb_prepacked_sizes")
+    return b.value, s.value, z.value
+
+
+def mnb_prepack(B: torch.Tensor, scales: torch.Tensor, zero_points: torch.Tensor | None,
+                N: int, K: int, block_size: int, *, stream=None) -> PackedWeight:
+    """Prepack one weight given in MatMulNBits layout (device tensors)."""
+    for name, t in (("B", B), ("scales", scales), ("zero_points", zero_points)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    sb, ss, sz = mnb_prepacked_sizes(N, K, block_size, scales.dtype,
+                                     zero_points is not None)
+    dev = B.device
+    packed_b = torch.empty(sb, dtype=torch.uint8, device=dev)
+    packed_s = torch.empty(ss, dtype=torch.uint8, device=dev)
+    packed_z = (torch.empty(sz, dtype=torch.uint8, device=dev)
+                if zero_points is not None else None)
+    _check(load().mnb_prepack(_ptr(B), _ptr(scales), _ptr(zero_points), N, K, block_size,
+                              _dtype_code(scales.dtype), _ptr(packed_b), _ptr(packed_s),
+                              _ptr(packed_z), _stream(stream)), "mnb_prepack")
+    return PackedWeight(packed_b, packed_s, packed_z, N, K, block_size, scales.dtype)
+
+
+def mnb_unprepack(w: PackedWeight, *, stream=None):
+    """Recover (B, scales, zero_points) in MatMulNBits layout from w."""
+    nb = -(-w.K // w.block_size)
+    dev = w.packed_b.device
+    B = torch.empty(w.N, nb, w.block_size // 2, dtype=torch.uint8, device=dev)
+    S = torch.empty(w.N, nb, dtype=w.scale_dtype, device=dev)
+    Z = (torch.empty(w.N, (nb + 1) // 2, dtype=torch.uint8, device=dev)
+         if w.packed_zp is not None else None)
+    _check(load().mnb_unprepack(_ptr(w.packed_b), _ptr(w.packed_scales), _ptr(w.packed_zp),
+                                w.N, w.K, w.block_size, _dtype_code(w.scale_dtype),
+                                _ptr(B), _ptr(S), _ptr(Z), _stream(stream)),
+           "mnb_unprepack")
+    return B, S, Z
+
+
+def mnb_matmul(A: torch.Tensor, w: PackedWeight, bias: torch.Tensor | None = None, *,
+               out: torch.Tensor | None = None, path: str = "auto",
+               stream=None) -> torch.Tensor:
+    """Y[M, N] = A[M, K] @ dequant(w)^T + bias, on the GPU."""
+    if A.dim() != 2 or A.shape[1] != w.K:
+        raise ValueError(f"A must be [M, {w.K}]")
+    if not A.is_cuda or not A.is_contiguous():
+        raise ValueError("A must be a contiguous CUDA tensor")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty(M, w.N, dtype=A.dtype, device=A.device)
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
+        raise ValueError("bias must be a CUDA float32 tensor")
+    _check(load().mnb_matmul_path(_ptr(A), _ptr(w.packed_b), _ptr(w.packed_scales),
+                                  _ptr(w.packed_zp), _ptr(bias), M, w.N, w.K,
+                                  w.block_size, _ptr(out), _dtype_code(A.dtype),
+                                  _dtype_code(w.scale_dtype), MNB_PATH[path],
+                                  _stream(stream)), "mnb_matmul")
+    return out
+
+
+def mnb_matmul_from_host(A_host: torch.Tensor, A_dev: torch.Tensor, w: PackedWeight,
+                         Y_dev: torch.Tensor, Y_host: torch.Tensor,
+                         bias: torch.Tensor | None = None, *, stream=None) -> torch.Tensor:
+    """Host A in, host Y out: copies and product enqueued on one stream."""
+    M = A_host.shape[0]
+    _check(load().mnb_matmul_from_host(
+        _ptr(A_host), _ptr(A_dev), _ptr(w.packed_b), _ptr(w.packed_scales),
+        _ptr(w.packed_zp), _ptr(bias), M, w.N, w.K, w.block_size, _ptr(Y_dev),
+        _ptr(Y_host), _dtype_code(A_host.dtype), _dtype_code(w.scale_dtype),
+        _stream(stream)), "mnb_matmul_from_host")
+    return Y_host

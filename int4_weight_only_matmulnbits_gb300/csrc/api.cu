@@ -1,0 +1,324 @@
+// C ABI of the MatMulNBits library (declared in include/mnb.h): argument
+// validation, path dispatch and launch-error reporting. Every check happens
+// on the host before anything is enqueued; nothing here falls back to a CPU
+// computation.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mnb.h"
+#include "mnb_common.cuh"
+#include "mnb_launch.h"
+
+namespace mnb {
+
+namespace {
+std::atomic<int> g_pdl{1};
+thread_local char g_last_error[256] = "";
+
+mnb_status cuda_fail(cudaError_t e, const char *where) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where,
+                cudaGetErrorName(e), cudaGetErrorString(e));
+  return MNB_ERR_CUDA;
+}
+
+bool valid_block_size(int bs) {
+  return bs >= 16 && bs <= 256 && (bs & (bs - 1)) == 0;
+}
+
+bool valid_dtype(int d) { return d == MNB_F32 || d == MNB_BF16; }
+
+size_t dtype_size(int d) { return d == MNB_F32 ? 4 : 2; }
+
+bool aligned(const void *p, size_t a) {
+  return reinterpret_cast<uintptr_t>(p) % a == 0;
+}
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a);
+  const uintptr_t y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+struct Sizes {
+  size_t b, s, z;
+};
+
+Sizes packed_sizes(int64_t N, int64_t K, int bs, int scale_dtype, bool zp) {
+  const int64_t N16 = ceil_div(N, kTileN), K64 = ceil_div(K, kChunkK);
+  const int64_t nb = ceil_div(K, bs);
+  Sizes s;
+  s.b = size_t(N16) * K64 * kChunkBytes;
+  s.s = size_t(N16) * nb * kTileN * dtype_size(scale_dtype);
+  s.z = zp ? size_t(N16) * nb * 8 : 0;
+  return s;
+}
+
+// Largest sizes the kernels index with 32-bit arithmetic.
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+mnb_status check_shape(int64_t N, int64_t K, int bs, int scale_dtype) {
+  if (N < 1 || K < 1 || N > kMaxDim || K > kMaxDim) return MNB_ERR_SHAPE;
+  if (ceil_div(N, kTileN) * ceil_div(K, kChunkK) > (int64_t(1) << 40))
+    return MNB_ERR_SHAPE;
+  if (!valid_block_size(bs)) return MNB_ERR_BLOCKSIZE;
+  if (!valid_dtype(scale_dtype)) return MNB_ERR_DTYPE;
+  return MNB_OK;
+}
+
+mnb_status check_device() {
+  int dev = 0, major = 0, minor = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess)
+    err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (err == cudaSuccess)
+    err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (err != cudaSuccess) return cuda_fail(err, "device query");
+  if (major != 10 || minor != 3) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "device is sm_%d%d; this library is built for sm_103a",
+                  major, minor);
+    return MNB_ERR_DEVICE;
+  }
+  return MNB_OK;
+}
+
+mnb_status check_outputs_disjoint(void *const outs[3], const size_t out_n[3],
+                                  const void *const ins[3],
+                                  const size_t in_n[3]) {
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(outs[i], out_n[i], ins[j], in_n[j])) return MNB_ERR_ALIAS;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], out_n[i], outs[j], out_n[j])) return MNB_ERR_ALIAS;
+  }
+  return MNB_OK;
+}
+
+mnb_status validate_matmul(const void *A, const void *packed_b,
+                           const void *scales, const void *zero_points,
+                           const float *bias, int64_t M, int64_t N, int64_t K,
+                           int block_size, const void *Y, int a_dtype,
+                           int scale_dtype, int path) {
+  if (!A || !packed_b || !scales || !Y) return MNB_ERR_NULL;
+  if (M < 1 || M > kMaxDim) return MNB_ERR_SHAPE;
+  mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  if (!valid_dtype(a_dtype)) return MNB_ERR_DTYPE;
+  if (path != MNB_PATH_AUTO && path != MNB_PATH_GEMV && path != MNB_PATH_GEMM)
+    return MNB_ERR_UNSUPPORTED;
+  if (path == MNB_PATH_GEMV && M > kGemvMaxM) return MNB_ERR_UNSUPPORTED;
+  const size_t es = dtype_size(a_dtype);
+  if (!aligned(A, es) || !aligned(Y, es) || !aligned(packed_b, 16) ||
+      !aligned(scales, 16) || (zero_points && !aligned(zero_points, 16)) ||
+      (bias && !aligned(bias, 4)))
+    return MNB_ERR_ALIGN;
+  const Sizes in = packed_sizes(N, K, block_size, scale_dtype, zero_points != nullptr);
+  const size_t y_bytes = size_t(M) * N * es;
+  const void *ins[5] = {A, packed_b, scales, zero_points, bias};
+  const size_t in_n[5] = {size_t(M) * K * es, in.b, in.s, in.z,
+                          bias ? size_t(N) * 4 : 0};
+  for (int j = 0; j < 5; ++j)
+    if (overlap(Y, y_bytes, ins[j], in_n[j])) return MNB_ERR_ALIAS;
+  return check_device();
+}
+
+mnb_status run_matmul(const void *A, const void *packed_b, const void *scales,
+                      const void *zero_points, const float *bias, int64_t M,
+                      int64_t N, int64_t K, int block_size, void *Y,
+                      int a_dtype, int scale_dtype, int path,
+                      cudaStream_t stream) {
+  MatmulArgs a{A, packed_b, scales, zero_points, bias, Y, M, N, K, block_size,
+               a_dtype == MNB_F32, scale_dtype == MNB_F32, g_pdl.load() != 0};
+  cudaError_t e;
+  if (path == MNB_PATH_GEMV || (path == MNB_PATH_AUTO && M <= kGemvMaxM))
+    e = launch_gemv(a, stream);
+  else
+    e = launch_gemm(a, stream);
+  if (e == cudaErrorNotSupported) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "no kernel for M=%lld N=%lld K=%lld bs=%d", (long long)M,
+                  (long long)N, (long long)K, block_size);
+    return MNB_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul");
+  return MNB_OK;
+}
+
+}  // namespace
+
+int sm_count() {
+  static std::once_flag once;
+  static int count = 148;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
+  });
+  return count;
+}
+
+}  // namespace mnb
+
+using namespace mnb;
+
+extern "C" {
+
+const char *mnb_status_string(int status) {
+  switch (status) {
+    case MNB_OK: return "MNB_OK";
+    case MNB_ERR_NULL: return "MNB_ERR_NULL: a required pointer is NULL";
+    case MNB_ERR_SHAPE: return "MNB_ERR_SHAPE: M, N or K out of range";
+    case MNB_ERR_BLOCKSIZE:
+      return "MNB_ERR_BLOCKSIZE: block_size must be a power of two in [16, 256]";
+    case MNB_ERR_DTYPE: return "MNB_ERR_DTYPE: unknown or unsupported dtype";
+    case MNB_ERR_ALIGN: return "MNB_ERR_ALIGN: a pointer breaks its alignment rule";
+    case MNB_ERR_ALIAS: return "MNB_ERR_ALIAS: an output overlaps an input";
+    case MNB_ERR_CUDA: return "MNB_ERR_CUDA: a CUDA launch or copy failed";
+    case MNB_ERR_UNSUPPORTED:
+      return "MNB_ERR_UNSUPPORTED: no kernel serves this combination";
+    case MNB_ERR_DEVICE: return "MNB_ERR_DEVICE: current device is not sm_103";
+    default: return "unknown mnb_status";
+  }
+}
+
+const char *mnb_last_error_string(void) { return g_last_error; }
+
+int mnb_version(void) { return (1 << 16) | 0; }
+
+void mnb_set_programmatic_launch(int enable) { g_pdl.store(enable ? 1 : 0); }
+
+mnb_status mnb_prepacked_sizes(int64_t N, int64_t K, int block_size,
+                               mnb_dtype scale_dtype, int has_zero_points,
+                               size_t *packed_b_bytes,
+                               size_t *packed_scales_bytes,
+                               size_t *packed_zp_bytes) {
+  if (!packed_b_bytes || !packed_scales_bytes || !packed_zp_bytes)
+    return MNB_ERR_NULL;
+  const mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  const Sizes s = packed_sizes(N, K, block_size, scale_dtype, has_zero_points != 0);
+  *packed_b_bytes = s.b;
+  *packed_scales_bytes = s.s;
+  *packed_zp_bytes = s.z;
+  return MNB_OK;
+}
+
+mnb_status mnb_prepack(const uint8_t *B, const void *scales,
+                       const uint8_t *zero_points, int64_t N, int64_t K,
+                       int block_size, mnb_dtype scale_dtype, void *packed_b,
+                       void *packed_scales, void *packed_zp,
+                       mnb_stream_t stream) {
+  if (!B || !scales || !packed_b || !packed_scales) return MNB_ERR_NULL;
+  if (zero_points && !packed_zp) return MNB_ERR_NULL;
+  mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  if (!aligned(packed_b, 16) || !aligned(packed_scales, 16) ||
+      (zero_points && !aligned(packed_zp, 16)) ||
+      !aligned(scales, dtype_size(scale_dtype)))
+    return MNB_ERR_ALIGN;
+  const int64_t nb = ceil_div(K, block_size);
+  const Sizes out = packed_sizes(N, K, block_size, scale_dtype, zero_points != nullptr);
+  const void *const ins[3] = {B, scales, zero_points};
+  const size_t in_n[3] = {size_t(N) * nb * (block_size / 2),
+                          size_t(N) * nb * dtype_size(scale_dtype),
+                          zero_points ? size_t(N) * ((nb + 1) / 2) : 0};
+  void *const outs[3] = {packed_b, packed_scales, zero_points ? packed_zp : nullptr};
+  const size_t out_n[3] = {out.b, out.s, out.z};
+  st = check_outputs_disjoint(outs, out_n, ins, in_n);
+  if (st != MNB_OK) return st;
+  st = check_device();
+  if (st != MNB_OK) return st;
+  PrepackArgs a{B, scales, zero_points, N, K, block_size,
+                scale_dtype == MNB_F32, packed_b, packed_scales, packed_zp};
+  const cudaError_t e = launch_prepack(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_prepack");
+  return MNB_OK;
+}
+
+mnb_status mnb_unprepack(const void *packed_b, const void *packed_scales,
+                         const void *packed_zp, int64_t N, int64_t K,
+                         int block_size, mnb_dtype scale_dtype, uint8_t *B,
+                         void *scales, uint8_t *zero_points,
+                         mnb_stream_t stream) {
+  if (!packed_b || !packed_scales || !B || !scales) return MNB_ERR_NULL;
+  if (packed_zp && !zero_points) return MNB_ERR_NULL;
+  mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  if (!aligned(packed_b, 16) || !aligned(packed_scales, 16) ||
+      (packed_zp && !aligned(packed_zp, 16)) ||
+      !aligned(scales, dtype_size(scale_dtype)))
+    return MNB_ERR_ALIGN;
+  const int64_t nb = ceil_div(K, block_size);
+  const Sizes in = packed_sizes(N, K, block_size, scale_dtype, packed_zp != nullptr);
+  const void *const ins[3] = {packed_b, packed_scales, packed_zp};
+  const size_t in_n[3] = {in.b, in.s, in.z};
+  void *const outs[3] = {B, scales, packed_zp ? zero_points : nullptr};
+  const size_t out_n[3] = {size_t(N) * nb * (block_size / 2),
+                           size_t(N) * nb * dtype_size(scale_dtype),
+                           packed_zp ? size_t(N) * ((nb + 1) / 2) : 0};
+  st = check_outputs_disjoint(outs, out_n, ins, in_n);
+  if (st != MNB_OK) return st;
+  st = check_device();
+  if (st != MNB_OK) return st;
+  UnprepackArgs a{packed_b, packed_scales, packed_zp, N, K, block_size,
+                  scale_dtype == MNB_F32, B, scales, zero_points};
+  const cudaError_t e = launch_unprepack(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_unprepack");
+  return MNB_OK;
+}
+
+mnb_status mnb_matmul_path(const void *A, const void *packed_b,
+                           const void *scales, const void *zero_points,
+                           const float *bias, int64_t M, int64_t N, int64_t K,
+                           int block_size, void *Y, mnb_dtype a_dtype,
+                           mnb_dtype scale_dtype, mnb_path path,
+                           mnb_stream_t stream) {
+  const mnb_status st = validate_matmul(A, packed_b, scales, zero_points, bias,
+                                        M, N, K, block_size, Y, a_dtype,
+                                        scale_dtype, path);
+  if (st != MNB_OK) return st;
+  return run_matmul(A, packed_b, scales, zero_points, bias, M, N, K,
+                    block_size, Y, a_dtype, scale_dtype, path,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+mnb_status mnb_matmul(const void *A, const void *packed_b, const void *scales,
+                      const void *zero_points, const float *bias, int64_t M,
+                      int64_t N, int64_t K, int block_size, void *Y,
+                      mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                      mnb_stream_t stream) {
+  return mnb_matmul_path(A, packed_b, scales, zero_points, bias, M, N, K,
+                         block_size, Y, a_dtype, scale_dtype, MNB_PATH_AUTO,
+                         stream);
+}
+
+mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,
+                                const void *packed_b, const void *scales,
+                                const void *zero_points, const float *bias,
+                                int64_t M, int64_t N, int64_t K,
+                                int block_size, void *Y_dev, void *Y_host,
+                                mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                mnb_stream_t stream) {
+  if (!A_host || !Y_host) return MNB_ERR_NULL;
+  const mnb_status st = validate_matmul(A_dev, packed_b, scales, zero_points,
+                                        bias, M, N, K, block_size, Y_dev,
+                                        a_dtype, scale_dtype, MNB_PATH_AUTO);
+  if (st != MNB_OK) return st;
+  const size_t es = dtype_size(a_dtype);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(A_dev, A_host, size_t(M) * K * es,
+                                  cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_from_host (A copy)");
+  const mnb_status rs = run_matmul(A_dev, packed_b, scales, zero_points, bias,
+                                   M, N, K, block_size, Y_dev, a_dtype,
+                                   scale_dtype, MNB_PATH_AUTO, s);
+  if (rs != MNB_OK) return rs;
+  e = cudaMemcpyAsync(Y_host, Y_dev, size_t(M) * N * es, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_from_host (Y copy)");
+  return MNB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,197 @@
+// Offline re-layout of MatMulNBits weights into the prepacked form, and its
+// inverse. The layout is defined in mnb_common.cuh.
+#include "mnb_common.cuh"
+#include "mnb_launch.h"
+
+namespace mnb {
+namespace {
+
+// Code q[n,k] of the MatMulNBits storage: byte (k mod bs)/2 of block k/bs,
+// low nibble for even k. Zero outside the logical N x K matrix.
+__device__ __forceinline__ uint32_t source_code(const uint8_t *B, int64_t n,
+                                                int64_t k, int64_t N, int64_t K,
+                                                int64_t nb, int bs) {
+  if (n >= N || k >= K) return 0;
+  const int64_t within = k % bs;
+  const uint8_t byte = B[(n * nb + k / bs) * (bs / 2) + within / 2];
+  return (within & 1) ? (byte >> 4) : (byte & 0x0F);
+}
+
+__global__ void pack_codes_kernel(const uint8_t *__restrict__ B,
+                                  uint32_t *__restrict__ out, int64_t N,
+                                  int64_t K, int64_t nb, int bs, int64_t K64,
+                                  int64_t words) {
+  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < words;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t chunk = w >> 7;
+    const int idx = static_cast<int>(w & 127);
+    const int lane = idx >> 2, j = idx & 3, g = lane >> 2, t = lane & 3;
+    const int64_t tile = chunk / K64, c = chunk % K64;
+    const int64_t r0 = tile * kTileN + g;
+    const int64_t k0 = c * kChunkK + 16 * j + 4 * t;
+    uint32_t word = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        word |= source_code(B, r0 + 8 * h, k0 + e, N, K, nb, bs)
+                << code_shift(e, h);
+    out[w] = word;
+  }
+}
+
+template <typename T>
+__global__ void pack_scales_kernel(const T *__restrict__ s, T *__restrict__ out,
+                                   int64_t N, int64_t nb, int64_t total) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = static_cast<int>(i & 15);
+    const int64_t tb = i >> 4;
+    const int64_t tile = tb / nb, b = tb % nb;
+    const int64_t n = tile * kTileN + r;
+    out[i] = n < N ? s[n * nb + b] : T(0);
+  }
+}
+
+__global__ void pack_zp_kernel(const uint8_t *__restrict__ zp,
+                               uint64_t *__restrict__ out, int64_t N,
+                               int64_t nb, int64_t total) {
+  const int64_t zbytes = (nb + 1) / 2;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = i / nb, b = i % nb;
+    uint64_t word = 0;
+    for (int r = 0; r < kTileN; ++r) {
+      const int64_t n = tile * kTileN + r;
+      if (n >= N) break;
+      const uint8_t byte = zp[n * zbytes + b / 2];
+      const uint64_t z = (b & 1) ? (byte >> 4) : (byte & 0x0F);
+      word |= z << (4 * r);
+    }
+    out[i] = word;
+  }
+}
+
+// Inverse of pack_codes_kernel: one thread per byte of B [N, nb, bs/2].
+__global__ void unpack_codes_kernel(const uint32_t *__restrict__ packed,
+                                    uint8_t *__restrict__ B, int64_t N,
+                                    int64_t K, int64_t nb, int bs, int64_t K64,
+                                    int64_t total) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t half = bs / 2;
+    const int64_t n = i / (nb * half);
+    const int64_t rem = i % (nb * half);
+    const int64_t kk = (rem / half) * bs + (rem % half) * 2;  // even k
+    uint32_t byte = 0;
+    for (int o = 0; o < 2; ++o) {
+      const int64_t k = kk + o;
+      if (k >= K) continue;
+      const int64_t tile = n / kTileN;
+      const int r = static_cast<int>(n % kTileN);
+      const int64_t c = k / kChunkK;
+      const int kin = static_cast<int>(k % kChunkK);
+      const int j = kin >> 4, t = (kin >> 2) & 3, e = kin & 3;
+      const int g = r & 7, h = r >> 3;
+      const int lane = g * 4 + t;
+      const uint32_t word = packed[(tile * K64 + c) * 128 + lane * 4 + j];
+      byte |= ((word >> code_shift(e, h)) & 0xF) << (4 * o);
+    }
+    B[i] = static_cast<uint8_t>(byte);
+  }
+}
+
+template <typename T>
+__global__ void unpack_scales_kernel(const T *__restrict__ packed,
+                                     T *__restrict__ s, int64_t nb,
+                                     int64_t total) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / nb, b = i % nb;
+    s[i] = packed[((n / kTileN) * nb + b) * kTileN + (n % kTileN)];
+  }
+}
+
+__global__ void unpack_zp_kernel(const uint64_t *__restrict__ packed,
+                                 uint8_t *__restrict__ zp, int64_t nb,
+                                 int64_t total) {
+  const int64_t zbytes = (nb + 1) / 2;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / zbytes, zb = i % zbytes;
+    const int64_t tile = n / kTileN;
+    const int r = static_cast<int>(n % kTileN);
+    uint32_t byte = 0;
+    for (int o = 0; o < 2; ++o) {
+      const int64_t b = zb * 2 + o;
+      if (b >= nb) continue;
+      byte |= static_cast<uint32_t>((packed[tile * nb + b] >> (4 * r)) & 0xF)
+              << (4 * o);
+    }
+    zp[i] = static_cast<uint8_t>(byte);
+  }
+}
+
+// Launched last by mnb_prepack. Matmul kernels launched with programmatic
+// dependent launch may start loading their packed weights as soon as the
+// kernel before them on the stream begins to exit; ending the prepack with
+// this empty kernel puts a full kernel boundary between the writes of the
+// packed weights and any such early load.
+__global__ void prepack_fence_kernel() {}
+
+inline unsigned grid_for(int64_t total) {
+  int64_t blocks = ceil_div(total, 256);
+  if (blocks > (1 << 20)) blocks = 1 << 20;
+  if (blocks < 1) blocks = 1;
+  return static_cast<unsigned>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream) {
+  const int64_t nb = ceil_div(a.K, a.bs);
+  const int64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
+  const int64_t words = N16 * K64 * (kChunkBytes / 4);
+  pack_codes_kernel<<<grid_for(words), 256, 0, stream>>>(
+      a.B, static_cast<uint32_t *>(a.packed_b), a.N, a.K, nb, a.bs, K64, words);
+  const int64_t ns = N16 * nb * kTileN;
+  if (a.scale_f32)
+    pack_scales_kernel<float><<<grid_for(ns), 256, 0, stream>>>(
+        static_cast<const float *>(a.scales),
+        static_cast<float *>(a.packed_scales), a.N, nb, ns);
+  else
+    pack_scales_kernel<uint16_t><<<grid_for(ns), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(a.scales),
+        static_cast<uint16_t *>(a.packed_scales), a.N, nb, ns);
+  if (a.zp != nullptr)
+    pack_zp_kernel<<<grid_for(N16 * nb), 256, 0, stream>>>(
+        a.zp, static_cast<uint64_t *>(a.packed_zp), a.N, nb, N16 * nb);
+  prepack_fence_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unprepack(const UnprepackArgs &a, cudaStream_t stream) {
+  const int64_t nb = ceil_div(a.K, a.bs);
+  const int64_t K64 = ceil_div(a.K, kChunkK);
+  const int64_t nbytes = a.N * nb * (a.bs / 2);
+  unpack_codes_kernel<<<grid_for(nbytes), 256, 0, stream>>>(
+      static_cast<const uint32_t *>(a.packed_b), a.B, a.N, a.K, nb, a.bs, K64,
+      nbytes);
+  const int64_t ns = a.N * nb;
+  if (a.scale_f32)
+    unpack_scales_kernel<float><<<grid_for(ns), 256, 0, stream>>>(
+        static_cast<const float *>(a.packed_scales),
+        static_cast<float *>(a.scales), nb, ns);
+  else
+    unpack_scales_kernel<uint16_t><<<grid_for(ns), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(a.packed_scales),
+        static_cast<uint16_t *>(a.scales), nb, ns);
+  if (a.packed_zp != nullptr) {
+    const int64_t nz = a.N * ((nb + 1) / 2);
+    unpack_zp_kernel<<<grid_for(nz), 256, 0, stream>>>(
+        static_cast<const uint64_t *>(a.packed_zp), a.zp, nb, nz);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mnb

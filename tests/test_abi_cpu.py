@@ -1,0 +1,118 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point include/mnb.h declares, and rejects invalid arguments on the host
+before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import int4_weight_only_matmulnbits_gb300 as mnb
+from int4_weight_only_matmulnbits_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mnb.build_library()
+    return mnb.load()
+
+
+def declared_entry_points():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"MNB_API\s+[\w\s\*]*?\b(mnb_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_binding_names():
+    assert declared_entry_points() == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(lib):
+    assert mnb.mnb_version() >> 16 == 1
+    for code in range(-9, 1):
+        assert mnb.status_string(code).startswith("MNB_")
+    assert "unknown" in mnb.status_string(42)
+
+
+@pytest.mark.parametrize("N,K,bs,zp", [(3072, 1024, 32, False), (7, 33, 16, True),
+                                       (151936, 2560, 128, False), (1, 1, 256, True)])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_prepacked_sizes(lib, N, K, bs, zp, dt):
+    b, s, z = mnb.mnb_prepacked_sizes(N, K, bs, dt, zp)
+    n16, k64, nb = -(-N // 16), -(-K // 64), -(-K // bs)
+    assert b == n16 * k64 * 512
+    assert s == n16 * nb * 16 * (4 if dt == torch.float32 else 2)
+    assert z == (n16 * nb * 8 if zp else 0)
+
+
+def test_packed_storage_within_bound_for_qwen_shapes(lib):
+    """Packed weights + scales + zero points stay within 1.25x the serialized
+    UINT4 codes + scales + zero points (page "Qwen3 CPU Inference Critical
+    Path", section "Benchmark gates", INT4 memory row)."""
+    from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_0P6B, QWEN3_4B
+    for model, bs, dt, zp in ((QWEN3_0P6B, 32, torch.float32, True),
+                              (QWEN3_4B, 128, torch.bfloat16, False)):
+        for p in model["projections"] + [model["lm_head"]]:
+            nb = -(-p.K // bs)
+            serial = p.N * nb * bs // 2 + p.N * nb * (4 if dt == torch.float32 else 2)
+            serial += p.N * ((nb + 1) // 2) if zp else 0
+            packed = sum(mnb.mnb_prepacked_sizes(p.N, p.K, bs, dt, zp))
+            assert packed <= 1.25 * serial, (p, packed / serial)
+
+
+def _call_matmul(lib, **kw):
+    args = dict(A=16, packed_b=256, scales=256, zp=None, bias=None, M=1, N=16, K=64,
+                bs=32, Y=1 << 20, a_t=0, s_t=0, path=0)
+    args.update(kw)
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.mnb_matmul_path(v(args["A"]), v(args["packed_b"]), v(args["scales"]),
+                               v(args["zp"]), v(args["bias"]), args["M"], args["N"],
+                               args["K"], args["bs"], v(args["Y"]), args["a_t"],
+                               args["s_t"], args["path"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(A=None), -1), (dict(packed_b=None), -1), (dict(scales=None), -1),
+    (dict(Y=None), -1), (dict(M=0), -2), (dict(N=0), -2), (dict(K=-1), -2),
+    (dict(M=1 << 31), -2), (dict(bs=0), -3), (dict(bs=48), -3), (dict(bs=512), -3),
+    (dict(bs=8), -3), (dict(a_t=7), -4), (dict(s_t=2), -4), (dict(packed_b=264), -5),
+    (dict(scales=260), -5), (dict(zp=1000), -5), (dict(A=17), -5), (dict(bias=2), -5),
+    (dict(path=9), -8), (dict(path=1, M=17), -8),
+    (dict(Y=16), -6), (dict(Y=300), -6),
+])
+def test_matmul_rejects_invalid_arguments_on_host(lib, kw, status):
+    assert _call_matmul(lib, **kw) == status
+
+
+def test_prepack_rejects_invalid_arguments_on_host(lib):
+    v = ctypes.c_void_p
+    ok = dict(B=v(4096), S=v(1 << 16), Z=None, N=16, K=64, bs=32, st=0,
+              pb=v(1 << 20), ps=v(1 << 21), pz=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.mnb_prepack(a["B"], a["S"], a["Z"], a["N"], a["K"], a["bs"], a["st"],
+                               a["pb"], a["ps"], a["pz"], None)
+    assert call(B=None) == -1
+    assert call(Z=v(8192), pz=None) == -1
+    assert call(N=0) == -2
+    assert call(bs=24) == -3
+    assert call(st=5) == -4
+    assert call(pb=v((1 << 20) + 8)) == -5
+    assert call(pb=v(4096 + 16)) == -6  # packed output overlaps B
+    assert call(ps=v((1 << 20) + 256)) == -6  # the two outputs overlap
+    assert lib.mnb_prepacked_sizes(16, 64, 32, 0, 0, None, None, None) == -1
