@@ -1,0 +1,392 @@
+"""Benchmark: INT4 weight-only MatMulNBits decode step on GB300.
+
+Workload: one batch-1 decode step of Qwen3-4B's projections (M = 1, bf16
+activations ~ N(0,1), block size 128, no zero points (8), bf16 scales
+U[0.002, 0.01]): q 2560->4096, k/v 2560->1024, o 4096->2560, gate/up
+2560->9728, down 9728->2560, for 36 layers, plus lm_head 2560->151936 —
+253 products and 2.08 GB of algorithmic bytes per step. Each projection has
+its own seeded weights and activation row; all are resident in HBM before
+timing. A step replays one CUDA graph of the 253 mnb_matmul launches. The
+step's bytes exceed the 129 MB L2 many times over, so no flush is needed.
+
+Also measured, outside the timed region of the headline number: the prefill
+GEMM at M = 2048 over the seven Qwen3-4B projection shapes (TFLOP/s), when
+the tensor-core path is available.
+
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload instead (there is no runnable reference implementation of this
+operator; the oracle is the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT4 decode GEMV GB/s and % HBM peak (M=1); prefill TFLOP/s (M=2048)"
+WORKLOAD = "Qwen3-4B decode step projections, M=1, bf16 A, bs 128, no zp"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        self.out = (os.path.join(out_dir, f"clocks_gpu{gpu_index}.csv")
+                    if os.path.isdir(out_dir) else f"/tmp/mnb_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.out) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle leg
+# ----------------------------------------------------------------------------
+
+def oracle_sample(budget_s: float, seed_base: int = 3000):
+    """Times the oracle (single thread) over the decode step's projections in
+    order until about budget_s seconds of CPU work; returns (bytes, seconds,
+    description)."""
+    import torch
+
+    import oracle
+    from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_4B, make_problem
+    oracle.load()
+    projs = [(l, p) for l in range(QWEN3_4B["layers"]) for p in QWEN3_4B["projections"]]
+    done_bytes, spent, names = 0, 0.0, []
+    for i, (layer, p) in enumerate(projs):
+        prob = make_problem(1, p.N, p.K, 128, dtype=torch.bfloat16, seed=seed_base + i,
+                            scale_range=(0.002, 0.01))
+        t0 = time.perf_counter()
+        oracle.matmulnbits(prob.A, prob.B, prob.scales, None, None, N=p.N, K=p.K,
+                           block_size=128)
+        spent += time.perf_counter() - t0
+        done_bytes += prob.algorithmic_bytes()
+        names.append(f"L{layer}.{p.name}")
+        if spent >= budget_s:
+            break
+    desc = (f"first {len(names)} projections of the decode step ({names[0]}..{names[-1]}, "
+            f"{done_bytes / 1e6:.1f} MB algorithmic), oracle single-threaded")
+    return done_bytes, spent, desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    desc = ""
+    for _ in range(args.warmup):
+        oracle_sample(args.ref_budget / 8)
+    nbytes_total, t_total = 0, 0.0
+    for _ in range(args.steps):
+        nbytes, t, desc = oracle_sample(args.ref_budget)
+        nbytes_total += nbytes
+        t_total += t
+    gbs = nbytes_total / t_total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD + " (bounded sample per step)", "M": 1,
+                   "block_size": 128, "a_dtype": "bf16"},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU leg
+# ----------------------------------------------------------------------------
+
+def build_decode_step(dev, seed_base=5000):
+    """Prepacked weights, activations and outputs of one decode step, all
+    resident on dev. Weights are drawn on the device from a seeded generator
+    (2 GB would take minutes on the host)."""
+    import torch
+
+    import int4_weight_only_matmulnbits_gb300 as mnb
+    from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_4B
+    projs = [(f"L{l}.{p.name}", p) for l in range(QWEN3_4B["layers"])
+             for p in QWEN3_4B["projections"]]
+    projs.append(("lm_head", QWEN3_4B["lm_head"]))
+    bs = 128
+    g = torch.Generator(device=dev)
+    items = []
+    a_total = sum(p.K for _, p in projs)
+    y_total = sum(p.N for _, p in projs)
+    A_all = torch.empty(a_total, dtype=torch.bfloat16, device=dev)
+    Y_all = torch.empty(y_total, dtype=torch.bfloat16, device=dev)
+    ao = yo = 0
+    algo_bytes = 0
+    for i, (name, p) in enumerate(projs):
+        g.manual_seed(seed_base + i)
+        nb = -(-p.K // bs)
+        B = torch.randint(0, 256, (p.N, nb, bs // 2), dtype=torch.uint8, device=dev,
+                          generator=g)
+        S = (torch.rand(p.N, nb, device=dev, generator=g) * 0.008 + 0.002).to(torch.bfloat16)
+        A = A_all[ao:ao + p.K].view(1, p.K)
+        A.copy_(torch.randn(1, p.K, device=dev, generator=g).to(torch.bfloat16))
+        Y = Y_all[yo:yo + p.N].view(1, p.N)
+        w = mnb.mnb_prepack(B, S, None, p.N, p.K, bs)
+        del B, S
+        items.append((name, p, w, A, Y))
+        ao += p.K
+        yo += p.N
+        algo_bytes += p.N * nb * bs // 2 + p.N * nb * 2 + p.K * 2 + p.N * 2
+    torch.cuda.synchronize()
+    return items, A_all, Y_all, algo_bytes
+
+
+def time_region(fn, steps, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def prefill_measure(dev, steps=5, warmup=3):
+    """TFLOP/s of the tensor-core path at M=2048 over the seven Qwen3-4B
+    projection shapes (bf16 A, bs 128, zero points, bias), each timed alone;
+    None when the path is not available."""
+    import torch
+
+    import int4_weight_only_matmulnbits_gb300 as mnb
+    from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_4B
+    M, bs = 2048, 128
+    g = torch.Generator(device=dev)
+    total_flops, total_s, per = 0, 0.0, {}
+    stream = torch.cuda.current_stream()
+    for i, p in enumerate(QWEN3_4B["projections"]):
+        g.manual_seed(9000 + i)
+        nb = -(-p.K // bs)
+        B = torch.randint(0, 256, (p.N, nb, bs // 2), dtype=torch.uint8, device=dev, generator=g)
+        S = (torch.rand(p.N, nb, device=dev, generator=g) * 0.008 + 0.002).to(torch.bfloat16)
+        Z = torch.randint(0, 256, (p.N, (nb + 1) // 2), dtype=torch.uint8, device=dev,
+                          generator=g)
+        bias = torch.randn(p.N, device=dev, generator=g) * 0.02
+        A = torch.randn(M, p.K, device=dev, generator=g).to(torch.bfloat16)
+        w = mnb.mnb_prepack(B, S, Z, p.N, p.K, bs)
+        Y = torch.empty(M, p.N, dtype=torch.bfloat16, device=dev)
+        try:
+            mnb.mnb_matmul(A, w, bias, out=Y, path="gemm")
+        except mnb.MnbError as e:
+            if e.status == -8:
+                return None
+            raise
+        for _ in range(warmup):
+            mnb.mnb_matmul(A, w, bias, out=Y, path="gemm")
+        t = time_region(lambda: mnb.mnb_matmul(A, w, bias, out=Y, path="gemm"), steps, stream)
+        flops = 2 * M * p.N * p.K * steps
+        per[p.name] = flops / t / 1e12
+        total_flops += flops
+        total_s += t
+    return {"value": total_flops / total_s / 1e12, "unit": "TFLOP/s", "M": M,
+            "per_projection_tflops": per}
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+
+    import int4_weight_only_matmulnbits_gb300 as mnb
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mnb.build_library()
+    mnb.load()
+    hbm_peak, _, _, peak_kind = peaks()
+
+    items, A_all, Y_all, algo_bytes = build_decode_step(dev)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step_eager():
+        for _, p, w, A, Y in items:
+            mnb.mnb_matmul(A, w, None, out=Y)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step_eager()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_eager()
+    torch.cuda.synchronize()
+    launches_per_step = len(items)
+
+    warmup = max(args.warmup, 3)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t = time_region(graph.replay, args.steps, torch.cuda.current_stream())
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    # end to end: host activations in, host results out, every step
+    A_host = torch.empty(A_all.shape, dtype=A_all.dtype).pin_memory()
+    A_host.copy_(A_all.cpu())
+    Y_host = torch.empty(Y_all.shape, dtype=Y_all.dtype).pin_memory()
+    cur = torch.cuda.current_stream()
+
+    def step_e2e():
+        A_all.copy_(A_host, non_blocking=True)
+        graph.replay()
+        Y_host.copy_(Y_all, non_blocking=True)
+
+    for _ in range(3):
+        step_e2e()
+    t_e2e = time_region(step_e2e, args.steps, cur)
+
+    ts = torch.tensor([t, t_e2e], device=dev, dtype=torch.float64)
+    if dist:
+        dist.all_reduce(ts, op=dist.ReduceOp.MAX)
+    t, t_e2e = ts.tolist()
+
+    if rank != 0:
+        return
+    value = algo_bytes * args.steps * world / t / 1e9
+    e2e = algo_bytes * args.steps * world / t_e2e / 1e9
+    per_gpu = algo_bytes * args.steps / t / 1e9
+
+    prefill = None if args.skip_prefill else prefill_measure(dev)
+    cpu = None
+    if world == 1 and not args.skip_cpu:
+        nbytes, secs, desc = oracle_sample(args.cpu_budget)
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup,
+        "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "block_size": 128, "a_dtype": "bf16",
+                   "projections_per_step": launches_per_step,
+                   "algorithmic_bytes_per_step": algo_bytes,
+                   "l2": "inputs larger than L2 (2.08 GB per step vs 129 MB)",
+                   "launch": "one CUDA graph of 253 launches, programmatic dependent launch",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_fraction": per_gpu / hbm_peak,
+        "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": per_gpu / hbm_peak, "traffic": None,
+                     "peak_kind": peak_kind,
+                     "kernel": "gemv_kernel (every launch of the step)"},
+        "e2e": {"value": e2e, "unit": "GB/s",
+                "h2d_bytes_per_step": A_all.numel() * A_all.element_size(),
+                "d2h_bytes_per_step": Y_all.numel() * Y_all.element_size()},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "prefill": prefill,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=8.0)
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    rank = int(os.environ.get("RANK", 0))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group(backend)
+        dist = tdist
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, dist)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
