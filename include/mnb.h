@@ -81,7 +81,8 @@ MNB_API int mnb_version(void);
  * the selected kernel). HOST outputs; zp_bytes is 0 when has_zero_points is
  * 0. The packed layout pads N up to a multiple of 16 and K up to a multiple
  * of 64 with zero codes; for N % 16 == 0 and K % 64 == 0 the packed codes
- * take exactly the N*K/2 bytes of the input.
+ * take exactly the N*K/2 bytes of the input. Zero points take 4 bits per
+ * (row, block), with rows padded to 16 and blocks to an even count.
  * Errors: MNB_ERR_NULL (an output pointer), MNB_ERR_SHAPE (N or K < 1),
  * MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE.
  */
@@ -171,6 +172,32 @@ MNB_API mnb_status mnb_matmul_path(const void *A, const void *packed_b,
                                    mnb_path path, mnb_stream_t stream);
 
 /*
+ * Fused-N projections: Y_i = A * dequant(B_i)^T + bias_i for i < count
+ * (1 <= count <= 4), for weights that read the same activations, such as
+ * the q/k/v or the gate/up projections of a decoder layer (page "Qwen3 CPU
+ * Inference Critical Path", section "Exact kernel inventory": the artifact's
+ * fused 1024x4096 QKV projection and its Split row; section "Phase Q5":
+ * fusions that remove measured memory traffic). One launch streams every
+ * weight of the group; A is read once.
+ *  packed_b, scales, zero_points, bias, N, Y: HOST arrays of count entries
+ *  (device pointers inside, except N). zero_points is NULL or holds count
+ *  entries that are all NULL or all non-NULL; bias may be NULL or hold NULL
+ *  entries. Every weight shares K, block_size and the dtypes.
+ * M <= 16 runs the decode kernel once for the whole group; larger M runs
+ * one product per weight. Errors: as mnb_matmul, for every entry; Y_i must
+ * not overlap any input or any other output.
+ */
+MNB_API mnb_status mnb_matmul_grouped(const void *A, int count,
+                                      const void *const *packed_b,
+                                      const void *const *scales,
+                                      const void *const *zero_points,
+                                      const float *const *bias,
+                                      const int64_t *N, void *const *Y,
+                                      int64_t M, int64_t K, int block_size,
+                                      mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                      mnb_stream_t stream);
+
+/*
  * mnb_matmul for callers whose activations and results live in HOST memory:
  * copies A_host [M, K] into the caller's device buffer A_dev, runs the
  * product into Y_dev, and copies Y_dev back into Y_host [M, N], all
@@ -201,6 +228,17 @@ MNB_API mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,
  * Process-wide setting.
  */
 MNB_API void mnb_set_programmatic_launch(int enable);
+
+/*
+ * Failure detection. Every wait inside a kernel (on a bulk copy's mbarrier)
+ * has an iteration cap far above any legitimate wait; a kernel whose wait
+ * runs out records a bit in a device fault word, abandons its tile and
+ * exits instead of hanging. This call waits for the current device to be
+ * idle, returns the fault bits seen since the last call in *fault_bits
+ * (HOST; 0 = none; 1 = decode kernel, 2 = tensor-core kernel) and clears
+ * them. Errors: MNB_ERR_NULL, MNB_ERR_CUDA.
+ */
+MNB_API mnb_status mnb_fault_status(unsigned int *fault_bits);
 
 #ifdef __cplusplus
 }

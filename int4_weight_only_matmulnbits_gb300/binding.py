@@ -24,7 +24,7 @@ MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_prepacked_sizes", "mnb_prepack", "mnb_unprepack", "mnb_matmul",
            "mnb_matmul_path", "mnb_matmul_from_host",
-           "mnb_set_programmatic_launch")
+           "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +82,11 @@ def load(build_if_missing: bool = False):
         lib.mnb_matmul_from_host.restype = i32
         lib.mnb_set_programmatic_launch.argtypes = [i32]
         lib.mnb_set_programmatic_launch.restype = None
+        lib.mnb_matmul_grouped.argtypes = [p, i32, p, p, p, p, p, p, i64, i64, i32,
+                                           i32, i32, p]
+        lib.mnb_matmul_grouped.restype = i32
+        lib.mnb_fault_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.mnb_fault_status.restype = i32
         _lib = lib
         return lib
 
@@ -136,6 +141,13 @@ def mnb_version() -> int:
 
 def mnb_set_programmatic_launch(enable: bool) -> None:
     load().mnb_set_programmatic_launch(1 if enable else 0)
+
+
+def mnb_fault_status() -> int:
+    """Fault bits recorded by kernels whose bounded waits ran out (cleared)."""
+    v = ctypes.c_uint()
+    _check(load().mnb_fault_status(ctypes.byref(v)), "mnb_fault_status")
+    return v.value
 
 
 def mnb_prepacked_sizes(N: int, K: int, block_size: int, scale_dtype: torch.dtype,
@@ -214,3 +226,30 @@ def mnb_matmul_from_host(A_host: torch.Tensor, A_dev: torch.Tensor, w: PackedWei
         _ptr(Y_host), _dtype_code(A_host.dtype), _dtype_code(w.scale_dtype),
         _stream(stream)), "mnb_matmul_from_host")
     return Y_host
+
+
+def mnb_matmul_grouped(A: torch.Tensor, ws: list[PackedWeight],
+                       biases: list[torch.Tensor | None] | None = None, *,
+                       outs: list[torch.Tensor] | None = None,
+                       stream=None) -> list[torch.Tensor]:
+    """Fused-N projections: [A @ dequant(w)^T + b for w, b in zip(ws, biases)]."""
+    n = len(ws)
+    if A.dim() != 2 or not A.is_cuda or not A.is_contiguous():
+        raise ValueError("A must be a contiguous 2-D CUDA tensor")
+    M, K = A.shape
+    if any(w.K != K or w.block_size != ws[0].block_size or
+           w.scale_dtype != ws[0].scale_dtype for w in ws):
+        raise ValueError("grouped weights must share K, block size and scale dtype")
+    if outs is None:
+        outs = [torch.empty(M, w.N, dtype=A.dtype, device=A.device) for w in ws]
+    biases = biases or [None] * n
+    VP = ctypes.c_void_p * n
+    vp = lambda ts: VP(*[None if t is None else t.data_ptr() for t in ts])
+    zps = [w.packed_zp for w in ws]
+    _check(load().mnb_matmul_grouped(
+        _ptr(A), n, vp([w.packed_b for w in ws]), vp([w.packed_scales for w in ws]),
+        None if zps[0] is None else vp(zps), vp(biases),
+        (ctypes.c_int64 * n)(*[w.N for w in ws]), vp(outs), M, K, ws[0].block_size,
+        _dtype_code(A.dtype), _dtype_code(ws[0].scale_dtype), _stream(stream)),
+        "mnb_matmul_grouped")
+    return outs

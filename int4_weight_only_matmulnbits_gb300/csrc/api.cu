@@ -52,7 +52,7 @@ Sizes packed_sizes(int64_t N, int64_t K, int bs, int scale_dtype, bool zp) {
   Sizes s;
   s.b = size_t(N16) * K64 * kChunkBytes;
   s.s = size_t(N16) * nb * kTileN * dtype_size(scale_dtype);
-  s.z = zp ? size_t(N16) * nb * 8 : 0;
+  s.z = zp ? size_t(N16) * ceil_div(nb, 2) * 2 * 8 : 0;
   return s;
 }
 
@@ -190,6 +190,17 @@ int mnb_version(void) { return (1 << 16) | 0; }
 
 void mnb_set_programmatic_launch(int enable) { g_pdl.store(enable ? 1 : 0); }
 
+mnb_status mnb_fault_status(unsigned int *fault_bits) {
+  if (!fault_bits) return MNB_ERR_NULL;
+  unsigned int a = 0, b = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = gemv_take_fault(&a);
+  if (e == cudaSuccess) e = gemm_take_fault(&b);
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_fault_status");
+  *fault_bits = a | b;
+  return MNB_OK;
+}
+
 mnb_status mnb_prepacked_sizes(int64_t N, int64_t K, int block_size,
                                mnb_dtype scale_dtype, int has_zero_points,
                                size_t *packed_b_bytes,
@@ -293,6 +304,77 @@ mnb_status mnb_matmul(const void *A, const void *packed_b, const void *scales,
   return mnb_matmul_path(A, packed_b, scales, zero_points, bias, M, N, K,
                          block_size, Y, a_dtype, scale_dtype, MNB_PATH_AUTO,
                          stream);
+}
+
+mnb_status mnb_matmul_grouped(const void *A, int count,
+                              const void *const *packed_b,
+                              const void *const *scales,
+                              const void *const *zero_points,
+                              const float *const *bias, const int64_t *N,
+                              void *const *Y, int64_t M, int64_t K,
+                              int block_size, mnb_dtype a_dtype,
+                              mnb_dtype scale_dtype, mnb_stream_t stream) {
+  if (!packed_b || !scales || !N || !Y) return MNB_ERR_NULL;
+  if (count < 1 || count > kMaxGroup) return MNB_ERR_SHAPE;
+  const bool has_zp = zero_points && zero_points[0];
+  for (int i = 0; i < count; ++i) {
+    if (zero_points && ((zero_points[i] != nullptr) != has_zp)) return MNB_ERR_NULL;
+    const mnb_status st = validate_matmul(
+        A, packed_b[i], scales[i], has_zp ? zero_points[i] : nullptr,
+        bias ? bias[i] : nullptr, M, N[i], K, block_size, Y[i], a_dtype,
+        scale_dtype, MNB_PATH_AUTO);
+    if (st != MNB_OK) return st;
+    const size_t es = dtype_size(a_dtype);
+    for (int j = 0; j < count; ++j) {
+      if (j == i) continue;
+      const Sizes in = packed_sizes(N[j], K, block_size, scale_dtype, has_zp);
+      const void *others[5] = {packed_b[j], scales[j], has_zp ? zero_points[j] : nullptr,
+                               bias ? bias[j] : nullptr, Y[j]};
+      const size_t on[5] = {in.b, in.s, in.z, (bias && bias[j]) ? size_t(N[j]) * 4 : 0,
+                            size_t(M) * N[j] * es};
+      for (int k = 0; k < 5; ++k)
+        if (overlap(Y[i], size_t(M) * N[i] * es, others[k], on[k])) return MNB_ERR_ALIAS;
+    }
+  }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M > kGemvMaxM) {
+    for (int i = 0; i < count; ++i) {
+      const mnb_status st = run_matmul(A, packed_b[i], scales[i],
+                                       has_zp ? zero_points[i] : nullptr,
+                                       bias ? bias[i] : nullptr, M, N[i], K,
+                                       block_size, Y[i], a_dtype, scale_dtype,
+                                       MNB_PATH_AUTO, s);
+      if (st != MNB_OK) return st;
+    }
+    return MNB_OK;
+  }
+  GroupArgs g{};
+  g.A = A;
+  g.count = count;
+  for (int i = 0; i < count; ++i) {
+    g.packed_b[i] = packed_b[i];
+    g.scales[i] = scales[i];
+    g.zp[i] = has_zp ? zero_points[i] : nullptr;
+    g.bias[i] = bias ? bias[i] : nullptr;
+    g.Y[i] = Y[i];
+    g.N[i] = N[i];
+  }
+  g.M = M;
+  g.K = K;
+  g.bs = block_size;
+  g.a_f32 = a_dtype == MNB_F32;
+  g.scale_f32 = scale_dtype == MNB_F32;
+  g.has_zp = has_zp;
+  g.pdl = g_pdl.load() != 0;
+  const cudaError_t e = launch_gemv_group(g, s);
+  if (e == cudaErrorNotSupported) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "no grouped kernel for M=%lld K=%lld bs=%d", (long long)M,
+                  (long long)K, block_size);
+    return MNB_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_grouped");
+  return MNB_OK;
 }
 
 mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,

@@ -1,66 +1,104 @@
 // Small-M (decode) MatMulNBits kernel for sm_103a.
 //
 // Computes Y[m,n] = sum_k A[m,k] (q[n,k] - z[n,b]) s[n,b] + bias[n] for
-// M <= 16 on the prepacked layout of mnb_common.cuh. It follows the page
-// "Qwen3 CPU Inference Critical Path", section "Prepared weight-only plan":
-// weights stay compressed, are unpacked in registers, zero points and scales
-// are applied per block and accumulation is fp32; int4_gemv streams every
-// weight byte once, partitioned over output channels, and int4_small_m reuses
-// the unpacked codes across a few activation rows.
+// M <= 16 on the prepacked layout of mnb_common.cuh, for one weight or for a
+// group of weights that share the same activations (fused-N projections such
+// as q/k/v or gate/up). It follows the page "Qwen3 CPU Inference Critical
+// Path", section "Prepared weight-only plan": weights stay compressed, are
+// unpacked in registers, zero points and scales are applied per block and
+// accumulation is fp32; int4_gemv streams every weight byte once,
+// partitioned over output channels, and int4_small_m reuses the unpacked
+// codes across a few activation rows.
 //
 // GB300 mapping:
-//  * A warp owns one 16-row tile and a contiguous range of <= 8 64-wide k
-//    chunks. It issues all its 128-bit weight loads at once, before waiting
-//    on the upstream kernel (the weights are constant), so each launch puts
-//    its whole weight stream in flight immediately.
-//  * Codes become bf16 (128 + q) with one lop3 per pair and feed
-//    mma.m16n8k16 as the 16-row operand, with the activations (8 rows per
-//    MMA) as the 8-column operand. Products and sums are exact up to fp32
-//    accumulation; no per-weight subtract or multiply is needed.
+//  * Warp-specialised, persistent CTAs: 16 consumer warps and one producer
+//    warp. Output rows form 16-row tiles; a CTA works on a tile group of
+//    `tpc` tiles, each consumer warp owning one tile and one of `ksw`
+//    interleaved k slices (chunk j*ksw + ks of the CTA's k range; a cluster
+//    of CTAs splits K further). CTAs walk the tile groups with a fixed
+//    stride.
+//  * Per pipeline stage the producer moves the next ksw chunks of all tpc
+//    tiles with one 3-D TMA tensor copy (8 KB), plus one copy each for their
+//    scales and zero points, into a ring of shared-memory stages guarded by
+//    full/empty mbarriers. TMA zero fill covers ragged N, K and blocks.
+//    The weights are constant, so the producer starts before the upstream
+//    kernel has finished, and the kernel lets its own dependents launch at
+//    once: consecutive launches overlap their weight streams.
+//  * Activations are staged once per CTA in shared memory as bf16 (fp32
+//    activations as a pair hi + lo exact to 2^-16). Codes become bf16
+//    128 + q (exact) with one lop3 per pair; they feed mma.m16n8k16 as the
+//    16-row operand, the activations (8 rows per MMA) as the 8-column
+//    operand: no per-weight zero-point or scale arithmetic.
 //  * Per block (or block piece) the fp32 correction
-//      acc += s * (D - (128 + z) * S),   S = sum of the block's activations,
-//    applies zero point and scale. fp32 activations are split into bf16
-//    hi + lo (two MMAs), and S is summed from hi + lo so the offset cancels.
-//  * Split-K partials are reduced in fixed order: warps of a CTA through
-//    shared memory, CTAs of a cluster through distributed shared memory.
-//    No global workspace, no atomics: results are bitwise reproducible.
+//      acc += s * (D - (128 + z) * S),   S = sum of the block's staged
+//    activations, applies zero point and scale.
+//  * Split-K partials are reduced in fixed order: consumer warps of a CTA
+//    through shared memory, CTAs of a cluster through distributed shared
+//    memory; a warp that owns all of K stores its tile directly. No global
+//    workspace, no atomics on results: outputs are bitwise reproducible.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "mnb_common.cuh"
 #include "mnb_launch.h"
 
 namespace mnb {
+
+__device__ unsigned int g_fault_gemv = 0;
+
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxChunks = 8;  // k chunks per warp (registers: 4 per chunk)
-constexpr int kSmemLimit = 160 * 1024;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kBarConsumers = 1;           // named barrier id for consumers
+// Shared memory per CTA small enough that a CTA of the next launch fits
+// beside a running one on the same SM.
+constexpr int kSmemBudget = 112 * 1024;
+constexpr int kMaxStages = 8;
 
 struct GemvParams {
+  CUtensorMap tmw[kMaxGroup];  // codes: {128 words, K64 chunks, N16 tiles}
+  CUtensorMap tms[kMaxGroup];  // scales: {16 scales as words, nb, N16}
+  CUtensorMap tmz[kMaxGroup];  // zero points: {4 words, nbz/2 pairs, N16}
   const void *A;
-  const uint4 *wq;
-  const void *scales;
-  const uint2 *zp;
-  const float *bias;
-  void *Y;
-  int M, N, K;
-  int K64, N16, nb;
-  int bs, bs_log2;
-  int scale_f32, has_zp;
-  int ksplit, tiles_per_cta, cluster, KS;
-  int a_vec;
-  int krp;      // row stride (elements) of the staged activations
-  int sg;       // activation-sum granules per staged row
-  int granule;  // min(bs, 64)
-  int nbr;      // block slots per tile in the staged scales
-  int off_alo, off_s, off_sc, off_zp, off_red, off_part;
+  const float *bias[kMaxGroup];
+  void *Y[kMaxGroup];
+  int N[kMaxGroup], N16[kMaxGroup], tg_begin[kMaxGroup];
+  int nprob, tg_total;
+  int M, K, K64, nb;
+  int a_f32, a_vec;
+  int ksw, tpc, cluster, R;  // k ranges per CTA, tiles per group, chunks per range
+  int krp, sg;               // staged activation row stride, granules per row
+  int nst, stage_bytes, stage_tx;  // ring depth, stage stride, bytes per stage
+  int st_sc, st_zp;  // offsets of scales and zero points in a stage (128-aligned)
+  int nbs, nps;      // blocks and zero-point word pairs per stage and tile
+  int off_alo, off_s, off_red, off_part, off_bar, off_ring;
 };
 
-template <bool AF32>
+template <int BS>
+struct BlockGeom {
+  static constexpr int kLog2 = BS == 16 ? 4 : BS == 32 ? 5 : BS == 64 ? 6 : BS == 128 ? 7 : 8;
+  static constexpr int kGranule = BS < kChunkK ? BS : kChunkK;
+  static constexpr int kChunksPerBlock = BS > kChunkK ? BS / kChunkK : 1;
+  static constexpr int kBlocksPerChunk = BS < kChunkK ? kChunkK / BS : 1;
+  static constexpr int kChunkShift = kLog2 > 6 ? kLog2 - 6 : 0;  // chunk -> block
+};
+
+// Problem of global tile group gi (the group table is tiny: linear scan).
+__device__ __forceinline__ int problem_of(const GemvParams &p, int gi) {
+  int q = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxGroup; ++i)
+    if (i < p.nprob && gi >= p.tg_begin[i]) q = i;
+  return q;
+}
+
+// Eight activations A[m][k..k+7] as fp32 (zeros past K).
 __device__ __forceinline__ void load8(const GemvParams &p, int m, int64_t k,
                                       float (&v)[8]) {
-  if (AF32) {
+  if (p.a_f32) {
     const float *a = static_cast<const float *>(p.A) + (int64_t)m * p.K;
     if (p.a_vec && k + 8 <= p.K) {
       const float4 x = *reinterpret_cast<const float4 *>(a + k);
@@ -89,330 +127,434 @@ __device__ __forceinline__ void load8(const GemvParams &p, int m, int64_t k,
   }
 }
 
-template <int MT, bool AF32>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint16_t *sAhi = reinterpret_cast<uint16_t *>(smem);
+// Y[m][n] = v + bias[n], in A's dtype (bf16 rounded to nearest even).
+__device__ __forceinline__ void store_y(const GemvParams &p, int q, int m, int n,
+                                        float v) {
+  if (p.bias[q]) v += __ldg(p.bias[q] + n);
+  if (p.a_f32)
+    static_cast<float *>(p.Y[q])[(int64_t)m * p.N[q] + n] = v;
+  else
+    static_cast<uint16_t *>(p.Y[q])[(int64_t)m * p.N[q] + n] =
+        static_cast<uint16_t>(bf16_bits(v));
+}
+
+template <int MT, int BS, bool HAS_ZP, bool SF32>
+__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
+    gemv_kernel(const __grid_constant__ GemvParams p) {
+  using G = BlockGeom<BS>;
+  constexpr int kEs = SF32 ? 4 : 2;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint16_t *sA = reinterpret_cast<uint16_t *>(smem);
   uint16_t *sAlo = reinterpret_cast<uint16_t *>(smem + p.off_alo);
   float *sS = reinterpret_cast<float *>(smem + p.off_s);
-  unsigned char *sSc = smem + p.off_sc;
-  uint2 *sZp = reinterpret_cast<uint2 *>(smem + p.off_zp);
   float *sRed = reinterpret_cast<float *>(smem + p.off_red);
   float *sPart = reinterpret_cast<float *>(smem + p.off_part);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+  uint64_t *empty = full + kMaxStages;
+  unsigned char *ring = smem + p.off_ring;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
   const int crank = static_cast<int>(blockIdx.x) % p.cluster;
-  const int tgroup = static_cast<int>(blockIdx.x) / p.cluster;
-  const int tau = warp / p.ksplit, ks = warp - tau * p.ksplit;
-  const int tile = tgroup * p.tiles_per_cta + tau;
-  const bool tile_ok = tile < p.N16;
-  const int kidx = crank * p.ksplit + ks;
-  const int c0 = static_cast<int>((int64_t)kidx * p.K64 / p.KS);
-  const int c1 = static_cast<int>((int64_t)(kidx + 1) * p.K64 / p.KS);
-  const int clo = static_cast<int>((int64_t)crank * p.K64 / p.cluster);
-  const int chi = static_cast<int>((int64_t)(crank + 1) * p.K64 / p.cluster);
-  const int blo = (clo * kChunkK) >> p.bs_log2;
-  const int bhi = min(p.nb, (chi * kChunkK + p.bs - 1) >> p.bs_log2);
+  const int gstride = static_cast<int>(gridDim.x) / p.cluster;
+  const int gfirst = static_cast<int>(blockIdx.x) / p.cluster;
+  const int clo = crank * p.ksw * p.R;  // first chunk of this CTA's k range
 
-  // 1. The warp's whole constant weight stream goes in flight first.
-  uint4 wreg[kMaxChunks];
-  {
-    const uint4 *src = p.wq + ((int64_t)tile * p.K64 + c0) * 32 + lane;
-#pragma unroll
-    for (int i = 0; i < kMaxChunks; ++i)
-      wreg[i] = (tile_ok && c0 + i < c1) ? ldg_stream(src + i * 32)
-                                         : make_uint4(0, 0, 0, 0);
-  }
-
-  // 2. Scales and zero points of the CTA's tiles over its block range.
-  {
-    const int nbl = bhi - blo;
-    const int per_tile = nbl * kTileN;
-    const int total = p.tiles_per_cta * per_tile;
-    for (int i = tid; i < total; i += kThreads) {
-      const int tt = i / per_tile, e = i - tt * per_tile;
-      const int tl = tgroup * p.tiles_per_cta + tt;
-      if (tl >= p.N16) continue;
-      const int64_t src = ((int64_t)tl * p.nb + blo) * kTileN + e;
-      const int dst = tt * p.nbr * kTileN + e;
-      if (p.scale_f32)
-        reinterpret_cast<float *>(sSc)[dst] =
-            __ldg(static_cast<const float *>(p.scales) + src);
-      else
-        reinterpret_cast<uint16_t *>(sSc)[dst] =
-            __ldg(static_cast<const uint16_t *>(p.scales) + src);
+  if (tid == 0) {
+    for (int i = 0; i < p.nst; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kConsumerWarps);
     }
-    if (p.has_zp) {
-      const int totz = p.tiles_per_cta * nbl;
-      for (int i = tid; i < totz; i += kThreads) {
-        const int tt = i / nbl, e = i - tt * nbl;
-        const int tl = tgroup * p.tiles_per_cta + tt;
-        if (tl < p.N16)
-          sZp[tt * p.nbr + e] = __ldg(p.zp + (int64_t)tl * p.nb + blo + e);
-      }
-    }
-  }
-
-  // 3. From here on the upstream kernel's results (A) are visible.
-  grid_dependency_wait();
-
-  // 4. Stage A rows [0, M) over the CTA's k range as bf16 (hi, lo) and the
-  //    activation sum of every granule (block, or 64-wide piece of a block).
-  {
-    const int kr = (chi - clo) * kChunkK;
-    const int ppr = kr >> 3;  // 8-element pieces per row
-    const int total = p.M * ppr;
-    const int gp = p.granule >> 3;
-    for (int base = 0; base < total; base += kThreads) {
-      const int pc = base + tid;
-      const bool ok = pc < total;
-      float part = 0.f;
-      int m = 0, kp = 0;
-      if (ok) {
-        m = pc / ppr;
-        kp = pc - m * ppr;
-        float v[8];
-        load8<AF32>(p, m, (int64_t)clo * kChunkK + kp * 8, v);
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t h0 = bf16_bits(v[2 * q]), h1 = bf16_bits(v[2 * q + 1]);
-          hi[q] = h0 | (h1 << 16);
-          if (AF32) {
-            const float r0 = v[2 * q] - bf16_bits_to_f32(h0);
-            const float r1 = v[2 * q + 1] - bf16_bits_to_f32(h1);
-            const uint32_t l0 = bf16_bits(r0), l1 = bf16_bits(r1);
-            lo[q] = l0 | (l1 << 16);
-            part += (bf16_bits_to_f32(h0) + bf16_bits_to_f32(l0)) +
-                    (bf16_bits_to_f32(h1) + bf16_bits_to_f32(l1));
-          } else {
-            part += v[2 * q] + v[2 * q + 1];
-          }
-        }
-        const int off = m * p.krp + kp * 8;
-        *reinterpret_cast<uint4 *>(sAhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if (AF32)
-          *reinterpret_cast<uint4 *>(sAlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-      for (int o = 1; o < gp; o <<= 1)
-        part += __shfl_xor_sync(0xffffffffu, part, o);
-      if (ok && (kp % gp) == 0) sS[m * p.sg + kp / gp] = part;
-    }
+    fence_barrier_init();
   }
   __syncthreads();
+  // Dependents may launch now: before waiting on this grid they only touch
+  // their own constant weights.
   grid_dependents_launch();
 
-  // 5. Convert, multiply and correct per block.
-  float acc[MT][4], d[MT][4], srun[MT][2];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) acc[mt][q] = d[mt][q] = 0.f;
-    srun[mt][0] = srun[mt][1] = 0.f;
-  }
-  if (tile_ok) {
-    const bool big_blocks = p.bs >= kChunkK;
-    const int spb_mask = (p.bs >> 4) - 1;
-#pragma unroll
-    for (int i = 0; i < kMaxChunks; ++i) {
-      const int c = c0 + i;
-      if (c < c1) {
-        const int cl = c - clo;
-        if (big_blocks) {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int m0 = mt * 8 + 2 * t;
-            if (m0 < p.M) srun[mt][0] += sS[m0 * p.sg + cl];
-            if (m0 + 1 < p.M) srun[mt][1] += sS[(m0 + 1) * p.sg + cl];
-          }
+  if (warp == kConsumerWarps) {
+    // ---- producer: one stage per chunk step of the tile group ----------------
+    // The whole warp runs the loop (converged, as cluster barriers need);
+    // lane 0 issues. In cluster mode the producer joins the two cluster
+    // barriers of each tile group right after issuing its last stage, and
+    // only then prefetches the next group, so it never waits on a slot that
+    // only a later group would free.
+    // Ring position: slot, its use count parity, and whether it was used.
+    int slot = 0;
+    uint32_t phase = 0;
+    bool wrapped = false;
+    bool ok = true;
+    for (int u = 0;; ++u) {
+      const int gi = gfirst + u * gstride;
+      if (gi >= p.tg_total) break;
+      const int q = problem_of(p, gi);
+      const int tile0 = (gi - p.tg_begin[q]) * p.tpc;
+      for (int j = 0; j < p.R && ok; ++j) {
+        if (wrapped && !mbar_wait(empty + slot, phase ^ 1)) {
+          if (lane == 0) record_fault(&g_fault_gemv, kFaultGemvWait);
+          ok = false;
+          break;
         }
-        const uint32_t wv[4] = {wreg[i].x, wreg[i].y, wreg[i].z, wreg[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t wf[4];
-          codes_to_bf16x2(wv[j], wf);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int m = mt * 8 + g;
-            uint2 bh = make_uint2(0, 0), bl = make_uint2(0, 0);
-            if (m < p.M) {
-              const int off = m * p.krp + cl * kChunkK + 16 * j + 4 * t;
-              bh = *reinterpret_cast<const uint2 *>(sAhi + off);
-              if (AF32) bl = *reinterpret_cast<const uint2 *>(sAlo + off);
-            }
-            mma_bf16_16816(d[mt], wf, bh.x, bh.y);
-            if (AF32) mma_bf16_16816(d[mt], wf, bl.x, bl.y);
-          }
-          const int s = c * 4 + j;
-          const bool block_end = ((s + 1) & spb_mask) == 0;
-          const bool range_end = (j == 3) && (c + 1 == c1);
-          if (block_end || range_end) {
-            // Blocks past the last real one (k >= nb*bs, chunk padding) hold
-            // no codes and no activations: their slot is never staged, so
-            // they contribute scale 0.
-            const int bglob = (s * 16) >> p.bs_log2;
-            const int bl = bglob - blo;
-            const int si = tau * p.nbr * kTileN + bl * kTileN + g;
-            float s0 = 0.f, s1 = 0.f;
-            float z0 = 136.f, z1 = 136.f;
-            if (bglob < p.nb) {
-              if (p.scale_f32) {
-                s0 = reinterpret_cast<const float *>(sSc)[si];
-                s1 = reinterpret_cast<const float *>(sSc)[si + 8];
-              } else {
-                s0 = bf16_bits_to_f32(reinterpret_cast<const uint16_t *>(sSc)[si]);
-                s1 = bf16_bits_to_f32(reinterpret_cast<const uint16_t *>(sSc)[si + 8]);
-              }
-              if (p.has_zp) {
-                const uint2 zw = sZp[tau * p.nbr + bl];
-                z0 = static_cast<float>(128 + ((zw.x >> (4 * g)) & 15));
-                z1 = static_cast<float>(128 + ((zw.y >> (4 * g)) & 15));
-              }
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              float S0, S1;
-              if (big_blocks) {
-                S0 = srun[mt][0];
-                S1 = srun[mt][1];
-                srun[mt][0] = srun[mt][1] = 0.f;
-              } else {
-                const int gl = (cl * kChunkK + 16 * j) >> p.bs_log2;
-                const int m0 = mt * 8 + 2 * t;
-                S0 = m0 < p.M ? sS[m0 * p.sg + gl] : 0.f;
-                S1 = m0 + 1 < p.M ? sS[(m0 + 1) * p.sg + gl] : 0.f;
-              }
-              acc[mt][0] = fmaf(s0, fmaf(-z0, S0, d[mt][0]), acc[mt][0]);
-              acc[mt][1] = fmaf(s0, fmaf(-z0, S1, d[mt][1]), acc[mt][1]);
-              acc[mt][2] = fmaf(s1, fmaf(-z1, S0, d[mt][2]), acc[mt][2]);
-              acc[mt][3] = fmaf(s1, fmaf(-z1, S1, d[mt][3]), acc[mt][3]);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) d[mt][q] = 0.f;
-            }
-          }
+        if (lane == 0) {
+          uint64_t *bar = full + slot;
+          unsigned char *st = ring + slot * p.stage_bytes;
+          const int c = clo + j * p.ksw;  // first chunk of the stage
+          const int b = (c * kChunkK) >> G::kLog2;
+          mbar_arrive_expect_tx(bar, p.stage_tx);
+          tma_load_3d(st, &p.tmw[q], 0, c, tile0, bar);
+          tma_load_3d(st + p.st_sc, &p.tms[q], 0, b, tile0, bar);
+          if (HAS_ZP) tma_load_3d(st + p.st_zp, &p.tmz[q], 0, b >> 1, tile0, bar);
+        }
+        __syncwarp();
+        if (++slot == p.nst) {
+          slot = 0;
+          phase ^= 1;
+          wrapped = true;
         }
       }
+      if (p.cluster > 1) {
+        cluster_sync_all();
+        cluster_sync_all();
+      }
     }
-  }
+  } else {
+    // ---- consumers ---------------------------------------------------------------
+    const int g = lane >> 2, t = lane & 3;
+    const int tau = warp / p.ksw, ks = warp - tau * p.ksw;
+    const int cbase = clo + ks;  // this warp's chunk in stage j is cbase + j*ksw
 
-  // 6. Fixed-order split-K reduction and epilogue.
-  constexpr int MC = MT * 8;
-  {
-    float *red = sRed + warp * (kTileN * MC);
+    // From here on the upstream kernel's results (A) are visible.
+    grid_dependency_wait();
+
+    // Stage A rows [0, M) over the CTA's k range as bf16 (fp32 activations
+    // as hi + lo) and the sum of every granule (block, or 64-wide piece of a
+    // block) of the staged values, so the code offset 128 cancels exactly up
+    // to fp32 rounding.
+    const int ppr = p.ksw * p.R * (kChunkK / 8);  // 8-element pieces per row
+    const int npieces = p.M * ppr;
+    {
+      constexpr int gp = G::kGranule / 8;
+      for (int base = 0; base < npieces; base += kConsumers) {
+        const int pc2 = base + tid;
+        const bool ok = pc2 < npieces;
+        float part = 0.f;
+        int m = 0, kp = 0;
+        if (ok) {
+          m = pc2 / ppr;
+          kp = pc2 - m * ppr;
+          float v[8];
+          load8(p, m, (int64_t)clo * kChunkK + kp * 8, v);
+          uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int col = mt * 8 + 2 * t;
-      red[g * MC + col] = acc[mt][0];
-      red[g * MC + col + 1] = acc[mt][1];
-      red[(g + 8) * MC + col] = acc[mt][2];
-      red[(g + 8) * MC + col + 1] = acc[mt][3];
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t h0 = bf16_bits(v[2 * q]), h1 = bf16_bits(v[2 * q + 1]);
+            hi[q] = h0 | (h1 << 16);
+            const float f0 = bf16_bits_to_f32(h0), f1 = bf16_bits_to_f32(h1);
+            const uint32_t l0 = bf16_bits(v[2 * q] - f0), l1 = bf16_bits(v[2 * q + 1] - f1);
+            lo[q] = l0 | (l1 << 16);
+            part += (f0 + bf16_bits_to_f32(l0)) + (f1 + bf16_bits_to_f32(l1));
+          }
+          const int off = m * p.krp + kp * 8;
+          *reinterpret_cast<uint4 *>(sA + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          if (p.a_f32)
+            *reinterpret_cast<uint4 *>(sAlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        // Pieces of one granule sit in consecutive lanes (ppr is a multiple of 8).
+#pragma unroll
+        for (int o = 1; o < gp; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (ok && (kp % gp) == 0) sS[m * p.sg + kp / gp] = part;
+      }
     }
-  }
-  __syncthreads();
+    named_barrier_sync(kBarConsumers, kConsumers);
 
-  const int rows = p.tiles_per_cta * kTileN;
-  const int total = p.M * rows;
-  const int n_base = tgroup * p.tiles_per_cta * kTileN;
-  auto store = [&](int e, float v) {
-    const int m = e / rows, r = e - m * rows;
-    const int n = n_base + r;
-    if (n < p.N) {
-      if (p.bias) v += __ldg(p.bias + n);
-      if (AF32)
-        static_cast<float *>(p.Y)[(int64_t)m * p.N + n] = v;
-      else
-        static_cast<uint16_t *>(p.Y)[(int64_t)m * p.N + n] =
-            static_cast<uint16_t>(bf16_bits(v));
+    constexpr int MC = MT * 8;
+    const int rows = p.tpc * kTileN;
+    // Activation fragments this lane reads (rows >= M stay zero) and the
+    // granule sums its accumulator columns need (rows >= M read row 0 and
+    // meet zero activations).
+    const bool mok0 = g < p.M, mok1 = 8 + g < p.M;
+    const uint16_t *arow0 = sA + (mok0 ? g : 0) * p.krp + 4 * t - clo * kChunkK;
+    const uint16_t *arow1 = sA + (mok1 ? 8 + g : 0) * p.krp + 4 * t - clo * kChunkK;
+    const int lo_off = static_cast<int>(sAlo - sA);
+    const bool two = p.a_f32 != 0;
+    const float *srow[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int m = mt * 8 + 2 * t + h;
+        srow[mt][h] = sS + (m < p.M ? m : 0) * p.sg - clo * (kChunkK / G::kGranule);
+      }
+    const bool direct = p.ksw == 1 && p.cluster == 1;
+    // This warp's slices of a stage: its chunk, and its tile's scales and
+    // zero-point pairs (stage block b0s = first block of the stage).
+    const int cofs = (tau * p.ksw + ks) * kChunkBytes + lane * 16;
+    const int sofs = p.st_sc + tau * p.nbs * kTileN * kEs;
+    const int zofs = p.st_zp + tau * p.nps * 16;
+    uint2 bfrag0 = make_uint2(0, 0), bfrag1 = make_uint2(0, 0);
+    int slot = 0;
+    uint32_t phase = 0;
+    bool fault = false;
+
+    for (int u = 0;; ++u) {
+      const int gi = gfirst + u * gstride;
+      if (gi >= p.tg_total) break;
+      const int q = problem_of(p, gi);
+      float acc[MT][4], d[MT][4], srun[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][e] = d[mt][e] = 0.f;
+        srun[mt][0] = srun[mt][1] = 0.f;
+      }
+
+      for (int j = 0; j < p.R && !fault; ++j) {
+        if (!mbar_wait(full + slot, phase)) {
+          record_fault(&g_fault_gemv, kFaultGemvWait);
+          fault = true;
+          break;
+        }
+        const unsigned char *st = ring + slot * p.stage_bytes;
+        const int c = cbase + j * p.ksw;
+        const int b0s = ((c - ks) * kChunkK) >> G::kLog2;  // first block of the stage
+
+        // Applies scale and zero point of block b to the block's MMA sums.
+        // Blocks past the last real one arrive zero-filled: scale 0.
+        auto correct = [&](int b, int gran) {
+          const int bi = b - b0s;
+          float s0, s1, z0 = 136.f, z1 = 136.f;
+          if (SF32) {
+            const float *sc = reinterpret_cast<const float *>(st + sofs) + bi * kTileN + g;
+            s0 = sc[0];
+            s1 = sc[8];
+          } else {
+            const uint16_t *sc = reinterpret_cast<const uint16_t *>(st + sofs) + bi * kTileN + g;
+            s0 = bf16_bits_to_f32(sc[0]);
+            s1 = bf16_bits_to_f32(sc[8]);
+          }
+          if (HAS_ZP) {
+            // b's word in the staged word pairs (the first pair holds b0s).
+            const uint2 zw = reinterpret_cast<const uint2 *>(st + zofs)
+                [b - (b0s & ~1)];
+            z0 = static_cast<float>(128 + ((zw.x >> (4 * g)) & 15));
+            z1 = static_cast<float>(128 + ((zw.y >> (4 * g)) & 15));
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            float S0, S1;
+            if (BS >= kChunkK) {
+              S0 = srun[mt][0];
+              S1 = srun[mt][1];
+              srun[mt][0] = srun[mt][1] = 0.f;
+            } else {
+              S0 = srow[mt][0][gran];
+              S1 = srow[mt][1][gran];
+            }
+            acc[mt][0] = fmaf(s0, fmaf(-z0, S0, d[mt][0]), acc[mt][0]);
+            acc[mt][1] = fmaf(s0, fmaf(-z0, S1, d[mt][1]), acc[mt][1]);
+            acc[mt][2] = fmaf(s1, fmaf(-z1, S0, d[mt][2]), acc[mt][2]);
+            acc[mt][3] = fmaf(s1, fmaf(-z1, S1, d[mt][3]), acc[mt][3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[mt][e] = 0.f;
+          }
+        };
+
+        if (BS >= kChunkK) {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            srun[mt][0] += srow[mt][0][c];
+            srun[mt][1] += srow[mt][1][c];
+          }
+        }
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(st + cofs);
+        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+        const uint16_t *a0 = arow0 + c * kChunkK;
+        const uint16_t *a1 = arow1 + c * kChunkK;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          uint32_t wf[4];
+          codes_to_bf16x2(wv[jj], wf);
+          lds64_if(mok0, bfrag0, a0 + 16 * jj);
+          mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
+          if (two) {
+            lds64_if(mok0, bfrag0, a0 + lo_off + 16 * jj);
+            mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
+          }
+          if (MT == 2) {
+            lds64_if(mok1, bfrag1, a1 + 16 * jj);
+            mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
+            if (two) {
+              lds64_if(mok1, bfrag1, a1 + lo_off + 16 * jj);
+              mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
+            }
+          }
+          if (BS < kChunkK && ((jj + 1) % (BS / 16)) == 0) {
+            const int b = (c * kChunkK >> G::kLog2) + jj / (BS / 16);
+            correct(b, b);
+          }
+        }
+        // Blocks of a chunk or larger end where this warp's next chunk (ksw
+        // further on) falls in another block, or with its k range.
+        if (BS >= kChunkK &&
+            (((c + p.ksw) >> G::kChunkShift) != (c >> G::kChunkShift) || j + 1 == p.R))
+          correct(c >> G::kChunkShift, 0);
+        // The stage slice is consumed: release it to the producer.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + slot);
+        if (++slot == p.nst) {
+          slot = 0;
+          phase ^= 1;
+        }
+      }
+
+      if (direct) {
+        // The warp owns all of K for its tile: store straight from registers.
+        const int n0 = (gi - p.tg_begin[q]) * rows + tau * kTileN + g;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int m = mt * 8 + 2 * t + (e & 1);
+            const int nn = n0 + 8 * (e >> 1);
+            if (m < p.M && nn < p.N[q]) store_y(p, q, m, nn, acc[mt][e]);
+          }
+        continue;
+      }
+
+      // Fixed-order split-K reduction of this tile group.
+      {
+        float *red = sRed + warp * (kTileN * MC);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int col = mt * 8 + 2 * t;
+          red[g * MC + col] = acc[mt][0];
+          red[g * MC + col + 1] = acc[mt][1];
+          red[(g + 8) * MC + col] = acc[mt][2];
+          red[(g + 8) * MC + col + 1] = acc[mt][3];
+        }
+      }
+      named_barrier_sync(kBarConsumers, kConsumers);
+      const int n_base = (gi - p.tg_begin[q]) * rows;
+      const int total = p.M * rows;
+      for (int e = tid; e < total; e += kConsumers) {
+        const int m = e / rows, r = e - m * rows;
+        const int tt = r >> 4, row = r & 15;
+        float v = 0.f;
+        for (int k2 = 0; k2 < p.ksw; ++k2)
+          v += sRed[((tt * p.ksw + k2) * kTileN + row) * MC + m];
+        if (p.cluster == 1) {
+          if (n_base + r < p.N[q]) store_y(p, q, m, n_base + r, v);
+        } else {
+          sPart[e] = v;
+        }
+      }
+      if (p.cluster > 1) {
+        // Combine the cluster's partials in rank order, then let every CTA
+        // reuse its buffers.
+        cluster_sync_all();
+        for (int e = tid * p.cluster + crank; e < total; e += kConsumers * p.cluster) {
+          float v = 0.f;
+          for (int r = 0; r < p.cluster; ++r) v += ld_dsmem_f32(sPart + e, r);
+          const int m = e / rows, r = e - m * rows;
+          if (n_base + r < p.N[q]) store_y(p, q, m, n_base + r, v);
+        }
+        cluster_sync_all();
+      } else {
+        named_barrier_sync(kBarConsumers, kConsumers);
+      }
     }
-  };
-  for (int e = tid; e < total; e += kThreads) {
-    const int m = e / rows, r = e - m * rows;
-    const int tt = r >> 4, row = r & 15;
-    float v = 0.f;
-    for (int q = 0; q < p.ksplit; ++q)
-      v += sRed[((tt * p.ksplit + q) * kTileN + row) * MC + m];
-    if (p.cluster == 1)
-      store(e, v);
-    else
-      sPart[e] = v;
-  }
-  if (p.cluster > 1) {
-    cluster_sync_all();
-    for (int e = tid * p.cluster + crank; e < total; e += kThreads * p.cluster) {
-      float v = 0.f;
-      for (int r = 0; r < p.cluster; ++r) v += ld_dsmem_f32(sPart + e, r);
-      store(e, v);
-    }
-    cluster_sync_all();
   }
 }
 
 struct Choice {
-  int KS, ksplit, cluster, tiles_per_cta, ctas;
+  int KS, ksw, cluster, tpc, R, nst;
+  int64_t tg;
   size_t smem;
   GemvParams layout;
 };
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
 
-bool layout_for(const MatmulArgs &a, int KS, Choice &ch) {
-  const int64_t K64 = ceil_div(a.K, kChunkK), N16 = ceil_div(a.N, kTileN);
-  if (ceil_div(K64, KS) > kMaxChunks) return false;
+bool layout_for(const GroupArgs &a, int KS, Choice &ch) {
+  const int64_t K64 = ceil_div(a.K, kChunkK);
   if (KS > 1 && KS > K64) return false;
-  const int ksplit = KS < kWarps ? KS : kWarps;
-  const int cluster = KS / ksplit;
+  const int ksw = KS < kConsumerWarps ? KS : kConsumerWarps;
+  const int cluster = KS / ksw;
   if (cluster > 8) return false;
-  const int tpc = kWarps / ksplit;
+  const int tpc = kConsumerWarps / ksw;
+  int64_t tg = 0;
+  for (int i = 0; i < a.count; ++i) tg += ceil_div(ceil_div(a.N[i], kTileN), tpc);
   const int MT = a.M <= 8 ? 1 : 2;
-  const int64_t krmax = ceil_div(K64, cluster) * kChunkK;
-  const int krp = static_cast<int>(krmax) + 16;
+  const int R = static_cast<int>(ceil_div(K64, KS));
+  const int64_t kr = int64_t(ksw) * R * kChunkK;  // staged activations per row
+  const int krp = static_cast<int>(kr) + 16;
   const int granule = a.bs < kChunkK ? a.bs : kChunkK;
-  const int sg = static_cast<int>(krmax / granule);
-  const int nbr = static_cast<int>(ceil_div(krmax, a.bs)) + 1;
+  const int sg = static_cast<int>(kr / granule);
   const int es = a.scale_f32 ? 4 : 2;
+  // A stage holds ksw consecutive chunks (ksw * 64 k) of tpc tiles, the
+  // nbs blocks they touch (stage starts are multiples of ksw chunks, so for
+  // blocks of at least ksw chunks a stage lies inside one block) and the
+  // nps zero-point pairs holding those blocks.
+  const int nbs = std::max<int>(1, ksw * kChunkK / a.bs);
+  const int nps = std::max(1, nbs / 2);
   GemvParams L{};
+  L.nbs = nbs;
+  L.nps = nps;
+  L.st_sc = ksw * tpc * kChunkBytes;  // 8 KB: 128-byte aligned
+  L.st_zp = static_cast<int>(align128(L.st_sc + size_t(tpc) * nbs * kTileN * es));
+  L.stage_bytes = static_cast<int>(align128(L.st_zp + (a.has_zp ? size_t(tpc) * nps * 16 : 0)));
+  L.stage_tx = tpc * (ksw * kChunkBytes + nbs * kTileN * es + (a.has_zp ? nps * 16 : 0));
   size_t off = align16(size_t(a.M) * krp * 2);
   L.off_alo = static_cast<int>(off);
   if (a.a_f32) off += align16(size_t(a.M) * krp * 2);
   L.off_s = static_cast<int>(off);
   off += align16(size_t(a.M) * sg * 4);
-  L.off_sc = static_cast<int>(off);
-  off += align16(size_t(tpc) * nbr * kTileN * es);
-  L.off_zp = static_cast<int>(off);
-  if (a.zp) off += align16(size_t(tpc) * nbr * 8);
   L.off_red = static_cast<int>(off);
-  off += align16(size_t(kWarps) * kTileN * MT * 8 * 4);
+  off += align16(size_t(kConsumerWarps) * kTileN * MT * 8 * 4);
   L.off_part = static_cast<int>(off);
   if (cluster > 1) off += align16(size_t(tpc) * kTileN * a.M * 4);
-  if (off > static_cast<size_t>(kSmemLimit)) return false;
+  L.off_bar = static_cast<int>(off);
+  off += 2 * kMaxStages * 8;
+  off = align128(off);
+  L.off_ring = static_cast<int>(off);
+  // Ring depth: as many stages as fit, at most kMaxStages, at least 2; stay
+  // within the two-CTAs-per-SM budget when the layout allows it.
+  size_t cap = kSmemBudget;
+  if (MT == 2 || off + 2 * size_t(L.stage_bytes) > cap) cap = 2 * kSmemBudget - 24 * 1024;
+  if (off + 2 * size_t(L.stage_bytes) > cap) return false;
+  int nst = static_cast<int>((cap - off) / L.stage_bytes);
+  nst = std::min(nst, kMaxStages);
+  // Do not hold more stages than the whole k range needs.
+  nst = std::max(2, std::min<int>(nst, R * 2));
+  off += size_t(nst) * L.stage_bytes;
   L.krp = krp;
   L.sg = sg;
-  L.granule = granule;
-  L.nbr = nbr;
+  L.nst = nst;
   ch.KS = KS;
-  ch.ksplit = ksplit;
+  ch.ksw = ksw;
   ch.cluster = cluster;
-  ch.tiles_per_cta = tpc;
-  ch.ctas = static_cast<int>(ceil_div(N16, tpc)) * cluster;
+  ch.tpc = tpc;
+  ch.R = R;
+  ch.nst = nst;
+  ch.tg = tg;
   ch.smem = off;
   ch.layout = L;
   return true;
 }
 
-template <int MT, bool AF32>
-cudaError_t launch_one(const GemvParams &p, const Choice &ch, bool pdl,
+template <int MT, int BS, bool HAS_ZP, bool SF32>
+cudaError_t launch_one(const GemvParams &p, const Choice &ch, int grid, bool pdl,
                        cudaStream_t stream) {
-  auto kernel = gemv_kernel<MT, AF32>;
+  auto kernel = gemv_kernel<MT, BS, HAS_ZP, SF32>;
   static bool configured = false;
   if (!configured) {
     const cudaError_t e = cudaFuncSetAttribute(
-        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kSmemBudget);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ch.ctas, 1, 1);
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = ch.smem;
   cfg.stream = stream;
@@ -435,53 +577,155 @@ cudaError_t launch_one(const GemvParams &p, const Choice &ch, bool pdl,
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+template <int MT, int BS>
+cudaError_t launch_flags(const GemvParams &p, const Choice &ch, int grid, bool has_zp,
+                         bool sf32, bool pdl, cudaStream_t stream) {
+  if (has_zp)
+    return sf32 ? launch_one<MT, BS, true, true>(p, ch, grid, pdl, stream)
+                : launch_one<MT, BS, true, false>(p, ch, grid, pdl, stream);
+  return sf32 ? launch_one<MT, BS, false, true>(p, ch, grid, pdl, stream)
+              : launch_one<MT, BS, false, false>(p, ch, grid, pdl, stream);
+}
+
+template <int MT>
+cudaError_t launch_bs(const GemvParams &p, const Choice &ch, int grid, int bs,
+                      bool has_zp, bool sf32, bool pdl, cudaStream_t stream) {
+  switch (bs) {
+    case 16: return launch_flags<MT, 16>(p, ch, grid, has_zp, sf32, pdl, stream);
+    case 32: return launch_flags<MT, 32>(p, ch, grid, has_zp, sf32, pdl, stream);
+    case 64: return launch_flags<MT, 64>(p, ch, grid, has_zp, sf32, pdl, stream);
+    case 128: return launch_flags<MT, 128>(p, ch, grid, has_zp, sf32, pdl, stream);
+    case 256: return launch_flags<MT, 256>(p, ch, grid, has_zp, sf32, pdl, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+// Tensor maps of one prepacked weight (see the layout in mnb_common.cuh).
+cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int ksw, GemvParams &p) {
+  const uint64_t N16 = ceil_div(a.N[i], kTileN), K64 = ceil_div(a.K, kChunkK);
+  const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
+  const uint64_t es = a.scale_f32 ? 4 : 2;
+  const uint32_t nbs = static_cast<uint32_t>(p.nbs), nps = static_cast<uint32_t>(p.nps);
+  {
+    const uint64_t dims[3] = {kChunkBytes / 4, K64, N16};
+    const uint64_t strides[2] = {kChunkBytes, K64 * kChunkBytes};
+    const uint32_t box[3] = {kChunkBytes / 4, static_cast<uint32_t>(ksw),
+                             static_cast<uint32_t>(tpc)};
+    cudaError_t e = make_tmap(&p.tmw[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.packed_b[i],
+                              dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const uint64_t words = kTileN * es / 4;
+    const uint64_t dims[3] = {words, nb, N16};
+    const uint64_t strides[2] = {kTileN * es, nb * kTileN * es};
+    const uint32_t box[3] = {static_cast<uint32_t>(words), nbs, static_cast<uint32_t>(tpc)};
+    cudaError_t e = make_tmap(&p.tms[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.scales[i],
+                              dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.has_zp) {
+    const uint64_t dims[3] = {4, nbz / 2, N16};
+    const uint64_t strides[2] = {16, nbz * 8};
+    const uint32_t box[3] = {4, nps, static_cast<uint32_t>(tpc)};
+    cudaError_t e = make_tmap(&p.tmz[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.zp[i], dims,
+                              strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
 
-cudaError_t launch_gemv(const MatmulArgs &a, cudaStream_t stream) {
-  if (a.M < 1 || a.M > kGemvMaxM) return cudaErrorNotSupported;
-  const int target = 2 * sm_count();
+cudaError_t gemv_take_fault(unsigned int *out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_fault_gemv, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fault_gemv, &zero, sizeof(unsigned int));
+  return e;
+}
+
+cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
+  if (a.M < 1 || a.M > kGemvMaxM || a.count < 1 || a.count > kMaxGroup)
+    return cudaErrorNotSupported;
+  const int sms = sm_count();
+  const int MT = a.M <= 8 ? 1 : 2;
+  // Pick the k split by a small cost model: rounds of resident CTAs times the
+  // chunks each warp streams per tile group, plus a per-round cost for the
+  // split-K reduction.
   Choice best{}, ch{};
   bool have = false;
-  for (int KS = 1; KS <= 64; KS *= 2) {
+  double best_cost = 0.0;
+  for (int KS = 1; KS <= 128; KS *= 2) {
     if (!layout_for(a, KS, ch)) continue;
-    if (!have || (best.ctas < target && ch.ctas > best.ctas)) {
+    const int per_sm = (MT == 1 && ch.smem <= static_cast<size_t>(kSmemBudget)) ? 2 : 1;
+    const int64_t resident = std::max<int64_t>(1, int64_t(sms) * per_sm / ch.cluster);
+    const int64_t rounds = ceil_div(ch.tg, resident);
+    const double per_round = double(ch.R) + (KS > 1 ? 2.0 : 0.0) + (ch.cluster > 1 ? 1.0 : 0.0);
+    const double cost = double(rounds) * per_round;
+    if (!have || cost < best_cost) {
       best = ch;
+      best_cost = cost;
       have = true;
     }
-    if (best.ctas >= target) break;
   }
   if (!have) return cudaErrorNotSupported;
 
   GemvParams p = best.layout;
   p.A = a.A;
-  p.wq = static_cast<const uint4 *>(a.packed_b);
-  p.scales = a.scales;
-  p.zp = static_cast<const uint2 *>(a.zp);
-  p.bias = a.bias;
-  p.Y = a.Y;
+  p.nprob = a.count;
+  int64_t tg = 0;
+  for (int i = 0; i < a.count; ++i) {
+    const cudaError_t e = weight_maps(a, i, best.tpc, best.ksw, p);
+    if (e != cudaSuccess) return e;
+    p.bias[i] = a.bias[i];
+    p.Y[i] = a.Y[i];
+    p.N[i] = static_cast<int>(a.N[i]);
+    p.N16[i] = static_cast<int>(ceil_div(a.N[i], kTileN));
+    p.tg_begin[i] = static_cast<int>(tg);
+    tg += ceil_div(p.N16[i], best.tpc);
+  }
+  p.tg_total = static_cast<int>(tg);
   p.M = static_cast<int>(a.M);
-  p.N = static_cast<int>(a.N);
   p.K = static_cast<int>(a.K);
   p.K64 = static_cast<int>(ceil_div(a.K, kChunkK));
-  p.N16 = static_cast<int>(ceil_div(a.N, kTileN));
   p.nb = static_cast<int>(ceil_div(a.K, a.bs));
-  p.bs = a.bs;
-  p.bs_log2 = 31 - __builtin_clz(static_cast<unsigned>(a.bs));
-  p.scale_f32 = a.scale_f32;
-  p.has_zp = a.zp != nullptr;
-  p.ksplit = best.ksplit;
-  p.tiles_per_cta = best.tiles_per_cta;
-  p.cluster = best.cluster;
-  p.KS = best.KS;
+  p.a_f32 = a.a_f32;
   const int vec_elems = a.a_f32 ? 4 : 8;
   p.a_vec = (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) && (a.K % vec_elems == 0);
+  p.ksw = best.ksw;
+  p.tpc = best.tpc;
+  p.cluster = best.cluster;
+  p.R = best.R;
 
-  const bool mt2 = a.M > 8;
-  if (a.a_f32)
-    return mt2 ? launch_one<2, true>(p, best, a.pdl, stream)
-               : launch_one<1, true>(p, best, a.pdl, stream);
-  return mt2 ? launch_one<2, false>(p, best, a.pdl, stream)
-             : launch_one<1, false>(p, best, a.pdl, stream);
+  // Persistent grid: every tile group gets a CTA (cluster) when they fit in
+  // the CTAs resident at once; otherwise CTAs walk the groups.
+  const int per_sm = (MT == 1 && best.smem <= static_cast<size_t>(kSmemBudget)) ? 2 : 1;
+  const int64_t resident = int64_t(sms) * per_sm / best.cluster;
+  const int64_t clusters = tg < resident ? tg : resident;
+  const int grid = static_cast<int>(clusters) * best.cluster;
+
+  return MT == 2 ? launch_bs<2>(p, best, grid, a.bs, a.has_zp, a.scale_f32, a.pdl, stream)
+                 : launch_bs<1>(p, best, grid, a.bs, a.has_zp, a.scale_f32, a.pdl, stream);
+}
+
+cudaError_t launch_gemv(const MatmulArgs &a, cudaStream_t stream) {
+  GroupArgs g{};
+  g.A = a.A;
+  g.count = 1;
+  g.packed_b[0] = a.packed_b;
+  g.scales[0] = a.scales;
+  g.zp[0] = a.zp;
+  g.bias[0] = a.bias;
+  g.Y[0] = a.Y;
+  g.N[0] = a.N;
+  g.M = a.M;
+  g.K = a.K;
+  g.bs = a.bs;
+  g.a_f32 = a.a_f32;
+  g.scale_f32 = a.scale_f32;
+  g.has_zp = a.zp != nullptr;
+  g.pdl = a.pdl;
+  return launch_gemv_group(g, stream);
 }
 
 }  // namespace mnb

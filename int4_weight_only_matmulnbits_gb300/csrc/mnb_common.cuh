@@ -20,7 +20,9 @@
 //  * packed_scales holds, per (tile, block b), the 16 scales of the tile's
 //    rows in the stored dtype: element ((tile*nb + b)*16 + r).
 //  * packed_zp holds, per (tile, block b), one 64-bit word whose nibble r is
-//    the zero point of row tile*16 + r.
+//    the zero point of row tile*16 + r; each tile has nbz = nb rounded up to
+//    even words (element tile*nbz + b), so any even-aligned block range of a
+//    tile is a 16-byte aligned span.
 #pragma once
 
 #include <cstdint>
@@ -57,6 +59,32 @@ __device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t (&r)[4]) {
   r[1] = lop3_and_or(w >> 4, kMask, kMagic);
   r[2] = lop3_and_or(w >> 8, kMask, kMagic);
   r[3] = lop3_and_or(w >> 12, kMask, kMagic);
+}
+
+// Eight packed codes -> four f16x2 registers, all exact: registers 0 and 2
+// (rows r0) hold q, registers 1 and 3 (rows r0 + 8) hold 1024 + 16 q. One
+// shift, four lop3 (OR-ing a nibble into the mantissa of 1024.0) and two
+// f16x2 subtractions of 1024.
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+  constexpr uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  r[0] = lop3_and_or(w, kLo, kMagic);
+  r[1] = lop3_and_or(w, kHi, kMagic);
+  r[2] = lop3_and_or(w8, kLo, kMagic);
+  r[3] = lop3_and_or(w8, kHi, kMagic);
+  asm("sub.f16x2 %0, %0, %1;" : "+r"(r[0]) : "r"(kMagic));
+  asm("sub.f16x2 %0, %0, %1;" : "+r"(r[2]) : "r"(kMagic));
+}
+
+// D += A * B, m16n8k16, f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4],
+                                              const uint32_t (&a)[4],
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
@@ -112,5 +140,113 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
 __device__ __forceinline__ uint32_t bf16_bits(float x) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
+
+}  // namespace mnb
+
+namespace mnb {
+
+// ---- mbarrier + bulk-copy (TMA, non-tensor) helpers ------------------------
+
+// Iteration cap for every mbarrier wait: far beyond any legitimate wait
+// (seconds), but finite, so a copy that never lands ends the kernel with a
+// recorded fault instead of a hang.
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n\t"
+               "fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; returns false if the cap was reached.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src,
+                                              uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 8-byte shared-memory load performed only when `pred` holds (v unchanged
+// otherwise); no branch.
+__device__ __forceinline__ void lds64_if(bool pred, uint2 &v, const void *p) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q ld.shared.v2.u32 {%0, %1}, [%3];\n\t}"
+      : "+r"(v.x), "+r"(v.y)
+      : "r"(static_cast<int>(pred)), "r"(smem_addr(p)));
+}
+
+// 3-D tiled TMA load into this CTA's shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x,
+                                            int y, int z, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+// Barrier among `count` threads (a multiple of 32) on hardware barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Each kernel file keeps a device fault word that a kernel sets when one of
+// its bounded waits runs out; mnb_fault_status() reads and clears them.
+__device__ __forceinline__ void record_fault(unsigned int *word,
+                                             unsigned int code) {
+  atomicOr(word, code);
+}
+
+constexpr unsigned int kFaultGemvWait = 1u;
+constexpr unsigned int kFaultGemmWait = 2u;
 
 }  // namespace mnb

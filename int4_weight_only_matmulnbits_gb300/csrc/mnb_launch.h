@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mnb {
@@ -42,15 +43,43 @@ struct MatmulArgs {
 cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream);
 cudaError_t launch_unprepack(const UnprepackArgs &a, cudaStream_t stream);
 
+// Up to kMaxGroup weights that share one activation matrix A (fused-N
+// projections), each with its own N, output and optional bias.
+constexpr int kMaxGroup = 4;
+struct GroupArgs {
+  const void *A;
+  int count;
+  const void *packed_b[kMaxGroup], *scales[kMaxGroup], *zp[kMaxGroup];
+  const float *bias[kMaxGroup];
+  void *Y[kMaxGroup];
+  int64_t N[kMaxGroup];
+  int64_t M, K;
+  int bs;
+  bool a_f32, scale_f32, has_zp;
+  bool pdl;
+};
+
 // Small-M split-K kernel (M <= kGemvMaxM). Returns cudaErrorNotSupported when
 // no launch configuration fits this shape.
 constexpr int kGemvMaxM = 16;
 cudaError_t launch_gemv(const MatmulArgs &a, cudaStream_t stream);
+cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream);
 
 // tcgen05/TMEM tensor-core kernel for larger M. Returns
 // cudaErrorNotSupported for combinations it does not serve.
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream);
 
 int sm_count();
+
+// Tiled tensor map over `rank` dims (dims[0] innermost; strides_bytes[i] is
+// the stride of dim i+1). cudaErrorInvalidValue if the driver rejects it.
+cudaError_t make_tmap(CUtensorMap *map, CUtensorMapDataType dtype, int rank,
+                      const void *base, const uint64_t *dims,
+                      const uint64_t *strides_bytes, const uint32_t *box,
+                      CUtensorMapSwizzle swizzle);
+
+// Read and clear the fault word of each kernel file (0 = no fault).
+cudaError_t gemv_take_fault(unsigned int *out);
+cudaError_t gemm_take_fault(unsigned int *out);
 
 }  // namespace mnb

@@ -55,13 +55,13 @@ __global__ void pack_scales_kernel(const T *__restrict__ s, T *__restrict__ out,
 
 __global__ void pack_zp_kernel(const uint8_t *__restrict__ zp,
                                uint64_t *__restrict__ out, int64_t N,
-                               int64_t nb, int64_t total) {
+                               int64_t nb, int64_t nbz, int64_t total) {
   const int64_t zbytes = (nb + 1) / 2;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t tile = i / nb, b = i % nb;
+    const int64_t tile = i / nbz, b = i % nbz;
     uint64_t word = 0;
-    for (int r = 0; r < kTileN; ++r) {
+    for (int r = 0; r < kTileN && b < nb; ++r) {
       const int64_t n = tile * kTileN + r;
       if (n >= N) break;
       const uint8_t byte = zp[n * zbytes + b / 2];
@@ -114,7 +114,7 @@ __global__ void unpack_scales_kernel(const T *__restrict__ packed,
 
 __global__ void unpack_zp_kernel(const uint64_t *__restrict__ packed,
                                  uint8_t *__restrict__ zp, int64_t nb,
-                                 int64_t total) {
+                                 int64_t nbz, int64_t total) {
   const int64_t zbytes = (nb + 1) / 2;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -125,7 +125,7 @@ __global__ void unpack_zp_kernel(const uint64_t *__restrict__ packed,
     for (int o = 0; o < 2; ++o) {
       const int64_t b = zb * 2 + o;
       if (b >= nb) continue;
-      byte |= static_cast<uint32_t>((packed[tile * nb + b] >> (4 * r)) & 0xF)
+      byte |= static_cast<uint32_t>((packed[tile * nbz + b] >> (4 * r)) & 0xF)
               << (4 * o);
     }
     zp[i] = static_cast<uint8_t>(byte);
@@ -163,9 +163,11 @@ cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream) {
     pack_scales_kernel<uint16_t><<<grid_for(ns), 256, 0, stream>>>(
         static_cast<const uint16_t *>(a.scales),
         static_cast<uint16_t *>(a.packed_scales), a.N, nb, ns);
-  if (a.zp != nullptr)
-    pack_zp_kernel<<<grid_for(N16 * nb), 256, 0, stream>>>(
-        a.zp, static_cast<uint64_t *>(a.packed_zp), a.N, nb, N16 * nb);
+  if (a.zp != nullptr) {
+    const int64_t nbz = ceil_div(nb, 2) * 2;
+    pack_zp_kernel<<<grid_for(N16 * nbz), 256, 0, stream>>>(
+        a.zp, static_cast<uint64_t *>(a.packed_zp), a.N, nb, nbz, N16 * nbz);
+  }
   prepack_fence_kernel<<<1, 32, 0, stream>>>();
   return cudaGetLastError();
 }
@@ -189,7 +191,7 @@ cudaError_t launch_unprepack(const UnprepackArgs &a, cudaStream_t stream) {
   if (a.packed_zp != nullptr) {
     const int64_t nz = a.N * ((nb + 1) / 2);
     unpack_zp_kernel<<<grid_for(nz), 256, 0, stream>>>(
-        static_cast<const uint64_t *>(a.packed_zp), a.zp, nb, nz);
+        static_cast<const uint64_t *>(a.packed_zp), a.zp, nb, ceil_div(nb, 2) * 2, nz);
   }
   return cudaGetLastError();
 }

@@ -55,7 +55,7 @@ def test_prepacked_sizes(lib, N, K, bs, zp, dt):
     n16, k64, nb = -(-N // 16), -(-K // 64), -(-K // bs)
     assert b == n16 * k64 * 512
     assert s == n16 * nb * 16 * (4 if dt == torch.float32 else 2)
-    assert z == (n16 * nb * 8 if zp else 0)
+    assert z == (n16 * (-(-nb // 2) * 2) * 8 if zp else 0)
 
 
 def test_packed_storage_within_bound_for_qwen_shapes(lib):

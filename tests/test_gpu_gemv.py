@@ -213,3 +213,28 @@ def test_invalid_arguments_raise_and_launch_nothing(dev):
         mnb.mnb_matmul(A, w, out=A[:, :64])  # output overlaps the input
     assert e.value.status == -6
     torch.cuda.synchronize()
+
+
+# --- fused-N projections (one launch, shared activations) ---------------------
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("with_zp", [False, True])
+def test_grouped_projections_match_oracle(dev, M, dtype, with_zp):
+    """q/k/v-like group (N 4096/1024/1023, shared A) and a 4-weight group
+    with a ragged K: each output against the oracle on the shared A."""
+    for K, bs, Ns in ((2560, 128, (4096, 1024, 1023)), (1000, 32, (96, 7, 300, 129))):
+        probs = [make_problem(M, N, K, bs, dtype=dtype, zero_points=with_zp,
+                              bias=(i % 2 == 0), seed=100 * i + M) for i, N in enumerate(Ns)]
+        A = probs[0].A
+        ws, biases = [], []
+        for pr in probs:
+            _, B, S, Z, b = to_dev(pr, dev)
+            ws.append(mnb.mnb_prepack(B, S, Z, pr.N, K, bs))
+            biases.append(b)
+        outs = mnb.mnb_matmul_grouped(A.to(dev), ws, biases)
+        torch.cuda.synchronize()
+        for pr, Y in zip(probs, outs):
+            R, mag = oracle.matmulnbits(A, pr.B, pr.scales, pr.zero_points, pr.bias,
+                                        N=pr.N, K=K, block_size=bs)
+            check(Y, R, mag, f"grouped N{pr.N} K{K}")
