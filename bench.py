@@ -4,10 +4,14 @@ Workload: one batch-1 decode step of Qwen3-4B's projections (M = 1, bf16
 activations ~ N(0,1), block size 128, no zero points (8), bf16 scales
 U[0.002, 0.01]): q 2560->4096, k/v 2560->1024, o 4096->2560, gate/up
 2560->9728, down 9728->2560, for 36 layers, plus lm_head 2560->151936 —
-253 products and 2.08 GB of algorithmic bytes per step. Each projection has
-its own seeded weights and activation row; all are resident in HBM before
-timing. A step replays one CUDA graph of the 253 mnb_matmul launches. The
-step's bytes exceed the 129 MB L2 many times over, so no flush is needed.
+253 weights and 2.08 GB of algorithmic bytes per step, each weight with its
+own seeded codes and scales, all resident in HBM before timing.
+
+The step follows the model's data flow: q, k and v read one activation row
+and run as one fused-N launch (mnb_matmul_grouped), as do gate and up; o,
+down and lm_head each read their own row. That is 4 launches per layer and
+145 per step, replayed as one CUDA graph. The step's bytes exceed the
+129 MB L2 many times over, so no flush is needed.
 
 Also measured, outside the timed region of the headline number: the prefill
 GEMM at M = 2048 over the seven Qwen3-4B projection shapes (TFLOP/s), when
@@ -161,41 +165,52 @@ def run_reference(args, rank, world):
 
 def build_decode_step(dev, seed_base=5000):
     """Prepacked weights, activations and outputs of one decode step, all
-    resident on dev. Weights are drawn on the device from a seeded generator
+    resident on dev, as a list of launches: (weights, activation row,
+    outputs). Weights are drawn on the device from a seeded generator
     (2 GB would take minutes on the host)."""
     import torch
 
     import int4_weight_only_matmulnbits_gb300 as mnb
     from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_4B
-    projs = [(f"L{l}.{p.name}", p) for l in range(QWEN3_4B["layers"])
-             for p in QWEN3_4B["projections"]]
-    projs.append(("lm_head", QWEN3_4B["lm_head"]))
+    P = {p.name: p for p in QWEN3_4B["projections"]}
+    groups = [("qkv", [P["q"], P["k"], P["v"]]), ("o", [P["o"]]),
+              ("gate_up", [P["gate"], P["up"]]), ("down", [P["down"]])]
+    plan = [(f"L{l}.{name}", ps) for l in range(QWEN3_4B["layers"]) for name, ps in groups]
+    plan.append(("lm_head", [QWEN3_4B["lm_head"]]))
     bs = 128
     g = torch.Generator(device=dev)
-    items = []
-    a_total = sum(p.K for _, p in projs)
-    y_total = sum(p.N for _, p in projs)
+    a_total = sum(ps[0].K for _, ps in plan)
+    y_total = sum(p.N for _, ps in plan for p in ps)
     A_all = torch.empty(a_total, dtype=torch.bfloat16, device=dev)
     Y_all = torch.empty(y_total, dtype=torch.bfloat16, device=dev)
     ao = yo = 0
     algo_bytes = 0
-    for i, (name, p) in enumerate(projs):
-        g.manual_seed(seed_base + i)
-        nb = -(-p.K // bs)
-        B = torch.randint(0, 256, (p.N, nb, bs // 2), dtype=torch.uint8, device=dev,
-                          generator=g)
-        S = (torch.rand(p.N, nb, device=dev, generator=g) * 0.008 + 0.002).to(torch.bfloat16)
-        A = A_all[ao:ao + p.K].view(1, p.K)
-        A.copy_(torch.randn(1, p.K, device=dev, generator=g).to(torch.bfloat16))
-        Y = Y_all[yo:yo + p.N].view(1, p.N)
-        w = mnb.mnb_prepack(B, S, None, p.N, p.K, bs)
-        del B, S
-        items.append((name, p, w, A, Y))
-        ao += p.K
-        yo += p.N
-        algo_bytes += p.N * nb * bs // 2 + p.N * nb * 2 + p.K * 2 + p.N * 2
+    launches = []
+    seed = seed_base
+    for name, ps in plan:
+        K = ps[0].K
+        nb = -(-K // bs)
+        A = A_all[ao:ao + K].view(1, K)
+        g.manual_seed(seed)
+        A.copy_(torch.randn(1, K, device=dev, generator=g).to(torch.bfloat16))
+        ao += K
+        algo_bytes += K * 2
+        ws, Ys = [], []
+        for p in ps:
+            seed += 1
+            g.manual_seed(seed)
+            B = torch.randint(0, 256, (p.N, nb, bs // 2), dtype=torch.uint8, device=dev,
+                              generator=g)
+            S = (torch.rand(p.N, nb, device=dev, generator=g) * 0.008 + 0.002).to(torch.bfloat16)
+            ws.append(mnb.mnb_prepack(B, S, None, p.N, K, bs))
+            del B, S
+            Ys.append(Y_all[yo:yo + p.N].view(1, p.N))
+            yo += p.N
+            algo_bytes += p.N * nb * bs // 2 + p.N * nb * 2 + p.N * 2
+        launches.append((name, ws, A, Ys))
+        seed += 1
     torch.cuda.synchronize()
-    return items, A_all, Y_all, algo_bytes
+    return launches, A_all, Y_all, algo_bytes
 
 
 def time_region(fn, steps, stream):
@@ -262,13 +277,16 @@ def run_gpu(args, rank, world, dist):
     mnb.load()
     hbm_peak, _, _, peak_kind = peaks()
 
-    items, A_all, Y_all, algo_bytes = build_decode_step(dev)
+    launches, A_all, Y_all, algo_bytes = build_decode_step(dev)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
     def step_eager():
-        for _, p, w, A, Y in items:
-            mnb.mnb_matmul(A, w, None, out=Y)
+        for _, ws, A, Ys in launches:
+            if len(ws) == 1:
+                mnb.mnb_matmul(A, ws[0], None, out=Ys[0])
+            else:
+                mnb.mnb_matmul_grouped(A, ws, outs=Ys)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -278,7 +296,7 @@ def run_gpu(args, rank, world, dist):
     with torch.cuda.graph(graph, stream=stream):
         step_eager()
     torch.cuda.synchronize()
-    launches_per_step = len(items)
+    launches_per_step = len(launches)
 
     warmup = max(args.warmup, 3)
     for _ in range(warmup):
@@ -335,16 +353,19 @@ def run_gpu(args, rank, world, dist):
         "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "block_size": 128, "a_dtype": "bf16",
-                   "projections_per_step": launches_per_step,
+                   "weights_per_step": sum(len(ws) for _, ws, _, _ in launches),
+                   "launches_per_step": launches_per_step,
                    "algorithmic_bytes_per_step": algo_bytes,
                    "l2": "inputs larger than L2 (2.08 GB per step vs 129 MB)",
-                   "launch": "one CUDA graph of 253 launches, programmatic dependent launch",
+                   "launch": "one CUDA graph per step: per layer fused qkv, o, fused gate+up, "
+                             "down, then lm_head (145 launches), programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
         "hbm_fraction": per_gpu / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": hbm_peak,
                      "unit": "GB/s", "frac": per_gpu / hbm_peak, "traffic": None,
                      "peak_kind": peak_kind,
-                     "kernel": "gemv_kernel (every launch of the step)"},
+                     "kernel": "gemv_kernel (every launch of the step)",
+                     "achieved_basis": "algorithmic bytes of the step / device time of the step"},
         "e2e": {"value": e2e, "unit": "GB/s",
                 "h2d_bytes_per_step": A_all.numel() * A_all.element_size(),
                 "d2h_bytes_per_step": Y_all.numel() * Y_all.element_size()},

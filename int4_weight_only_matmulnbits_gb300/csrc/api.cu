@@ -133,10 +133,23 @@ mnb_status run_matmul(const void *A, const void *packed_b, const void *scales,
   MatmulArgs a{A, packed_b, scales, zero_points, bias, Y, M, N, K, block_size,
                a_dtype == MNB_F32, scale_dtype == MNB_F32, g_pdl.load() != 0};
   cudaError_t e;
-  if (path == MNB_PATH_GEMV || (path == MNB_PATH_AUTO && M <= kGemvMaxM))
+  if (path == MNB_PATH_GEMV || (path == MNB_PATH_AUTO && M <= kGemvMaxM)) {
     e = launch_gemv(a, stream);
-  else
+  } else if (path == MNB_PATH_GEMM || gemm_supports(a)) {
     e = launch_gemm(a, stream);
+  } else {
+    // Activations the tensor-core kernel cannot stage (fp32, or rows that
+    // are not 16-byte aligned): the decode kernel over 16-row slices.
+    const size_t es = dtype_size(a_dtype);
+    e = cudaSuccess;
+    for (int64_t m0 = 0; m0 < M && e == cudaSuccess; m0 += kGemvMaxM) {
+      MatmulArgs s = a;
+      s.A = static_cast<const char *>(A) + size_t(m0) * K * es;
+      s.Y = static_cast<char *>(Y) + size_t(m0) * N * es;
+      s.M = M - m0 < kGemvMaxM ? M - m0 : kGemvMaxM;
+      e = launch_gemv(s, stream);
+    }
+  }
   if (e == cudaErrorNotSupported) {
     std::snprintf(g_last_error, sizeof g_last_error,
                   "no kernel for M=%lld N=%lld K=%lld bs=%d", (long long)M,

@@ -1,10 +1,402 @@
-// Tensor-core (tcgen05 / TMEM) MatMulNBits kernel for larger M.
+// Tensor-core (tcgen05 / TMEM) MatMulNBits kernel for larger M (prefill).
+//
+// Computes Y[m,n] = sum_k A[m,k] (q[n,k] - z[n,b]) s[n,b] + bias[n] with
+// bf16 activations on the prepacked layout of mnb_common.cuh. It follows
+// the page "Qwen3 CPU Inference Critical Path", section "Prepared weight-only
+// plan", int4_gemm: activation panels are packed (here: TMA-staged tiles),
+// weight blocks are reused across the rows of a tile, and the full weight
+// matrix is never expanded: only one 128 x 64 bf16 slice per pipeline stage
+// exists, in shared memory.
+//
+// GB300 mapping (one CTA per 128 x BN output tile):
+//  * warp 0, one thread: TMA producer. Per 64-wide k stage it loads the A
+//    tile (128 x 64 bf16, 128-byte swizzle), the BN x 64 packed codes of the
+//    stage and their scales and zero points, completing on full[s].
+//  * warps 2-5: dequantise the stage's codes to bf16 (q - z) * s (the
+//    difference is exact; one rounding in the product) straight into the
+//    K-major, 128-byte-swizzled layout tcgen05.mma reads, fence the writes
+//    to the async proxy and arrive on dq[s].
+//  * warp 1: allocates the TMEM accumulator (128 lanes x BN fp32 columns);
+//    one thread issues four tcgen05.mma (M=128, N=BN, K=16) per stage and
+//    commits each stage to empty[s], the last one to acc_full.
+//  * warps 2-5 then read the accumulator with tcgen05.ld, add the bias,
+//    round to bf16 and store Y.
+// Every mbarrier wait is bounded; a wait that runs out records a fault bit
+// and the kernel abandons the tile.
+#include <cuda_bf16.h>
+
 #include "mnb_common.cuh"
 #include "mnb_launch.h"
 
 namespace mnb {
 
 __device__ unsigned int g_fault_gemm = 0;
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 64;  // one chunk of the packed layout
+constexpr int kStages = 4;
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kTilesN = kBN / kTileN;
+constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
+constexpr int kBTileBytes = kBN * kBK * 2;  // 16 KB
+constexpr int kCodeBytes = kTilesN * kChunkBytes;  // 4 KB
+
+struct GemmParams {
+  CUtensorMap tma;  // A: {K, M} bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap tmw;  // codes: {128 words, K64, N16}, box {128, 1, 8}
+  CUtensorMap tms;  // scales: {16 scales as words, nb, N16}, box {.., bpc, 8}
+  CUtensorMap tmz;  // zero points: {4 words, nbz/2, N16}, box {4, ppc, 8}
+  const float *bias;
+  void *Y;
+  int M, N, K64;
+  int has_zp;
+  int y_vec;  // Y rows are 16-byte aligned: 16-byte stores
+  int sc_bytes, zp_bytes;  // per stage
+};
+
+// Shared-memory plan (offsets from a 1024-aligned base).
+struct Smem {
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + kStages * kATileBytes;
+  static constexpr int kCodes = kB + kStages * kBTileBytes;
+  static constexpr int kSc = kCodes + kStages * kCodeBytes;
+  static constexpr int kScBytes = 2048;  // 8 tiles x up to 4 blocks x 16 fp32 scales
+  static constexpr int kZp = kSc + kStages * kScBytes;
+  static constexpr int kZpBytes = 256;  // 8 tiles * 2 pairs * 16 bytes
+  static constexpr int kBar = kZp + kStages * kZpBytes;
+  static constexpr int kTmemSlot = kBar + (3 * kStages + 1) * 8;
+  static constexpr int kTotal = kTmemSlot + 16;
+};
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  // K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms of
+  // 1024 bytes (stride dimension byte offset), descriptor version 1.
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFF) >> 4);         // start address
+  d |= static_cast<uint64_t>(16 >> 4) << 16;                  // leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                        // version
+  d |= static_cast<uint64_t>(2) << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = kBN.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(kBN >> 3) << 17) |
+                            (static_cast<uint32_t>(kBM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(static_cast<int>(accumulate))
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+        "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// (q - z) * s for a bf16 pair holding 128 + q: exact difference, one rounding.
+template <bool SF32>
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t v, uint32_t zc, uint32_t sb,
+                                                 float sf) {
+  const uint32_t dq = bf16x2_sub(v, zc);  // q - z, exact
+  if (!SF32) return bf16x2_mul(dq, sb);
+  const float lo = bf16_bits_to_f32(dq & 0xFFFFu) * sf;
+  const float hi = bf16_bits_to_f32(dq >> 16) * sf;
+  return bf16_bits(lo) | (bf16_bits(hi) << 16);
+}
+
+template <int BS, bool HAS_ZP, bool SF32>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte alignment for the swizzled operand tiles.
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Smem::kBar);
+  uint64_t *dq = full + kStages;
+  uint64_t *empty = dq + kStages;
+  uint64_t *acc_full = empty + kStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.y * kBM;
+  const int nt0 = blockIdx.x * kTilesN;  // first 16-row weight tile
+  constexpr int kBpc = BS < kBK ? kBK / BS : 1;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(dq + i, 4);
+      mbar_init(empty + i, 1);
+    }
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kBN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Dependents may launch once every CTA of this grid has started; A is the
+  // upstream kernel's output.
+  grid_dependents_launch();
+  grid_dependency_wait();
+
+  bool fault = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = 0; kb < p.K64; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages && !mbar_wait(empty + s, ((kb / kStages) - 1) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          break;
+        }
+        uint64_t *bar = full + s;
+        mbar_arrive_expect_tx(bar, kATileBytes + kCodeBytes + p.sc_bytes + p.zp_bytes);
+        const int blk = (kb * kBK) / BS;
+        tma_load_2d(smem + Smem::kA + s * kATileBytes, &p.tma, kb * kBK, m0, bar);
+        tma_load_3d(smem + Smem::kCodes + s * kCodeBytes, &p.tmw, 0, kb, nt0, bar);
+        tma_load_3d(smem + Smem::kSc + s * Smem::kScBytes, &p.tms, 0, blk, nt0, bar);
+        if (HAS_ZP)
+          tma_load_3d(smem + Smem::kZp + s * Smem::kZpBytes, &p.tmz, 0, blk >> 1, nt0, bar);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int kb = 0; kb < p.K64; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t par = (kb / kStages) & 1;
+        if (!mbar_wait(full + s, par) || !mbar_wait(dq + s, par)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          fault = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_addr(smem + Smem::kA + s * kATileBytes);
+        const uint32_t b_base = smem_addr(smem + Smem::kB + s * kBTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16(tmem, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(b_base + kk * 32),
+                    kb > 0 || kk > 0);
+        umma_commit(empty + s);
+      }
+      if (!fault) umma_commit(acc_full);
+    }
+  } else {
+    // ---- dequantisation warps (2..5), then the epilogue --------------------
+    const int dw = warp - 2;                // 0..3: tiles 2*dw, 2*dw + 1
+    const int g = lane >> 2, t = lane & 3;
+    for (int kb = 0; kb < p.K64; ++kb) {
+      const int s = kb % kStages;
+      if (!mbar_wait(full + s, (kb / kStages) & 1)) {
+        record_fault(&g_fault_gemm, kFaultGemmWait);
+        fault = true;
+        break;
+      }
+      const unsigned char *codes = smem + Smem::kCodes + s * kCodeBytes;
+      const unsigned char *sc = smem + Smem::kSc + s * Smem::kScBytes;
+      const uint2 *zp = reinterpret_cast<const uint2 *>(smem + Smem::kZp + s * Smem::kZpBytes);
+      unsigned char *btile = smem + Smem::kB + s * kBTileBytes;
+      const int blk0 = (kb * kBK) / BS;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int tile = 2 * dw + h;
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + tile * kChunkBytes + lane * 16);
+        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+        const int r0 = tile * kTileN + g;  // rows r0 and r0 + 8 of the B tile
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int bi = BS < kBK ? (16 * j) / BS : 0;  // block within the stage
+          // Scales of rows r0, r0 + 8 for block bi (zero-filled past nb).
+          float sf0, sf1;
+          uint32_t sb0 = 0, sb1 = 0;
+          if (SF32) {
+            const float *s4 = reinterpret_cast<const float *>(sc) + (tile * kBpc + bi) * kTileN;
+            sf0 = s4[g];
+            sf1 = s4[g + 8];
+          } else {
+            const uint16_t *s2 =
+                reinterpret_cast<const uint16_t *>(sc) + (tile * kBpc + bi) * kTileN;
+            sb0 = s2[g] * 0x10001u;
+            sb1 = s2[g + 8] * 0x10001u;
+            sf0 = sf1 = 0.f;
+          }
+          uint32_t zc0 = 0x43084308u, zc1 = 0x43084308u;  // bf16 136 = 128 + 8
+          if (HAS_ZP) {
+            const int b = blk0 + bi;
+            const int pairs = BS < 32 ? 2 : 1;
+            const uint2 zw = zp[(tile * pairs + (BS < 32 ? bi >> 1 : 0)) * 2 + (b & 1)];
+            const uint32_t z0 = (zw.x >> (4 * g)) & 15, z1 = (zw.y >> (4 * g)) & 15;
+            zc0 = (0x4300u | z0) * 0x10001u;
+            zc1 = (0x4300u | z1) * 0x10001u;
+          }
+          uint32_t r[4];
+          codes_to_bf16x2(wv[j], r);
+          const uint32_t v00 = dequant_pair<SF32>(r[0], zc0, sb0, sf0);  // row r0, k0..k0+1
+          const uint32_t v02 = dequant_pair<SF32>(r[2], zc0, sb0, sf0);  // row r0, k0+2..3
+          const uint32_t v10 = dequant_pair<SF32>(r[1], zc1, sb1, sf1);  // row r0+8
+          const uint32_t v12 = dequant_pair<SF32>(r[3], zc1, sb1, sf1);
+          // K-major 128-byte swizzle: 16-byte chunk (k / 8) XOR (row % 8).
+          const int k0 = 16 * j + 4 * t;
+          const int chunk = (k0 >> 3) ^ (r0 & 7);
+          const int inner = (k0 & 7) * 2;
+          *reinterpret_cast<uint2 *>(btile + r0 * 128 + chunk * 16 + inner) = make_uint2(v00, v02);
+          *reinterpret_cast<uint2 *>(btile + (r0 + 8) * 128 + chunk * 16 + inner) =
+              make_uint2(v10, v12);
+        }
+      }
+      fence_async_smem();  // make the tile visible to the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq + s);
+    }
+
+    // ---- epilogue: TMEM -> registers -> Y ----------------------------------
+    if (!fault && !mbar_wait(acc_full, 0)) {
+      record_fault(&g_fault_gemm, kFaultGemmWait);
+      fault = true;
+    }
+    if (!fault) {
+      tc_fence_after();
+      const int quarter = warp & 3;  // TMEM lanes this warp may read
+      const int m = m0 + quarter * 32 + lane;
+      const int n_base = nt0 * kTileN;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
+        if (m < p.M) {
+          const int n0 = n_base + c * 32;
+          uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
+          if (n0 + 32 <= p.N && p.y_vec) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float a = v[i + 2 * e], b = v[i + 2 * e + 1];
+                if (p.bias) {
+                  a += __ldg(p.bias + n0 + i + 2 * e);
+                  b += __ldg(p.bias + n0 + i + 2 * e + 1);
+                }
+                w[e] = bf16_bits(a) | (bf16_bits(b) << 16);
+              }
+              *reinterpret_cast<uint4 *>(yrow + n0 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            for (int i = 0; i < 32; ++i) {
+              const int n = n0 + i;
+              if (n < p.N) {
+                float a = v[i];
+                if (p.bias) a += __ldg(p.bias + n);
+                yrow[n] = static_cast<uint16_t>(bf16_bits(a));
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN)
+                 : "memory");
+  }
+}
+
+template <int BS, bool HAS_ZP, bool SF32>
+cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
+  auto kernel = gemm_kernel<BS, HAS_ZP, SF32>;
+  const int smem = Smem::kTotal + 1024;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <int BS>
+cudaError_t launch_flags(const GemmParams &p, dim3 grid, bool sf32, bool pdl,
+                         cudaStream_t stream) {
+  if (p.has_zp)
+    return sf32 ? launch_one<BS, true, true>(p, grid, pdl, stream)
+                : launch_one<BS, true, false>(p, grid, pdl, stream);
+  return sf32 ? launch_one<BS, false, true>(p, grid, pdl, stream)
+              : launch_one<BS, false, false>(p, grid, pdl, stream);
+}
+
+}  // namespace
 
 cudaError_t gemm_take_fault(unsigned int *out) {
   unsigned int zero = 0;
@@ -13,8 +405,73 @@ cudaError_t gemm_take_fault(unsigned int *out) {
   return e;
 }
 
-cudaError_t launch_gemm(const MatmulArgs &, cudaStream_t) {
-  return cudaErrorNotSupported;
+bool gemm_supports(const MatmulArgs &a) {
+  // bf16 activations whose rows TMA can address (16-byte row stride).
+  return !a.a_f32 && (a.K % 8) == 0 && (reinterpret_cast<uintptr_t>(a.A) % 16) == 0;
+}
+
+cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
+  if (!gemm_supports(a)) return cudaErrorNotSupported;
+  GemmParams p{};
+  const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
+  const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
+  const uint64_t es = a.scale_f32 ? 4 : 2;
+  const uint32_t bpc = a.bs < kBK ? kBK / a.bs : 1;
+  const uint32_t ppc = a.bs < 32 ? 2 : 1;
+  cudaError_t e;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
+    const uint32_t box[2] = {kBK, kBM};
+    e = make_tmap(&p.tma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.A, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const uint64_t dims[3] = {kChunkBytes / 4, K64, N16};
+    const uint64_t strides[2] = {kChunkBytes, K64 * kChunkBytes};
+    const uint32_t box[3] = {kChunkBytes / 4, 1, kTilesN};
+    e = make_tmap(&p.tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.packed_b, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const uint64_t words = kTileN * es / 4;
+    const uint64_t dims[3] = {words, nb, N16};
+    const uint64_t strides[2] = {kTileN * es, nb * kTileN * es};
+    const uint32_t box[3] = {static_cast<uint32_t>(words), bpc, kTilesN};
+    e = make_tmap(&p.tms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.scales, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  p.sc_bytes = static_cast<int>(kTilesN * bpc * kTileN * es);
+  p.zp_bytes = 0;
+  if (a.zp) {
+    const uint64_t dims[3] = {4, nbz / 2, N16};
+    const uint64_t strides[2] = {16, nbz * 8};
+    const uint32_t box[3] = {4, ppc, kTilesN};
+    e = make_tmap(&p.tmz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.zp, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    p.zp_bytes = static_cast<int>(kTilesN * ppc * 16);
+  }
+  p.bias = a.bias;
+  p.Y = a.Y;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K64 = static_cast<int>(K64);
+  p.has_zp = a.zp != nullptr;
+  p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
+  const dim3 grid(static_cast<unsigned>(ceil_div(a.N, kBN)),
+                  static_cast<unsigned>(ceil_div(a.M, kBM)), 1);
+  switch (a.bs) {
+    case 16: return launch_flags<16>(p, grid, a.scale_f32, a.pdl, stream);
+    case 32: return launch_flags<32>(p, grid, a.scale_f32, a.pdl, stream);
+    case 64: return launch_flags<64>(p, grid, a.scale_f32, a.pdl, stream);
+    case 128: return launch_flags<128>(p, grid, a.scale_f32, a.pdl, stream);
+    case 256: return launch_flags<256>(p, grid, a.scale_f32, a.pdl, stream);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace mnb

@@ -228,6 +228,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x,
       : "memory");
 }
 
+// 2-D tiled TMA load into this CTA's shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x,
+                                            int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
                    smem_addr(bar))

@@ -65,8 +65,9 @@ constexpr int kGemvMaxM = 16;
 cudaError_t launch_gemv(const MatmulArgs &a, cudaStream_t stream);
 cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream);
 
-// tcgen05/TMEM tensor-core kernel for larger M. Returns
-// cudaErrorNotSupported for combinations it does not serve.
+// tcgen05/TMEM tensor-core kernel for larger M: bf16 activations whose rows
+// are 16-byte aligned (K % 8 == 0). Returns cudaErrorNotSupported otherwise.
+bool gemm_supports(const MatmulArgs &a);
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream);
 
 int sm_count();
