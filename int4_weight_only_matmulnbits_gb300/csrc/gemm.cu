@@ -8,19 +8,23 @@
 // matrix is never expanded: only one 128 x 64 bf16 slice per pipeline stage
 // exists, in shared memory.
 //
-// GB300 mapping (one CTA per 128 x BN output tile):
+// GB300 mapping (one CTA per 128 x BN output tile, two CTAs per SM so one
+// CTA's epilogue overlaps the other's main loop):
 //  * warp 0, one thread: TMA producer. Per 64-wide k stage it loads the A
 //    tile (128 x 64 bf16, 128-byte swizzle), the BN x 64 packed codes of the
-//    stage and their scales and zero points, completing on full[s].
-//  * warps 2-5: dequantise the stage's codes to bf16 (q - z) * s (the
-//    difference is exact; one rounding in the product) straight into the
-//    K-major, 128-byte-swizzled layout tcgen05.mma reads, fence the writes
-//    to the async proxy and arrive on dq[s].
+//    stage and their scales and zero points into a three-deep input ring,
+//    completing on full[s].
+//  * warps 2-9, one 16-row weight tile each: dequantise the stage's codes to
+//    bf16 (q - z) * s (the difference is exact; one rounding in the product)
+//    into a two-deep ring of B tiles in the K-major, 128-byte-swizzled layout
+//    tcgen05.mma reads, fence the writes to the async proxy and arrive on
+//    bfull[b].
 //  * warp 1: allocates the TMEM accumulator (128 lanes x BN fp32 columns);
 //    one thread issues four tcgen05.mma (M=128, N=BN, K=16) per stage and
-//    commits each stage to empty[s], the last one to acc_full.
-//  * warps 2-5 then read the accumulator with tcgen05.ld, add the bias,
-//    round to bf16 and store Y.
+//    commits each stage to empty[s] and bempty[b], the last one to acc_full.
+//  * warps 2-9 then read the accumulator with tcgen05.ld (each warp its
+//    TMEM lane quarter and half of the columns), add the bias, round to
+//    bf16 and store Y.
 // Every mbarrier wait is bounded; a wait that runs out records a fault bit
 // and the kernel abandons the tile.
 #include <cuda_bf16.h>
@@ -37,8 +41,10 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kBK = 64;  // one chunk of the packed layout
-constexpr int kStages = 4;
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kStages = 3;   // input ring: A, codes, scales, zero points
+constexpr int kBStages = 2;  // dequantised B tiles
+constexpr int kDqWarps = 8;
+constexpr int kThreads = 32 * (2 + kDqWarps);
 constexpr int kTilesN = kBN / kTileN;
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBTileBytes = kBN * kBK * 2;  // 16 KB
@@ -61,15 +67,18 @@ struct GemmParams {
 struct Smem {
   static constexpr int kA = 0;
   static constexpr int kB = kA + kStages * kATileBytes;
-  static constexpr int kCodes = kB + kStages * kBTileBytes;
+  static constexpr int kCodes = kB + kBStages * kBTileBytes;
   static constexpr int kSc = kCodes + kStages * kCodeBytes;
   static constexpr int kScBytes = 2048;  // 8 tiles x up to 4 blocks x 16 fp32 scales
   static constexpr int kZp = kSc + kStages * kScBytes;
   static constexpr int kZpBytes = 256;  // 8 tiles * 2 pairs * 16 bytes
   static constexpr int kBar = kZp + kStages * kZpBytes;
-  static constexpr int kTmemSlot = kBar + (3 * kStages + 1) * 8;
+  static constexpr int kTmemSlot = kBar + (2 * kStages + 2 * kBStages + 1) * 8;
   static constexpr int kTotal = kTmemSlot + 16;
 };
+// Two CTAs share an SM: each may use at most half of its 228 KB, less the
+// 1 KB the runtime reserves per CTA and the 1 KB alignment slack.
+static_assert(Smem::kTotal + 1024 <= (228 * 1024) / 2 - 1024, "two CTAs per SM");
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   // K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms of
@@ -156,15 +165,16 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t v, uint32_t zc, uint32
 }
 
 template <int BS, bool HAS_ZP, bool SF32>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles.
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Smem::kBar);
-  uint64_t *dq = full + kStages;
-  uint64_t *empty = dq + kStages;
-  uint64_t *acc_full = empty + kStages;
+  uint64_t *empty = full + kStages;
+  uint64_t *bfull = empty + kStages;
+  uint64_t *bempty = bfull + kBStages;
+  uint64_t *acc_full = bempty + kBStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -175,8 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(full + i, 1);
-      mbar_init(dq + i, 4);
       mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(bfull + i, kDqWarps);
+      mbar_init(bempty + i, 1);
     }
     mbar_init(acc_full, 1);
     fence_barrier_init();
@@ -220,31 +233,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else if (warp == 1) {
     if (lane == 0) {
       for (int kb = 0; kb < p.K64; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t par = (kb / kStages) & 1;
-        if (!mbar_wait(full + s, par) || !mbar_wait(dq + s, par)) {
+        const int s = kb % kStages, b = kb % kBStages;
+        if (!mbar_wait(full + s, (kb / kStages) & 1) ||
+            !mbar_wait(bfull + b, (kb / kBStages) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           fault = true;
           break;
         }
         tc_fence_after();
         const uint32_t a_base = smem_addr(smem + Smem::kA + s * kATileBytes);
-        const uint32_t b_base = smem_addr(smem + Smem::kB + s * kBTileBytes);
+        const uint32_t b_base = smem_addr(smem + Smem::kB + b * kBTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
           umma_bf16(tmem, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(b_base + kk * 32),
                     kb > 0 || kk > 0);
         umma_commit(empty + s);
+        umma_commit(bempty + b);
       }
       if (!fault) umma_commit(acc_full);
     }
   } else {
-    // ---- dequantisation warps (2..5), then the epilogue --------------------
-    const int dw = warp - 2;                // 0..3: tiles 2*dw, 2*dw + 1
+    // ---- dequantisation warps (2..9), then the epilogue --------------------
+    const int tile = warp - 2;  // this warp's 16-row weight tile of the stage
     const int g = lane >> 2, t = lane & 3;
+    const int r0 = tile * kTileN + g;  // rows r0 and r0 + 8 of the B tile
     for (int kb = 0; kb < p.K64; ++kb) {
-      const int s = kb % kStages;
-      if (!mbar_wait(full + s, (kb / kStages) & 1)) {
+      const int s = kb % kStages, bslot = kb % kBStages;
+      if (!mbar_wait(full + s, (kb / kStages) & 1) ||
+          (kb >= kBStages && !mbar_wait(bempty + bslot, ((kb / kBStages) - 1) & 1))) {
         record_fault(&g_fault_gemm, kFaultGemmWait);
         fault = true;
         break;
@@ -252,58 +268,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const unsigned char *codes = smem + Smem::kCodes + s * kCodeBytes;
       const unsigned char *sc = smem + Smem::kSc + s * Smem::kScBytes;
       const uint2 *zp = reinterpret_cast<const uint2 *>(smem + Smem::kZp + s * Smem::kZpBytes);
-      unsigned char *btile = smem + Smem::kB + s * kBTileBytes;
+      unsigned char *btile = smem + Smem::kB + bslot * kBTileBytes;
       const int blk0 = (kb * kBK) / BS;
+      // Scales and zero points of rows r0, r0 + 8 for the stage's blocks
+      // (zero-filled past the last block).
+      uint32_t sb0[kBpc], sb1[kBpc], zc0[kBpc], zc1[kBpc];
+      float sf0[kBpc], sf1[kBpc];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int tile = 2 * dw + h;
-        const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + tile * kChunkBytes + lane * 16);
-        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-        const int r0 = tile * kTileN + g;  // rows r0 and r0 + 8 of the B tile
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int bi = BS < kBK ? (16 * j) / BS : 0;  // block within the stage
-          // Scales of rows r0, r0 + 8 for block bi (zero-filled past nb).
-          float sf0, sf1;
-          uint32_t sb0 = 0, sb1 = 0;
-          if (SF32) {
-            const float *s4 = reinterpret_cast<const float *>(sc) + (tile * kBpc + bi) * kTileN;
-            sf0 = s4[g];
-            sf1 = s4[g + 8];
-          } else {
-            const uint16_t *s2 =
-                reinterpret_cast<const uint16_t *>(sc) + (tile * kBpc + bi) * kTileN;
-            sb0 = s2[g] * 0x10001u;
-            sb1 = s2[g + 8] * 0x10001u;
-            sf0 = sf1 = 0.f;
-          }
-          uint32_t zc0 = 0x43084308u, zc1 = 0x43084308u;  // bf16 136 = 128 + 8
-          if (HAS_ZP) {
-            const int b = blk0 + bi;
-            const int pairs = BS < 32 ? 2 : 1;
-            const uint2 zw = zp[(tile * pairs + (BS < 32 ? bi >> 1 : 0)) * 2 + (b & 1)];
-            const uint32_t z0 = (zw.x >> (4 * g)) & 15, z1 = (zw.y >> (4 * g)) & 15;
-            zc0 = (0x4300u | z0) * 0x10001u;
-            zc1 = (0x4300u | z1) * 0x10001u;
-          }
-          uint32_t r[4];
-          codes_to_bf16x2(wv[j], r);
-          const uint32_t v00 = dequant_pair<SF32>(r[0], zc0, sb0, sf0);  // row r0, k0..k0+1
-          const uint32_t v02 = dequant_pair<SF32>(r[2], zc0, sb0, sf0);  // row r0, k0+2..3
-          const uint32_t v10 = dequant_pair<SF32>(r[1], zc1, sb1, sf1);  // row r0+8
-          const uint32_t v12 = dequant_pair<SF32>(r[3], zc1, sb1, sf1);
-          // K-major 128-byte swizzle: 16-byte chunk (k / 8) XOR (row % 8).
-          const int k0 = 16 * j + 4 * t;
-          const int chunk = (k0 >> 3) ^ (r0 & 7);
-          const int inner = (k0 & 7) * 2;
-          *reinterpret_cast<uint2 *>(btile + r0 * 128 + chunk * 16 + inner) = make_uint2(v00, v02);
-          *reinterpret_cast<uint2 *>(btile + (r0 + 8) * 128 + chunk * 16 + inner) =
-              make_uint2(v10, v12);
+      for (int bi = 0; bi < kBpc; ++bi) {
+        if (SF32) {
+          const float *s4 = reinterpret_cast<const float *>(sc) + (tile * kBpc + bi) * kTileN;
+          sf0[bi] = s4[g];
+          sf1[bi] = s4[g + 8];
+          sb0[bi] = sb1[bi] = 0;
+        } else {
+          const uint16_t *s2 = reinterpret_cast<const uint16_t *>(sc) + (tile * kBpc + bi) * kTileN;
+          sb0[bi] = s2[g] * 0x10001u;
+          sb1[bi] = s2[g + 8] * 0x10001u;
+          sf0[bi] = sf1[bi] = 0.f;
         }
+        zc0[bi] = zc1[bi] = 0x43084308u;  // bf16 136 = 128 + 8
+        if (HAS_ZP) {
+          const int b = blk0 + bi;
+          const int pairs = BS < 32 ? 2 : 1;
+          const uint2 zw = zp[(tile * pairs + (BS < 32 ? bi >> 1 : 0)) * 2 + (b & 1)];
+          zc0[bi] = (0x4300u | ((zw.x >> (4 * g)) & 15)) * 0x10001u;
+          zc1[bi] = (0x4300u | ((zw.y >> (4 * g)) & 15)) * 0x10001u;
+        }
+      }
+      const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + tile * kChunkBytes + lane * 16);
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int bi = BS < kBK ? (16 * j) / BS : 0;  // block of this k step
+        uint32_t r[4];
+        codes_to_bf16x2(wv[j], r);
+        const uint32_t v00 = dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi]);  // row r0
+        const uint32_t v02 = dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi]);
+        const uint32_t v10 = dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi]);  // row r0 + 8
+        const uint32_t v12 = dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi]);
+        // K-major 128-byte swizzle: 16-byte chunk (k / 8) XOR (row % 8).
+        const int k0 = 16 * j + 4 * t;
+        const int chunk = (k0 >> 3) ^ (r0 & 7);
+        const int inner = (k0 & 7) * 2;
+        *reinterpret_cast<uint2 *>(btile + r0 * 128 + chunk * 16 + inner) = make_uint2(v00, v02);
+        *reinterpret_cast<uint2 *>(btile + (r0 + 8) * 128 + chunk * 16 + inner) =
+            make_uint2(v10, v12);
       }
       fence_async_smem();  // make the tile visible to the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq + s);
+      if (lane == 0) mbar_arrive(bfull + bslot);
     }
 
     // ---- epilogue: TMEM -> registers -> Y ----------------------------------
@@ -313,11 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     if (!fault) {
       tc_fence_after();
-      const int quarter = warp & 3;  // TMEM lanes this warp may read
+      const int quarter = warp & 3;          // TMEM lanes this warp may read
+      const int half = (warp - 2) >> 2;      // which half of the columns
       const int m = m0 + quarter * 32 + lane;
       const int n_base = nt0 * kTileN;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
         float v[32];
         tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
         if (m < p.M) {
