@@ -14,13 +14,15 @@
 //  * Warp-specialised, persistent CTAs: 16 consumer warps and one producer
 //    warp. Output rows form 16-row tiles; a CTA works on a tile group of
 //    `tpc` tiles, each consumer warp owning one tile and one of `ksw`
-//    interleaved k slices (chunk j*ksw + ks of the CTA's k range; a cluster
-//    of CTAs splits K further). CTAs walk the tile groups with a fixed
-//    stride.
-//  * Per pipeline stage the producer moves the next ksw chunks of all tpc
-//    tiles with one 3-D TMA tensor copy (8 KB), plus one copy each for their
-//    scales and zero points, into a ring of shared-memory stages guarded by
-//    full/empty mbarriers. TMA zero fill covers ragged N, K and blocks.
+//    interleaved k slices: in stage j it takes `cpw` consecutive chunks,
+//    starting at chunk (j*ksw + ks)*cpw of the CTA's k range (a cluster of
+//    CTAs splits K further). CTAs walk the tile groups with a fixed stride.
+//  * Per pipeline stage the producer moves the next ksw*cpw chunks of all
+//    tpc tiles with one 3-D TMA tensor copy (8 KB per chunk per warp), plus
+//    one copy each for their scales and zero points, into a ring of
+//    shared-memory stages guarded by full/empty mbarriers. Several chunks
+//    per warp and stage spread the ring bookkeeping over more weights. TMA
+//    zero fill covers ragged N, K and blocks.
 //    The weights are constant, so the producer starts before the upstream
 //    kernel has finished, and the kernel lets its own dependents launch at
 //    once: consecutive launches overlap their weight streams.
@@ -69,7 +71,8 @@ struct GemvParams {
   int nprob, tg_total;
   int M, K, K64, nb;
   int a_f32, a_vec;
-  int ksw, tpc, cluster, R;  // k ranges per CTA, tiles per group, chunks per range
+  int ksw, tpc, cluster, R;  // k slices per CTA, tiles per group, stages per tile group
+  int cpw, scs;              // chunks per warp and stage; chunks per stage and tile (ksw*cpw)
   int krp, sg;               // staged activation row stride, granules per row
   int nst, stage_bytes, stage_tx;  // ring depth, stage stride, bytes per stage
   int st_sc, st_zp;  // offsets of scales and zero points in a stage (128-aligned)
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   const int crank = static_cast<int>(blockIdx.x) % p.cluster;
   const int gstride = static_cast<int>(gridDim.x) / p.cluster;
   const int gfirst = static_cast<int>(blockIdx.x) / p.cluster;
-  const int clo = crank * p.ksw * p.R;  // first chunk of this CTA's k range
+  const int clo = crank * p.scs * p.R;  // first chunk of this CTA's k range
 
   if (tid == 0) {
     for (int i = 0; i < p.nst; ++i) {
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         if (lane == 0) {
           uint64_t *bar = full + slot;
           unsigned char *st = ring + slot * p.stage_bytes;
-          const int c = clo + j * p.ksw;  // first chunk of the stage
+          const int c = clo + j * p.scs;  // first chunk of the stage
           const int b = (c * kChunkK) >> G::kLog2;
           mbar_arrive_expect_tx(bar, p.stage_tx);
           tma_load_3d(st, &p.tmw[q], 0, c, tile0, bar);
@@ -220,7 +223,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     // ---- consumers ---------------------------------------------------------------
     const int g = lane >> 2, t = lane & 3;
     const int tau = warp / p.ksw, ks = warp - tau * p.ksw;
-    const int cbase = clo + ks;  // this warp's chunk in stage j is cbase + j*ksw
+    // This warp's chunks in stage j are cbase + j*scs + i, i < cpw.
+    const int cbase = clo + ks * p.cpw;
 
     // From here on the upstream kernel's results (A) are visible.
     grid_dependency_wait();
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     // as hi + lo) and the sum of every granule (block, or 64-wide piece of a
     // block) of the staged values, so the code offset 128 cancels exactly up
     // to fp32 rounding.
-    const int ppr = p.ksw * p.R * (kChunkK / 8);  // 8-element pieces per row
+    const int ppr = p.scs * p.R * (kChunkK / 8);  // 8-element pieces per row
     const int npieces = p.M * ppr;
     {
       constexpr int gp = G::kGranule / 8;
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     const bool direct = p.ksw == 1 && p.cluster == 1;
     // This warp's slices of a stage: its chunk, and its tile's scales and
     // zero-point pairs (stage block b0s = first block of the stage).
-    const int cofs = (tau * p.ksw + ks) * kChunkBytes + lane * 16;
+    const int cofs = (tau * p.scs + ks * p.cpw) * kChunkBytes + lane * 16;
     const int sofs = p.st_sc + tau * p.nbs * kTileN * kEs;
     const int zofs = p.st_zp + tau * p.nps * 16;
     uint2 bfrag0 = make_uint2(0, 0), bfrag1 = make_uint2(0, 0);
@@ -314,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           break;
         }
         const unsigned char *st = ring + slot * p.stage_bytes;
-        const int c = cbase + j * p.ksw;
-        const int b0s = ((c - ks) * kChunkK) >> G::kLog2;  // first block of the stage
+        const int cst = cbase + j * p.scs;                            // warp's first chunk
+        const int b0s = ((cst - ks * p.cpw) * kChunkK) >> G::kLog2;  // stage's first block
 
         // Applies scale and zero point of block b to the block's MMA sums.
         // Blocks past the last real one arrive zero-filled: scale 0.
@@ -358,45 +362,53 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           }
         };
 
-        if (BS >= kChunkK) {
+#pragma unroll 1
+        for (int i = 0; i < p.cpw; ++i) {
+          const int c = cst + i;
+          if (BS >= kChunkK) {
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            srun[mt][0] += srow[mt][0][c];
-            srun[mt][1] += srow[mt][1][c];
-          }
-        }
-        const uint4 w4 = *reinterpret_cast<const uint4 *>(st + cofs);
-        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-        const uint16_t *a0 = arow0 + c * kChunkK;
-        const uint16_t *a1 = arow1 + c * kChunkK;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          uint32_t wf[4];
-          codes_to_bf16x2(wv[jj], wf);
-          lds64_if(mok0, bfrag0, a0 + 16 * jj);
-          mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
-          if (two) {
-            lds64_if(mok0, bfrag0, a0 + lo_off + 16 * jj);
-            mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
-          }
-          if (MT == 2) {
-            lds64_if(mok1, bfrag1, a1 + 16 * jj);
-            mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
-            if (two) {
-              lds64_if(mok1, bfrag1, a1 + lo_off + 16 * jj);
-              mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
+            for (int mt = 0; mt < MT; ++mt) {
+              srun[mt][0] += srow[mt][0][c];
+              srun[mt][1] += srow[mt][1][c];
             }
           }
-          if (BS < kChunkK && ((jj + 1) % (BS / 16)) == 0) {
-            const int b = (c * kChunkK >> G::kLog2) + jj / (BS / 16);
-            correct(b, b);
+          const uint4 w4 = *reinterpret_cast<const uint4 *>(st + cofs + i * kChunkBytes);
+          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+          const uint16_t *a0 = arow0 + c * kChunkK;
+          const uint16_t *a1 = arow1 + c * kChunkK;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint32_t wf[4];
+            codes_to_bf16x2(wv[jj], wf);
+            lds64_if(mok0, bfrag0, a0 + 16 * jj);
+            mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
+            if (two) {
+              lds64_if(mok0, bfrag0, a0 + lo_off + 16 * jj);
+              mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
+            }
+            if (MT == 2) {
+              lds64_if(mok1, bfrag1, a1 + 16 * jj);
+              mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
+              if (two) {
+                lds64_if(mok1, bfrag1, a1 + lo_off + 16 * jj);
+                mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
+              }
+            }
+            if (BS < kChunkK && ((jj + 1) % (BS / 16)) == 0) {
+              const int b = (c * kChunkK >> G::kLog2) + jj / (BS / 16);
+              correct(b, b);
+            }
+          }
+          // Blocks of a chunk or larger end where this warp's next chunk (the
+          // next one in the stage, else scs - cpw + 1 further on) falls in
+          // another block, or with its k range.
+          if (BS >= kChunkK) {
+            const int next = (i + 1 < p.cpw) ? c + 1 : c + p.scs - p.cpw + 1;
+            if ((next >> G::kChunkShift) != (c >> G::kChunkShift) ||
+                (j + 1 == p.R && i + 1 == p.cpw))
+              correct(c >> G::kChunkShift, 0);
           }
         }
-        // Blocks of a chunk or larger end where this warp's next chunk (ksw
-        // further on) falls in another block, or with its k range.
-        if (BS >= kChunkK &&
-            (((c + p.ksw) >> G::kChunkShift) != (c >> G::kChunkShift) || j + 1 == p.R))
-          correct(c >> G::kChunkShift, 0);
         // The stage slice is consumed: release it to the producer.
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + slot);
@@ -466,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 }
 
 struct Choice {
-  int KS, ksw, cluster, tpc, R, nst;
+  int KS, ksw, cluster, tpc, R, nst, cpw;
   int64_t tg;
   size_t smem;
   GemvParams layout;
@@ -475,35 +487,36 @@ struct Choice {
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
 
-bool layout_for(const GroupArgs &a, int KS, Choice &ch) {
+bool layout_for(const GroupArgs &a, int KS, int cpw, Choice &ch) {
   const int64_t K64 = ceil_div(a.K, kChunkK);
-  if (KS > 1 && KS > K64) return false;
+  if ((KS > 1 || cpw > 1) && int64_t(KS) * cpw > K64) return false;
   const int ksw = KS < kConsumerWarps ? KS : kConsumerWarps;
   const int cluster = KS / ksw;
   if (cluster > 8) return false;
   const int tpc = kConsumerWarps / ksw;
+  const int scs = ksw * cpw;
   int64_t tg = 0;
   for (int i = 0; i < a.count; ++i) tg += ceil_div(ceil_div(a.N[i], kTileN), tpc);
   const int MT = a.M <= 8 ? 1 : 2;
-  const int R = static_cast<int>(ceil_div(K64, KS));
-  const int64_t kr = int64_t(ksw) * R * kChunkK;  // staged activations per row
+  const int R = static_cast<int>(ceil_div(K64, int64_t(KS) * cpw));
+  const int64_t kr = int64_t(scs) * R * kChunkK;  // staged activations per row
   const int krp = static_cast<int>(kr) + 16;
   const int granule = a.bs < kChunkK ? a.bs : kChunkK;
   const int sg = static_cast<int>(kr / granule);
   const int es = a.scale_f32 ? 4 : 2;
-  // A stage holds ksw consecutive chunks (ksw * 64 k) of tpc tiles, the
-  // nbs blocks they touch (stage starts are multiples of ksw chunks, so for
-  // blocks of at least ksw chunks a stage lies inside one block) and the
+  // A stage holds scs consecutive chunks (scs * 64 k) of tpc tiles, the
+  // nbs blocks they touch (stage starts are multiples of scs chunks, so for
+  // blocks of at least scs chunks a stage lies inside one block) and the
   // nps zero-point pairs holding those blocks.
-  const int nbs = std::max<int>(1, ksw * kChunkK / a.bs);
+  const int nbs = std::max<int>(1, scs * kChunkK / a.bs);
   const int nps = std::max(1, nbs / 2);
   GemvParams L{};
   L.nbs = nbs;
   L.nps = nps;
-  L.st_sc = ksw * tpc * kChunkBytes;  // 8 KB: 128-byte aligned
+  L.st_sc = scs * tpc * kChunkBytes;  // cpw * 8 KB: 128-byte aligned
   L.st_zp = static_cast<int>(align128(L.st_sc + size_t(tpc) * nbs * kTileN * es));
   L.stage_bytes = static_cast<int>(align128(L.st_zp + (a.has_zp ? size_t(tpc) * nps * 16 : 0)));
-  L.stage_tx = tpc * (ksw * kChunkBytes + nbs * kTileN * es + (a.has_zp ? nps * 16 : 0));
+  L.stage_tx = tpc * (scs * kChunkBytes + nbs * kTileN * es + (a.has_zp ? nps * 16 : 0));
   size_t off = align16(size_t(a.M) * krp * 2);
   L.off_alo = static_cast<int>(off);
   if (a.a_f32) off += align16(size_t(a.M) * krp * 2);
@@ -536,6 +549,7 @@ bool layout_for(const GroupArgs &a, int KS, Choice &ch) {
   ch.tpc = tpc;
   ch.R = R;
   ch.nst = nst;
+  ch.cpw = cpw;
   ch.tg = tg;
   ch.smem = off;
   ch.layout = L;
@@ -601,7 +615,7 @@ cudaError_t launch_bs(const GemvParams &p, const Choice &ch, int grid, int bs,
 }
 
 // Tensor maps of one prepacked weight (see the layout in mnb_common.cuh).
-cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int ksw, GemvParams &p) {
+cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int scs, GemvParams &p) {
   const uint64_t N16 = ceil_div(a.N[i], kTileN), K64 = ceil_div(a.K, kChunkK);
   const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
   const uint64_t es = a.scale_f32 ? 4 : 2;
@@ -609,7 +623,7 @@ cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int ksw, GemvParams 
   {
     const uint64_t dims[3] = {kChunkBytes / 4, K64, N16};
     const uint64_t strides[2] = {kChunkBytes, K64 * kChunkBytes};
-    const uint32_t box[3] = {kChunkBytes / 4, static_cast<uint32_t>(ksw),
+    const uint32_t box[3] = {kChunkBytes / 4, static_cast<uint32_t>(scs),
                              static_cast<uint32_t>(tpc)};
     cudaError_t e = make_tmap(&p.tmw[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.packed_b[i],
                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -649,23 +663,27 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
     return cudaErrorNotSupported;
   const int sms = sm_count();
   const int MT = a.M <= 8 ? 1 : 2;
-  // Pick the k split by a small cost model: rounds of resident CTAs times the
-  // chunks each warp streams per tile group, plus a per-round cost for the
-  // split-K reduction.
+  // Pick the k split and the chunks per warp and stage by a small cost
+  // model: rounds of resident CTAs times the chunks each warp streams per
+  // tile group, plus a per-stage cost for the ring bookkeeping and a
+  // per-round cost for the split-K reduction.
   Choice best{}, ch{};
   bool have = false;
   double best_cost = 0.0;
   for (int KS = 1; KS <= 128; KS *= 2) {
-    if (!layout_for(a, KS, ch)) continue;
-    const int per_sm = (MT == 1 && ch.smem <= static_cast<size_t>(kSmemBudget)) ? 2 : 1;
-    const int64_t resident = std::max<int64_t>(1, int64_t(sms) * per_sm / ch.cluster);
-    const int64_t rounds = ceil_div(ch.tg, resident);
-    const double per_round = double(ch.R) + (KS > 1 ? 2.0 : 0.0) + (ch.cluster > 1 ? 1.0 : 0.0);
-    const double cost = double(rounds) * per_round;
-    if (!have || cost < best_cost) {
-      best = ch;
-      best_cost = cost;
-      have = true;
+    for (int cpw = 1; cpw <= 4; cpw *= 2) {
+      if (!layout_for(a, KS, cpw, ch)) continue;
+      const int per_sm = (MT == 1 && ch.smem <= static_cast<size_t>(kSmemBudget)) ? 2 : 1;
+      const int64_t resident = std::max<int64_t>(1, int64_t(sms) * per_sm / ch.cluster);
+      const int64_t rounds = ceil_div(ch.tg, resident);
+      const double per_round = double(ch.R) * (cpw + 0.6) + (KS > 1 ? 2.0 : 0.0) +
+                               (ch.cluster > 1 ? 1.0 : 0.0);
+      const double cost = double(rounds) * per_round;
+      if (!have || cost < best_cost - 1e-9) {
+        best = ch;
+        best_cost = cost;
+        have = true;
+      }
     }
   }
   if (!have) return cudaErrorNotSupported;
@@ -675,7 +693,7 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   p.nprob = a.count;
   int64_t tg = 0;
   for (int i = 0; i < a.count; ++i) {
-    const cudaError_t e = weight_maps(a, i, best.tpc, best.ksw, p);
+    const cudaError_t e = weight_maps(a, i, best.tpc, best.ksw * best.cpw, p);
     if (e != cudaSuccess) return e;
     p.bias[i] = a.bias[i];
     p.Y[i] = a.Y[i];
@@ -696,6 +714,8 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   p.tpc = best.tpc;
   p.cluster = best.cluster;
   p.R = best.R;
+  p.cpw = best.cpw;
+  p.scs = best.ksw * best.cpw;
 
   // Persistent grid: every tile group gets a CTA (cluster) when they fit in
   // the CTAs resident at once; otherwise CTAs walk the groups.
