@@ -58,7 +58,10 @@ constexpr int kBarConsumers = 1;           // named barrier id for consumers
 // Shared memory per CTA small enough that a CTA of the next launch fits
 // beside a running one on the same SM.
 constexpr int kSmemBudget = 112 * 1024;
+constexpr int kSmemMax = 227 * 1024;  // one CTA per SM
 constexpr int kMaxStages = 8;
+constexpr int kStageBatch = 4;  // activation pieces a thread loads before converting
+constexpr int kPrefetchStages = 1;  // weight stages issued before the upstream kernel ends
 
 struct GemvParams {
   CUtensorMap tmw[kMaxGroup];  // codes: {128 words, K64 chunks, N16 tiles}
@@ -71,9 +74,10 @@ struct GemvParams {
   int nprob, tg_total;
   int M, K, K64, nb;
   int a_f32, a_vec;
+  int a_bulk;  // bf16 rows TMA can copy (16-byte aligned, K % 8 == 0)
   int ksw, tpc, cluster, R;  // k slices per CTA, tiles per group, stages per tile group
   int cpw, scs;              // chunks per warp and stage; chunks per stage and tile (ksw*cpw)
-  int krp, sg;               // staged activation row stride, granules per row
+  int krp, sg;               // staged activation row stride, block sums per row
   int nst, stage_bytes, stage_tx;  // ring depth, stage stride, bytes per stage
   int st_sc, st_zp;  // offsets of scales and zero points in a stage (128-aligned)
   int nbs, nps;      // blocks and zero-point word pairs per stage and tile
@@ -83,10 +87,6 @@ struct GemvParams {
 template <int BS>
 struct BlockGeom {
   static constexpr int kLog2 = BS == 16 ? 4 : BS == 32 ? 5 : BS == 64 ? 6 : BS == 128 ? 7 : 8;
-  static constexpr int kGranule = BS < kChunkK ? BS : kChunkK;
-  static constexpr int kChunksPerBlock = BS > kChunkK ? BS / kChunkK : 1;
-  static constexpr int kBlocksPerChunk = BS < kChunkK ? kChunkK / BS : 1;
-  static constexpr int kChunkShift = kLog2 > 6 ? kLog2 - 6 : 0;  // chunk -> block
 };
 
 // Problem of global tile group gi (the group table is tiny: linear scan).
@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   float *sPart = reinterpret_cast<float *>(smem + p.off_part);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
   uint64_t *empty = full + kMaxStages;
+  uint64_t *abar = empty + kMaxStages;  // activation copy
   unsigned char *ring = smem + p.off_ring;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       mbar_init(full + i, 1);
       mbar_init(empty + i, kConsumerWarps);
     }
+    mbar_init(abar, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -181,17 +183,39 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     // barriers of each tile group right after issuing its last stage, and
     // only then prefetches the next group, so it never waits on a slot that
     // only a later group would free.
+    // Only the first kPrefetchStages stages go out before the upstream
+    // kernel has finished; the activation copy follows them, so it does
+    // not queue behind the whole weight stream, then the rest.
     // Ring position: slot, its use count parity, and whether it was used.
     int slot = 0;
     uint32_t phase = 0;
     bool wrapped = false;
     bool ok = true;
+    int issued = 0;
+    bool a_issued = false;
+    auto issue_a = [&] {
+      grid_dependency_wait();
+      if (p.a_bulk && lane == 0) {
+        const int64_t k0 = int64_t(clo) * kChunkK;
+        const int kr = p.scs * p.R * kChunkK;
+        const int n = p.K - k0 < kr ? static_cast<int>(p.K - k0) : kr;
+        mbar_arrive_expect_tx(abar, static_cast<uint32_t>(p.M) * n * 2);
+        for (int m = 0; m < p.M; ++m)
+          bulk_copy_g2s(sA + m * p.krp,
+                        static_cast<const uint16_t *>(p.A) + int64_t(m) * p.K + k0,
+                        static_cast<uint32_t>(n) * 2, abar);
+      }
+      __syncwarp();
+      a_issued = true;
+    };
     for (int u = 0;; ++u) {
       const int gi = gfirst + u * gstride;
       if (gi >= p.tg_total) break;
       const int q = problem_of(p, gi);
       const int tile0 = (gi - p.tg_begin[q]) * p.tpc;
       for (int j = 0; j < p.R && ok; ++j) {
+        if (!a_issued && issued == kPrefetchStages) issue_a();
+        ++issued;
         if (wrapped && !mbar_wait(empty + slot, phase ^ 1)) {
           if (lane == 0) record_fault(&g_fault_gemv, kFaultGemvWait);
           ok = false;
@@ -215,10 +239,13 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         }
       }
       if (p.cluster > 1) {
+        // The consumers reach these barriers only after the activations.
+        if (!a_issued) issue_a();
         cluster_sync_all();
         cluster_sync_all();
       }
     }
+    if (!a_issued) issue_a();
   } else {
     // ---- consumers ---------------------------------------------------------------
     const int g = lane >> 2, t = lane & 3;
@@ -230,42 +257,86 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     grid_dependency_wait();
 
     // Stage A rows [0, M) over the CTA's k range as bf16 (fp32 activations
-    // as hi + lo) and the sum of every granule (block, or 64-wide piece of a
-    // block) of the staged values, so the code offset 128 cancels exactly up
-    // to fp32 rounding.
+    // as hi + lo) and the sum of every block of the staged values, so the
+    // code offset 128 cancels exactly up to fp32 rounding.
     const int ppr = p.scs * p.R * (kChunkK / 8);  // 8-element pieces per row
     const int npieces = p.M * ppr;
-    {
-      constexpr int gp = G::kGranule / 8;
+    constexpr int gp = BS / 8;  // pieces per block, consecutive lanes
+    bool fault = false;
+    if (p.a_bulk) {
+      // bf16 rows: the producer copies the part inside K with one bulk copy
+      // per row; zeros past K.
+      const int64_t k0 = int64_t(clo) * kChunkK;
+      const int kr = ppr * 8;
+      const int n = p.K - k0 < kr ? static_cast<int>(p.K - k0) : kr;
+      for (int e = n + tid; e < kr; e += kConsumers)
+        for (int m = 0; m < p.M; ++m) sA[m * p.krp + e] = 0;
+      if (!mbar_wait(abar, 0)) {
+        record_fault(&g_fault_gemv, kFaultGemvWait);
+        fault = true;
+      }
+      named_barrier_sync(kBarConsumers, kConsumers);  // zero tails visible
       for (int base = 0; base < npieces; base += kConsumers) {
         const int pc2 = base + tid;
         const bool ok = pc2 < npieces;
+        const int m = ok ? pc2 / ppr : 0;
+        const int kp = pc2 - m * ppr;
         float part = 0.f;
-        int m = 0, kp = 0;
         if (ok) {
-          m = pc2 / ppr;
-          kp = pc2 - m * ppr;
-          float v[8];
-          load8(p, m, (int64_t)clo * kChunkK + kp * 8, v);
-          uint32_t hi[4], lo[4];
+          const uint4 x = *reinterpret_cast<const uint4 *>(sA + m * p.krp + kp * 8);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t h0 = bf16_bits(v[2 * q]), h1 = bf16_bits(v[2 * q + 1]);
-            hi[q] = h0 | (h1 << 16);
-            const float f0 = bf16_bits_to_f32(h0), f1 = bf16_bits_to_f32(h1);
-            const uint32_t l0 = bf16_bits(v[2 * q] - f0), l1 = bf16_bits(v[2 * q + 1] - f1);
-            lo[q] = l0 | (l1 << 16);
-            part += (f0 + bf16_bits_to_f32(l0)) + (f1 + bf16_bits_to_f32(l1));
-          }
-          const int off = m * p.krp + kp * 8;
-          *reinterpret_cast<uint4 *>(sA + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          if (p.a_f32)
-            *reinterpret_cast<uint4 *>(sAlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          for (int e = 0; e < 4; ++e)
+            part += bf16_bits_to_f32(w[e] & 0xFFFFu) + bf16_bits_to_f32(w[e] >> 16);
         }
-        // Pieces of one granule sit in consecutive lanes (ppr is a multiple of 8).
 #pragma unroll
         for (int o = 1; o < gp; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (ok && (kp % gp) == 0) sS[m * p.sg + kp / gp] = part;
+      }
+    } else {
+      // Each thread first issues the loads of up to kStageBatch pieces,
+      // then converts them.
+      for (int base = 0; base < npieces; base += kConsumers * kStageBatch) {
+        float v[kStageBatch][8];
+#pragma unroll
+        for (int q = 0; q < kStageBatch; ++q) {
+          const int pc2 = base + q * kConsumers + tid;
+          if (pc2 < npieces) {
+            const int m = pc2 / ppr;
+            load8(p, m, (int64_t)clo * kChunkK + (pc2 - m * ppr) * 8, v[q]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[q][e] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kStageBatch; ++q) {
+          const int pc2 = base + q * kConsumers + tid;
+          if (base + q * kConsumers >= npieces) break;  // warp-uniform
+          const bool ok = pc2 < npieces;
+          const int m = ok ? pc2 / ppr : 0;
+          const int kp = pc2 - m * ppr;
+          float part = 0.f;
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t h0 = bf16_bits(v[q][2 * e]), h1 = bf16_bits(v[q][2 * e + 1]);
+            hi[e] = h0 | (h1 << 16);
+            const float f0 = bf16_bits_to_f32(h0), f1 = bf16_bits_to_f32(h1);
+            const uint32_t l0 = bf16_bits(v[q][2 * e] - f0), l1 = bf16_bits(v[q][2 * e + 1] - f1);
+            lo[e] = l0 | (l1 << 16);
+            part += (f0 + bf16_bits_to_f32(l0)) + (f1 + bf16_bits_to_f32(l1));
+          }
+          if (ok) {
+            const int off = m * p.krp + kp * 8;
+            *reinterpret_cast<uint4 *>(sA + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            if (p.a_f32)
+              *reinterpret_cast<uint4 *>(sAlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+#pragma unroll
+          for (int o = 1; o < gp; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+          if (ok && (kp % gp) == 0) sS[m * p.sg + kp / gp] = part;
+        }
       }
     }
     named_barrier_sync(kBarConsumers, kConsumers);
@@ -273,23 +344,24 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     constexpr int MC = MT * 8;
     const int rows = p.tpc * kTileN;
     // Activation fragments this lane reads (rows >= M stay zero) and the
-    // granule sums its accumulator columns need (rows >= M read row 0 and
+    // block sums its accumulator columns need (rows >= M read row 0 and
     // meet zero activations).
     const bool mok0 = g < p.M, mok1 = 8 + g < p.M;
     const uint16_t *arow0 = sA + (mok0 ? g : 0) * p.krp + 4 * t - clo * kChunkK;
     const uint16_t *arow1 = sA + (mok1 ? 8 + g : 0) * p.krp + 4 * t - clo * kChunkK;
     const int lo_off = static_cast<int>(sAlo - sA);
     const bool two = p.a_f32 != 0;
+    const int blo = (clo * kChunkK) >> G::kLog2;  // first block of the CTA's k range
     const float *srow[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int m = mt * 8 + 2 * t + h;
-        srow[mt][h] = sS + (m < p.M ? m : 0) * p.sg - clo * (kChunkK / G::kGranule);
+        srow[mt][h] = sS + (m < p.M ? m : 0) * p.sg - blo;
       }
     const bool direct = p.ksw == 1 && p.cluster == 1;
-    // This warp's slices of a stage: its chunk, and its tile's scales and
+    // This warp's slices of a stage: its chunks, and its tile's scales and
     // zero-point pairs (stage block b0s = first block of the stage).
     const int cofs = (tau * p.scs + ks * p.cpw) * kChunkBytes + lane * 16;
     const int sofs = p.st_sc + tau * p.nbs * kTileN * kEs;
@@ -297,19 +369,16 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     uint2 bfrag0 = make_uint2(0, 0), bfrag1 = make_uint2(0, 0);
     int slot = 0;
     uint32_t phase = 0;
-    bool fault = false;
 
     for (int u = 0;; ++u) {
       const int gi = gfirst + u * gstride;
       if (gi >= p.tg_total) break;
       const int q = problem_of(p, gi);
-      float acc[MT][4], d[MT][4], srun[MT][2];
+      float acc[MT][4];
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][e] = d[mt][e] = 0.f;
-        srun[mt][0] = srun[mt][1] = 0.f;
-      }
+        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
       for (int j = 0; j < p.R && !fault; ++j) {
         if (!mbar_wait(full + slot, phase)) {
@@ -320,10 +389,13 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         const unsigned char *st = ring + slot * p.stage_bytes;
         const int cst = cbase + j * p.scs;                            // warp's first chunk
         const int b0s = ((cst - ks * p.cpw) * kChunkK) >> G::kLog2;  // stage's first block
+        const unsigned char *wp = st + cofs;
+        const uint16_t *ap0 = arow0 + cst * kChunkK;
+        const uint16_t *ap1 = arow1 + cst * kChunkK;
 
-        // Applies scale and zero point of block b to the block's MMA sums.
+        // Applies scale and zero point of block b to its MMA sums d.
         // Blocks past the last real one arrive zero-filled: scale 0.
-        auto correct = [&](int b, int gran) {
+        auto correct = [&](int b, float (&d)[MT][4]) {
           const int bi = b - b0s;
           float s0, s1, z0 = 136.f, z1 = 136.f;
           if (SF32) {
@@ -337,76 +409,78 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           }
           if (HAS_ZP) {
             // b's word in the staged word pairs (the first pair holds b0s).
-            const uint2 zw = reinterpret_cast<const uint2 *>(st + zofs)
-                [b - (b0s & ~1)];
+            const uint2 zw = reinterpret_cast<const uint2 *>(st + zofs)[b - (b0s & ~1)];
             z0 = static_cast<float>(128 + ((zw.x >> (4 * g)) & 15));
             z1 = static_cast<float>(128 + ((zw.y >> (4 * g)) & 15));
           }
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            float S0, S1;
-            if (BS >= kChunkK) {
-              S0 = srun[mt][0];
-              S1 = srun[mt][1];
-              srun[mt][0] = srun[mt][1] = 0.f;
-            } else {
-              S0 = srow[mt][0][gran];
-              S1 = srow[mt][1][gran];
-            }
+            const float S0 = srow[mt][0][b], S1 = srow[mt][1][b];
             acc[mt][0] = fmaf(s0, fmaf(-z0, S0, d[mt][0]), acc[mt][0]);
             acc[mt][1] = fmaf(s0, fmaf(-z0, S1, d[mt][1]), acc[mt][1]);
             acc[mt][2] = fmaf(s1, fmaf(-z1, S0, d[mt][2]), acc[mt][2]);
             acc[mt][3] = fmaf(s1, fmaf(-z1, S1, d[mt][3]), acc[mt][3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) d[mt][e] = 0.f;
           }
         };
 
-#pragma unroll 1
-        for (int i = 0; i < p.cpw; ++i) {
-          const int c = cst + i;
-          if (BS >= kChunkK) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              srun[mt][0] += srow[mt][0][c];
-              srun[mt][1] += srow[mt][1][c];
-            }
-          }
-          const uint4 w4 = *reinterpret_cast<const uint4 *>(st + cofs + i * kChunkBytes);
-          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-          const uint16_t *a0 = arow0 + c * kChunkK;
-          const uint16_t *a1 = arow1 + c * kChunkK;
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            uint32_t wf[4];
-            codes_to_bf16x2(wv[jj], wf);
-            lds64_if(mok0, bfrag0, a0 + 16 * jj);
+        // One 16-wide k step of chunk ci (relative to cst): convert the
+        // lane's codes, multiply with the activation fragments; the first
+        // step of a block starts its sums from zero.
+        auto kstep = [&](uint32_t w, int ci, int jj, bool first, float (&d)[MT][4]) {
+          uint32_t wf[4];
+          codes_to_bf16x2(w, wf);
+          const int ko = ci * kChunkK + 16 * jj;
+          if (mok0) bfrag0 = *reinterpret_cast<const uint2 *>(ap0 + ko);
+          if (first) mma_bf16_16816_zero(d[0], wf, bfrag0.x, bfrag0.y);
+          else mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
+          if (two) {
+            if (mok0) bfrag0 = *reinterpret_cast<const uint2 *>(ap0 + lo_off + ko);
             mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
+          }
+          if (MT == 2) {
+            if (mok1) bfrag1 = *reinterpret_cast<const uint2 *>(ap1 + ko);
+            if (first) mma_bf16_16816_zero(d[MT - 1], wf, bfrag1.x, bfrag1.y);
+            else mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
             if (two) {
-              lds64_if(mok0, bfrag0, a0 + lo_off + 16 * jj);
-              mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
-            }
-            if (MT == 2) {
-              lds64_if(mok1, bfrag1, a1 + 16 * jj);
+              if (mok1) bfrag1 = *reinterpret_cast<const uint2 *>(ap1 + lo_off + ko);
               mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
-              if (two) {
-                lds64_if(mok1, bfrag1, a1 + lo_off + 16 * jj);
-                mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
-              }
-            }
-            if (BS < kChunkK && ((jj + 1) % (BS / 16)) == 0) {
-              const int b = (c * kChunkK >> G::kLog2) + jj / (BS / 16);
-              correct(b, b);
             }
           }
-          // Blocks of a chunk or larger end where this warp's next chunk (the
-          // next one in the stage, else scs - cpw + 1 further on) falls in
-          // another block, or with its k range.
-          if (BS >= kChunkK) {
-            const int next = (i + 1 < p.cpw) ? c + 1 : c + p.scs - p.cpw + 1;
-            if ((next >> G::kChunkShift) != (c >> G::kChunkShift) ||
-                (j + 1 == p.R && i + 1 == p.cpw))
-              correct(c >> G::kChunkShift, 0);
+        };
+
+        if (BS >= kChunkK) {
+          // The warp's chunks of a stage are whole blocks of BS/64 chunks.
+          constexpr int kCpb = BS >= kChunkK ? BS / kChunkK : 1;
+          const int cb0 = (cst * kChunkK) >> G::kLog2;
+#pragma unroll 1
+          for (int ub = 0; ub < p.cpw / kCpb; ++ub) {
+            float d[MT][4];
+#pragma unroll
+            for (int cc = 0; cc < kCpb; ++cc) {
+              const int ci = ub * kCpb + cc;
+              const uint4 w4 = *reinterpret_cast<const uint4 *>(wp + ci * kChunkBytes);
+              kstep(w4.x, ci, 0, cc == 0, d);
+              kstep(w4.y, ci, 1, false, d);
+              kstep(w4.z, ci, 2, false, d);
+              kstep(w4.w, ci, 3, false, d);
+            }
+            correct(cb0 + ub, d);
+          }
+        } else {
+          constexpr int kSpb = BS / 16;  // k steps per block
+#pragma unroll 1
+          for (int ci = 0; ci < p.cpw; ++ci) {
+            const uint4 w4 = *reinterpret_cast<const uint4 *>(wp + ci * kChunkBytes);
+            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+            const int cb0 = ((cst + ci) * kChunkK) >> G::kLog2;
+#pragma unroll
+            for (int bb = 0; bb < 4 / kSpb; ++bb) {
+              float d[MT][4];
+#pragma unroll
+              for (int jj = 0; jj < kSpb; ++jj)
+                kstep(wv[bb * kSpb + jj], ci, bb * kSpb + jj, jj == 0, d);
+              correct(cb0 + bb, d);
+            }
           }
         }
         // The stage slice is consumed: release it to the producer.
@@ -487,22 +561,27 @@ struct Choice {
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
 
-bool layout_for(const GroupArgs &a, int KS, int cpw, Choice &ch) {
+// Chunks a warp takes per stage at least: whole blocks for blocks of a
+// chunk or more.
+int min_cpw(int bs) { return bs > kChunkK ? bs / kChunkK : 1; }
+
+bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   const int64_t K64 = ceil_div(a.K, kChunkK);
-  if ((KS > 1 || cpw > 1) && int64_t(KS) * cpw > K64) return false;
-  const int ksw = KS < kConsumerWarps ? KS : kConsumerWarps;
-  const int cluster = KS / ksw;
-  if (cluster > 8) return false;
+  const int KS = ksw * cluster;  // k ranges per tile group
+  // More chunks per warp than blocks need only while the split still
+  // covers K with them.
+  if (cpw < min_cpw(a.bs) || (cpw > min_cpw(a.bs) && int64_t(KS) * cpw > K64)) return false;
   const int tpc = kConsumerWarps / ksw;
   const int scs = ksw * cpw;
+  // Every CTA of a cluster starts inside K.
+  if (int64_t(cluster - 1) * scs * ceil_div(K64, int64_t(KS) * cpw) >= K64) return false;
   int64_t tg = 0;
   for (int i = 0; i < a.count; ++i) tg += ceil_div(ceil_div(a.N[i], kTileN), tpc);
   const int MT = a.M <= 8 ? 1 : 2;
   const int R = static_cast<int>(ceil_div(K64, int64_t(KS) * cpw));
   const int64_t kr = int64_t(scs) * R * kChunkK;  // staged activations per row
   const int krp = static_cast<int>(kr) + 16;
-  const int granule = a.bs < kChunkK ? a.bs : kChunkK;
-  const int sg = static_cast<int>(kr / granule);
+  const int sg = static_cast<int>(kr / a.bs);  // block sums per staged row
   const int es = a.scale_f32 ? 4 : 2;
   // A stage holds scs consecutive chunks (scs * 64 k) of tpc tiles, the
   // nbs blocks they touch (stage starts are multiples of scs chunks, so for
@@ -527,13 +606,13 @@ bool layout_for(const GroupArgs &a, int KS, int cpw, Choice &ch) {
   L.off_part = static_cast<int>(off);
   if (cluster > 1) off += align16(size_t(tpc) * kTileN * a.M * 4);
   L.off_bar = static_cast<int>(off);
-  off += 2 * kMaxStages * 8;
+  off += (2 * kMaxStages + 1) * 8;
   off = align128(off);
   L.off_ring = static_cast<int>(off);
   // Ring depth: as many stages as fit, at most kMaxStages, at least 2; stay
   // within the two-CTAs-per-SM budget when the layout allows it.
   size_t cap = kSmemBudget;
-  if (MT == 2 || off + 2 * size_t(L.stage_bytes) > cap) cap = 2 * kSmemBudget - 24 * 1024;
+  if (MT == 2 || off + 2 * size_t(L.stage_bytes) > cap) cap = kSmemMax;
   if (off + 2 * size_t(L.stage_bytes) > cap) return false;
   int nst = static_cast<int>((cap - off) / L.stage_bytes);
   nst = std::min(nst, kMaxStages);
@@ -563,7 +642,7 @@ cudaError_t launch_one(const GemvParams &p, const Choice &ch, int grid, bool pdl
   static bool configured = false;
   if (!configured) {
     const cudaError_t e = cudaFuncSetAttribute(
-        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kSmemBudget);
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -670,22 +749,22 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   Choice best{}, ch{};
   bool have = false;
   double best_cost = 0.0;
-  for (int KS = 1; KS <= 128; KS *= 2) {
-    for (int cpw = 1; cpw <= 4; cpw *= 2) {
-      if (!layout_for(a, KS, cpw, ch)) continue;
-      const int per_sm = (MT == 1 && ch.smem <= static_cast<size_t>(kSmemBudget)) ? 2 : 1;
-      const int64_t resident = std::max<int64_t>(1, int64_t(sms) * per_sm / ch.cluster);
-      const int64_t rounds = ceil_div(ch.tg, resident);
-      const double per_round = double(ch.R) * (cpw + 0.6) + (KS > 1 ? 2.0 : 0.0) +
-                               (ch.cluster > 1 ? 1.0 : 0.0);
-      const double cost = double(rounds) * per_round;
-      if (!have || cost < best_cost - 1e-9) {
-        best = ch;
-        best_cost = cost;
-        have = true;
+  for (int ksw = 1; ksw <= kConsumerWarps; ksw *= 2)
+    for (int cluster = 1; cluster <= 8; cluster *= 2)
+      for (int cpw = 1; cpw <= 4; cpw *= 2) {
+        if (!layout_for(a, ksw, cluster, cpw, ch)) continue;
+        const int per_sm = (MT == 1 && ch.smem <= static_cast<size_t>(kSmemBudget)) ? 2 : 1;
+        const int64_t resident = std::max<int64_t>(1, int64_t(sms) * per_sm / cluster);
+        const int64_t rounds = ceil_div(ch.tg, resident);
+        const double per_round = double(ch.R) * (cpw + 0.6) + (ksw * cluster > 1 ? 2.0 : 0.0) +
+                                 (cluster > 1 ? 1.0 : 0.0);
+        const double cost = double(rounds) * per_round;
+        if (!have || cost < best_cost - 1e-9) {
+          best = ch;
+          best_cost = cost;
+          have = true;
+        }
       }
-    }
-  }
   if (!have) return cudaErrorNotSupported;
 
   GemvParams p = best.layout;
@@ -710,6 +789,7 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   p.a_f32 = a.a_f32;
   const int vec_elems = a.a_f32 ? 4 : 8;
   p.a_vec = (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) && (a.K % vec_elems == 0);
+  p.a_bulk = !a.a_f32 && p.a_vec;
   p.ksw = best.ksw;
   p.tpc = best.tpc;
   p.cluster = best.cluster;

@@ -61,41 +61,25 @@ __device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t (&r)[4]) {
   r[3] = lop3_and_or(w >> 12, kMask, kMagic);
 }
 
-// Eight packed codes -> four f16x2 registers, all exact: registers 0 and 2
-// (rows r0) hold q, registers 1 and 3 (rows r0 + 8) hold 1024 + 16 q. One
-// shift, four lop3 (OR-ing a nibble into the mantissa of 1024.0) and two
-// f16x2 subtractions of 1024.
-__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
-  constexpr uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;
-  const uint32_t w8 = w >> 8;
-  r[0] = lop3_and_or(w, kLo, kMagic);
-  r[1] = lop3_and_or(w, kHi, kMagic);
-  r[2] = lop3_and_or(w8, kLo, kMagic);
-  r[3] = lop3_and_or(w8, kHi, kMagic);
-  asm("sub.f16x2 %0, %0, %1;" : "+r"(r[0]) : "r"(kMagic));
-  asm("sub.f16x2 %0, %0, %1;" : "+r"(r[2]) : "r"(kMagic));
-}
-
-// D += A * B, m16n8k16, f16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4],
-                                              const uint32_t (&a)[4],
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4],
                                                const uint32_t (&a)[4],
                                                uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The same product into d, starting from zero sums.
+__device__ __forceinline__ void mma_bf16_16816_zero(float (&d)[4],
+                                                    const uint32_t (&a)[4],
+                                                    uint32_t b0, uint32_t b1) {
+  const float z = 0.f;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
 }
 
 // Streaming 128-bit load of constant data (not kept in L1).
@@ -205,16 +189,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src,
       "[%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
-}
-
-// 8-byte shared-memory load performed only when `pred` holds (v unchanged
-// otherwise); no branch.
-__device__ __forceinline__ void lds64_if(bool pred, uint2 &v, const void *p) {
-  asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
-      "@q ld.shared.v2.u32 {%0, %1}, [%3];\n\t}"
-      : "+r"(v.x), "+r"(v.y)
-      : "r"(static_cast<int>(pred)), "r"(smem_addr(p)));
 }
 
 // 3-D tiled TMA load into this CTA's shared memory, completing on bar.
