@@ -38,6 +38,25 @@ METRIC = "INT4 decode GEMV GB/s and % HBM peak (M=1); prefill TFLOP/s (M=2048)"
 WORKLOAD = "Qwen3-4B decode step projections, M=1, bf16 A, bs 128, no zp"
 
 
+# DRAM read + write per decode-kernel launch of one decode step, from one ncu
+# capture of the 145 launches (dram__bytes_read.sum + dram__bytes_write.sum),
+# valid only for the decode-kernel sources it was measured on.
+STEP_TRAFFIC = {
+    "bytes_per_launch": 14385392,
+    "sources": ("gemv.cu", "mnb_common.cuh", "mnb_launch.h"),
+    "sha256": "69769c30e29066916a7e7b0203d7679c0316761b4d5190f76a5502650af4fe48",
+}
+
+
+def step_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in STEP_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, "int4_weight_only_matmulnbits_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return STEP_TRAFFIC["bytes_per_launch"] if h.hexdigest() == STEP_TRAFFIC["sha256"] else None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -362,10 +381,14 @@ def run_gpu(args, rank, world, dist):
                    "parallelism": f"replicas x{world}"},
         "hbm_fraction": per_gpu / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": per_gpu / hbm_peak, "traffic": None,
+                     "unit": "GB/s", "frac": per_gpu / hbm_peak, "traffic": step_traffic(),
                      "peak_kind": peak_kind,
                      "kernel": "gemv_kernel (every launch of the step)",
-                     "achieved_basis": "algorithmic bytes of the step / device time of the step"},
+                     "achieved_basis": "algorithmic bytes of the step / device time of the "
+                                       "step (= bytes per launch / mean launch time)",
+                     "algorithmic_bytes_per_launch": algo_bytes / launches_per_step,
+                     "traffic_basis": "ncu dram read+write per launch, mean over the "
+                                      "step's 145 launches; null if the kernel changed"},
         "e2e": {"value": e2e, "unit": "GB/s",
                 "h2d_bytes_per_step": A_all.numel() * A_all.element_size(),
                 "d2h_bytes_per_step": Y_all.numel() * Y_all.element_size()},
@@ -375,6 +398,123 @@ def run_gpu(args, rank, world, dist):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# single-kernel cases (for profiler captures) and the GEMV/GEMM crossover sweep
+# ----------------------------------------------------------------------------
+
+def _weights(dev, N, K, bs, sdtype, zp, seed):
+    import torch
+
+    import int4_weight_only_matmulnbits_gb300 as mnb
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    nb = -(-K // bs)
+    B = torch.randint(0, 256, (N, nb, bs // 2), dtype=torch.uint8, device=dev, generator=g)
+    S = (torch.rand(N, nb, device=dev, generator=g) * 0.008 + 0.002).to(sdtype)
+    Z = (torch.randint(0, 256, (N, (nb + 1) // 2), dtype=torch.uint8, device=dev, generator=g)
+         if zp else None)
+    w = mnb.mnb_prepack(B, S, Z, N, K, bs)
+    nbytes = N * nb * bs // 2 + N * nb * S.element_size() + (N * ((nb + 1) // 2) if zp else 0)
+    return w, nbytes
+
+
+def _cold_launch_us(fn, reps, flush):
+    """Median device time of fn, each launch after an L2 flush."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
+CASES = {
+    # name: (M, N, K, bs, A dtype, zero points, bias, path)
+    "single": (1, 3072, 1024, 32, "f32", False, False, "auto"),
+    "gemv_gate": (1, 9728, 2560, 128, "bf16", False, False, "auto"),
+    "gemv_lm_head": (1, 151936, 2560, 128, "bf16", False, False, "auto"),
+    "gemm_gate": (2048, 9728, 2560, 128, "bf16", True, True, "gemm"),
+}
+
+
+def run_case(args):
+    """One kernel shape, --steps cold launches (L2 flushed before each); or one
+    eager decode step per --steps ("step"); or the crossover sweep."""
+    import torch
+
+    import int4_weight_only_matmulnbits_gb300 as mnb
+    dev = torch.device("cuda", 0)
+    mnb.build_library()
+    mnb.load()
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    if args.case == "step":
+        launches, _, _, algo_bytes = build_decode_step(dev)
+        for _ in range(args.steps):
+            for _, ws, A, Ys in launches:
+                if len(ws) == 1:
+                    mnb.mnb_matmul(A, ws[0], None, out=Ys[0])
+                else:
+                    mnb.mnb_matmul_grouped(A, ws, outs=Ys)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": "step", "launches": len(launches) * args.steps,
+                          "algorithmic_bytes_per_step": algo_bytes}))
+        return
+    if args.case == "sweep":
+        return run_sweep(dev, flush)
+    M, N, K, bs, adt, zp, bias, path = CASES[args.case]
+    dt = torch.float32 if adt == "f32" else torch.bfloat16
+    w, wbytes = _weights(dev, N, K, bs, dt, zp, 11)
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    A = torch.randn(M, K, device=dev, generator=g).to(dt)
+    b = torch.randn(N, device=dev, generator=g) * 0.02 if bias else None
+    Y = torch.empty(M, N, dtype=dt, device=dev)
+    us = _cold_launch_us(lambda: mnb.mnb_matmul(A, w, b, out=Y, path=path), args.steps, flush)
+    nbytes = wbytes + A.numel() * A.element_size() + Y.numel() * Y.element_size() + (
+        4 * N if bias else 0)
+    print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "block_size": bs,
+                      "us_per_launch_cold": us, "algorithmic_bytes": nbytes,
+                      "GB_s": nbytes / us / 1e3, "TFLOP_s": 2 * M * N * K / us / 1e6}))
+
+
+def run_sweep(dev, flush):
+    """GEMV and tensor-core GEMM device time per M on the gate and down shapes,
+    per block size, activation dtype and zero points (cold L2, median of 7)."""
+    import torch
+
+    import int4_weight_only_matmulnbits_gb300 as mnb
+    Ms = (1, 2, 4, 8, 16, 32, 64, 256)
+    rows = []
+    for name, N, K in (("gate", 9728, 2560), ("down", 2560, 9728)):
+        for bs in (32, 64, 128):
+            for adt in ("f32", "bf16"):
+                dt = torch.float32 if adt == "f32" else torch.bfloat16
+                for zp in (False, True):
+                    w, _ = _weights(dev, N, K, bs, dt, zp, 21)
+                    for M in Ms:
+                        A = torch.randn(M, K, device=dev).to(dt)
+                        Y = torch.empty(M, N, dtype=dt, device=dev)
+                        t = {}
+                        for path in ("gemv", "gemm", "auto"):
+                            try:
+                                mnb.mnb_matmul(A, w, None, out=Y, path=path)
+                            except mnb.MnbError:
+                                continue
+                            t[path] = _cold_launch_us(
+                                lambda: mnb.mnb_matmul(A, w, None, out=Y, path=path), 7, flush)
+                        rows.append({"shape": name, "bs": bs, "a": adt, "zp": zp, "M": M, **t})
+                        print(json.dumps(rows[-1]), flush=True)
+                    del w
+                    torch.cuda.empty_cache()
+    return rows
 
 
 def main():
@@ -387,7 +527,13 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=8.0)
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--case", default=None, choices=sorted(CASES) + ["step", "sweep"],
+                    help="run one kernel shape (or one eager decode step per --steps, or "
+                         "the GEMV/GEMM crossover sweep) instead of the benchmark")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", 1))
     rank = int(os.environ.get("RANK", 0))
