@@ -8,23 +8,27 @@
 // matrix is never expanded: only one 128 x 64 bf16 slice per pipeline stage
 // exists, in shared memory.
 //
-// GB300 mapping (one CTA per 128 x BN output tile, two CTAs per SM so one
-// CTA's epilogue overlaps the other's main loop):
+// GB300 mapping (one CTA per (128*MH) x 128 output tile, MH = 1 or 2 halves
+// of 128 rows; two CTAs per SM so one CTA's epilogue overlaps the other's
+// main loop):
 //  * warp 0, one thread: TMA producer. Per 64-wide k stage it loads the A
-//    tile (128 x 64 bf16, 128-byte swizzle), the BN x 64 packed codes of the
-//    stage and their scales and zero points into a three-deep input ring,
+//    tile ((128*MH) x 64 bf16, 128-byte swizzle), the 128 x 64 packed codes
+//    of the stage and their scales and zero points into the input ring,
 //    completing on full[s].
 //  * warps 2-9, one 16-row weight tile each: dequantise the stage's codes to
 //    bf16 (q - z) * s (the difference is exact; one rounding in the product)
 //    into a two-deep ring of B tiles in the K-major, 128-byte-swizzled layout
 //    tcgen05.mma reads, fence the writes to the async proxy and arrive on
-//    bfull[b].
-//  * warp 1: allocates the TMEM accumulator (128 lanes x BN fp32 columns);
-//    one thread issues four tcgen05.mma (M=128, N=BN, K=16) per stage and
-//    commits each stage to empty[s] and bempty[b], the last one to acc_full.
-//  * warps 2-9 then read the accumulator with tcgen05.ld (each warp its
-//    TMEM lane quarter and half of the columns), add the bias, round to
-//    bf16 and store Y.
+//    bfull[b]. Weight rows g and g+8 of a 16-row tile go to B rows 2g and
+//    2g+1, which keeps every warp's stores free of bank conflicts; the
+//    epilogue maps the columns back.
+//  * warp 1: allocates the TMEM accumulators (128 lanes x 128*MH fp32
+//    columns); one thread issues 4*MH tcgen05.mma (M=128, N=128, K=16) per
+//    stage, the MH halves of A sharing the B tile, and commits each stage to
+//    empty[s] and bempty[b], the last one to acc_full.
+//  * warps 2-9 then read the accumulators with tcgen05.ld (each warp its
+//    TMEM lane quarter and half of the columns), add the bias (staged in
+//    shared memory), round to bf16 and store Y.
 // Every mbarrier wait is bounded; a wait that runs out records a fault bit
 // and the kernel abandons the tile.
 #include <cuda_bf16.h>
@@ -38,20 +42,20 @@ __device__ unsigned int g_fault_gemm = 0;
 
 namespace {
 
-constexpr int kBM = 128;
+constexpr int kBH = 128;  // rows of one A half (the MMA's M)
 constexpr int kBN = 128;
 constexpr int kBK = 64;  // one chunk of the packed layout
-constexpr int kStages = 3;   // input ring: A, codes, scales, zero points
 constexpr int kBStages = 2;  // dequantised B tiles
 constexpr int kDqWarps = 8;
 constexpr int kThreads = 32 * (2 + kDqWarps);
 constexpr int kTilesN = kBN / kTileN;
-constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
+constexpr int kAHalfBytes = kBH * kBK * 2;  // 16 KB
 constexpr int kBTileBytes = kBN * kBK * 2;  // 16 KB
 constexpr int kCodeBytes = kTilesN * kChunkBytes;  // 4 KB
+constexpr int kBarEpi = 1;  // named barrier of the dequantisation/epilogue warps
 
 struct GemmParams {
-  CUtensorMap tma;  // A: {K, M} bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap tma;  // A: {K, M} bf16, box {64, 128*MH}, 128-byte swizzle
   CUtensorMap tmw;  // codes: {128 words, K64, N16}, box {128, 1, 8}
   CUtensorMap tms;  // scales: {16 scales as words, nb, N16}, box {.., bpc, 8}
   CUtensorMap tmz;  // zero points: {4 words, nbz/2, N16}, box {4, ppc, 8}
@@ -64,7 +68,10 @@ struct GemmParams {
 };
 
 // Shared-memory plan (offsets from a 1024-aligned base).
+template <int MH>
 struct Smem {
+  static constexpr int kStages = MH == 1 ? 3 : 2;  // input ring depth
+  static constexpr int kATileBytes = MH * kAHalfBytes;
   static constexpr int kA = 0;
   static constexpr int kB = kA + kStages * kATileBytes;
   static constexpr int kCodes = kB + kBStages * kBTileBytes;
@@ -72,13 +79,15 @@ struct Smem {
   static constexpr int kScBytes = 2048;  // 8 tiles x up to 4 blocks x 16 fp32 scales
   static constexpr int kZp = kSc + kStages * kScBytes;
   static constexpr int kZpBytes = 256;  // 8 tiles * 2 pairs * 16 bytes
-  static constexpr int kBar = kZp + kStages * kZpBytes;
+  static constexpr int kBias = kZp + kStages * kZpBytes;
+  static constexpr int kBar = kBias + kBN * 4;
   static constexpr int kTmemSlot = kBar + (2 * kStages + 2 * kBStages + 1) * 8;
   static constexpr int kTotal = kTmemSlot + 16;
 };
 // Two CTAs share an SM: each may use at most half of its 228 KB, less the
 // 1 KB the runtime reserves per CTA and the 1 KB alignment slack.
-static_assert(Smem::kTotal + 1024 <= (228 * 1024) / 2 - 1024, "two CTAs per SM");
+static_assert(Smem<1>::kTotal + 1024 <= (228 * 1024) / 2 - 1024, "two CTAs per SM");
+static_assert(Smem<2>::kTotal + 1024 <= (228 * 1024) / 2 - 1024, "two CTAs per SM");
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   // K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms of
@@ -95,7 +104,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 // Instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = kBN.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);
+                            (static_cast<uint32_t>(kBH >> 4) << 24);
 
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                           bool accumulate) {
@@ -164,21 +173,29 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t v, uint32_t zc, uint32
   return bf16_bits(lo) | (bf16_bits(hi) << 16);
 }
 
-template <int BS, bool HAS_ZP, bool SF32>
+// Output column (within the CTA's 128) of B row / accumulator column c.
+__host__ __device__ constexpr int out_col(int c) {
+  return (c & ~15) + ((c & 1) ? 8 : 0) + ((c & 15) >> 1);
+}
+
+template <int BS, bool HAS_ZP, bool SF32, int MH>
 __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant__ GemmParams p) {
+  using S = Smem<MH>;
+  constexpr int kStages = S::kStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles.
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Smem::kBar);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBar);
   uint64_t *empty = full + kStages;
   uint64_t *bfull = empty + kStages;
   uint64_t *bempty = bfull + kBStages;
   uint64_t *acc_full = bempty + kBStages;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::kTmemSlot);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kTmemSlot);
+  float *sBias = reinterpret_cast<float *>(smem + S::kBias);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.y * kBM;
+  const int m0 = blockIdx.y * (kBH * MH);
   const int nt0 = blockIdx.x * kTilesN;  // first 16-row weight tile
   constexpr int kBpc = BS < kBK ? kBK / BS : 1;
 
@@ -197,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
-                 "r"(kBN)
+                 "r"(kBN * MH)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -221,13 +238,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
           break;
         }
         uint64_t *bar = full + s;
-        mbar_arrive_expect_tx(bar, kATileBytes + kCodeBytes + p.sc_bytes + p.zp_bytes);
+        mbar_arrive_expect_tx(bar, S::kATileBytes + kCodeBytes + p.sc_bytes + p.zp_bytes);
         const int blk = (kb * kBK) / BS;
-        tma_load_2d(smem + Smem::kA + s * kATileBytes, &p.tma, kb * kBK, m0, bar);
-        tma_load_3d(smem + Smem::kCodes + s * kCodeBytes, &p.tmw, 0, kb, nt0, bar);
-        tma_load_3d(smem + Smem::kSc + s * Smem::kScBytes, &p.tms, 0, blk, nt0, bar);
+        tma_load_2d(smem + S::kA + s * S::kATileBytes, &p.tma, kb * kBK, m0, bar);
+        tma_load_3d(smem + S::kCodes + s * kCodeBytes, &p.tmw, 0, kb, nt0, bar);
+        tma_load_3d(smem + S::kSc + s * S::kScBytes, &p.tms, 0, blk, nt0, bar);
         if (HAS_ZP)
-          tma_load_3d(smem + Smem::kZp + s * Smem::kZpBytes, &p.tmz, 0, blk >> 1, nt0, bar);
+          tma_load_3d(smem + S::kZp + s * S::kZpBytes, &p.tmz, 0, blk >> 1, nt0, bar);
       }
     }
   } else if (warp == 1) {
@@ -241,12 +258,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_addr(smem + Smem::kA + s * kATileBytes);
-        const uint32_t b_base = smem_addr(smem + Smem::kB + b * kBTileBytes);
+        const uint32_t a_base = smem_addr(smem + S::kA + s * S::kATileBytes);
+        const uint32_t b_base = smem_addr(smem + S::kB + b * kBTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          umma_bf16(tmem, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(b_base + kk * 32),
-                    kb > 0 || kk > 0);
+#pragma unroll
+          for (int h = 0; h < MH; ++h)
+            umma_bf16(tmem + h * kBN, smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32),
+                      smem_desc_sw128(b_base + kk * 32), kb > 0 || kk > 0);
         umma_commit(empty + s);
         umma_commit(bempty + b);
       }
@@ -256,7 +275,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
     // ---- dequantisation warps (2..9), then the epilogue --------------------
     const int tile = warp - 2;  // this warp's 16-row weight tile of the stage
     const int g = lane >> 2, t = lane & 3;
-    const int r0 = tile * kTileN + g;  // rows r0 and r0 + 8 of the B tile
+    // Weight rows g and g + 8 of the tile go to B rows 2g and 2g + 1.
+    const int r0 = tile * kTileN + 2 * g;
+    {
+      const int e = tid - 64;  // 0..255
+      if (e < kBN) {
+        const int n = nt0 * kTileN + e;
+        sBias[e] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
+      }
+    }
     for (int kb = 0; kb < p.K64; ++kb) {
       const int s = kb % kStages, bslot = kb % kBStages;
       if (!mbar_wait(full + s, (kb / kStages) & 1) ||
@@ -265,13 +292,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         fault = true;
         break;
       }
-      const unsigned char *codes = smem + Smem::kCodes + s * kCodeBytes;
-      const unsigned char *sc = smem + Smem::kSc + s * Smem::kScBytes;
-      const uint2 *zp = reinterpret_cast<const uint2 *>(smem + Smem::kZp + s * Smem::kZpBytes);
-      unsigned char *btile = smem + Smem::kB + bslot * kBTileBytes;
+      const unsigned char *codes = smem + S::kCodes + s * kCodeBytes;
+      const unsigned char *sc = smem + S::kSc + s * S::kScBytes;
+      const uint2 *zp = reinterpret_cast<const uint2 *>(smem + S::kZp + s * S::kZpBytes);
+      unsigned char *btile = smem + S::kB + bslot * kBTileBytes;
       const int blk0 = (kb * kBK) / BS;
-      // Scales and zero points of rows r0, r0 + 8 for the stage's blocks
-      // (zero-filled past the last block).
+      // Scales and zero points of weight rows g, g + 8 for the stage's
+      // blocks (zero-filled past the last block).
       uint32_t sb0[kBpc], sb1[kBpc], zc0[kBpc], zc1[kBpc];
       float sf0[kBpc], sf1[kBpc];
 #pragma unroll
@@ -303,16 +330,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         const int bi = BS < kBK ? (16 * j) / BS : 0;  // block of this k step
         uint32_t r[4];
         codes_to_bf16x2(wv[j], r);
-        const uint32_t v00 = dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi]);  // row r0
+        const uint32_t v00 = dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi]);  // row g
         const uint32_t v02 = dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi]);
-        const uint32_t v10 = dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi]);  // row r0 + 8
+        const uint32_t v10 = dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi]);  // row g + 8
         const uint32_t v12 = dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi]);
         // K-major 128-byte swizzle: 16-byte chunk (k / 8) XOR (row % 8).
         const int k0 = 16 * j + 4 * t;
-        const int chunk = (k0 >> 3) ^ (r0 & 7);
         const int inner = (k0 & 7) * 2;
-        *reinterpret_cast<uint2 *>(btile + r0 * 128 + chunk * 16 + inner) = make_uint2(v00, v02);
-        *reinterpret_cast<uint2 *>(btile + (r0 + 8) * 128 + chunk * 16 + inner) =
+        *reinterpret_cast<uint2 *>(btile + r0 * 128 + (((k0 >> 3) ^ (r0 & 7)) * 16) + inner) =
+            make_uint2(v00, v02);
+        *reinterpret_cast<uint2 *>(btile + (r0 + 1) * 128 +
+                                   (((k0 >> 3) ^ ((r0 + 1) & 7)) * 16) + inner) =
             make_uint2(v10, v12);
       }
       fence_async_smem();  // make the tile visible to the tensor core
@@ -325,42 +353,39 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
       record_fault(&g_fault_gemm, kFaultGemmWait);
       fault = true;
     }
+    named_barrier_sync(kBarEpi, 32 * kDqWarps);  // bias staged
     if (!fault) {
       tc_fence_after();
       const int quarter = warp & 3;          // TMEM lanes this warp may read
       const int half = (warp - 2) >> 2;      // which half of the columns
-      const int m = m0 + quarter * 32 + lane;
       const int n_base = nt0 * kTileN;
 #pragma unroll 1
-      for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
-        float v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
-        if (m < p.M) {
-          const int n0 = n_base + c * 32;
-          uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
-          if (n0 + 32 <= p.N && p.y_vec) {
+      for (int h = 0; h < MH; ++h) {
+        const int m = m0 + h * kBH + quarter * 32 + lane;
+#pragma unroll 1
+        for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
+          float v[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + h * kBN + c * 32, v);
+          if (m < p.M) {
+            // Accumulator columns c*32 + i hold output columns out_col(c*32 + i):
+            // two whole 16-column tiles, permuted within each.
+            const int n0 = n_base + c * 32;
+            uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
+            float o[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint32_t w[4];
+            for (int i = 0; i < 32; ++i) o[out_col(i)] = v[i] + sBias[c * 32 + out_col(i)];
+            if (n0 + 32 <= p.N && p.y_vec) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float a = v[i + 2 * e], b = v[i + 2 * e + 1];
-                if (p.bias) {
-                  a += __ldg(p.bias + n0 + i + 2 * e);
-                  b += __ldg(p.bias + n0 + i + 2 * e + 1);
-                }
-                w[e] = bf16_bits(a) | (bf16_bits(b) << 16);
+              for (int i = 0; i < 32; i += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  w[e] = bf16_bits(o[i + 2 * e]) | (bf16_bits(o[i + 2 * e + 1]) << 16);
+                *reinterpret_cast<uint4 *>(yrow + n0 + i) = make_uint4(w[0], w[1], w[2], w[3]);
               }
-              *reinterpret_cast<uint4 *>(yrow + n0 + i) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          } else {
-            for (int i = 0; i < 32; ++i) {
-              const int n = n0 + i;
-              if (n < p.N) {
-                float a = v[i];
-                if (p.bias) a += __ldg(p.bias + n);
-                yrow[n] = static_cast<uint16_t>(bf16_bits(a));
-              }
+            } else {
+              for (int i = 0; i < 32; ++i)
+                if (n0 + i < p.N) yrow[n0 + i] = static_cast<uint16_t>(bf16_bits(o[i]));
             }
           }
         }
@@ -372,15 +397,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kBN * MH)
                  : "memory");
   }
 }
 
-template <int BS, bool HAS_ZP, bool SF32>
+template <int BS, bool HAS_ZP, bool SF32, int MH>
 cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
-  auto kernel = gemm_kernel<BS, HAS_ZP, SF32>;
-  const int smem = Smem::kTotal + 1024;
+  auto kernel = gemm_kernel<BS, HAS_ZP, SF32, MH>;
+  const int smem = Smem<MH>::kTotal + 1024;
   static bool configured = false;
   if (!configured) {
     const cudaError_t e =
@@ -401,14 +427,21 @@ cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int BS>
+template <int BS, int MH>
 cudaError_t launch_flags(const GemmParams &p, dim3 grid, bool sf32, bool pdl,
                          cudaStream_t stream) {
   if (p.has_zp)
-    return sf32 ? launch_one<BS, true, true>(p, grid, pdl, stream)
-                : launch_one<BS, true, false>(p, grid, pdl, stream);
-  return sf32 ? launch_one<BS, false, true>(p, grid, pdl, stream)
-              : launch_one<BS, false, false>(p, grid, pdl, stream);
+    return sf32 ? launch_one<BS, true, true, MH>(p, grid, pdl, stream)
+                : launch_one<BS, true, false, MH>(p, grid, pdl, stream);
+  return sf32 ? launch_one<BS, false, true, MH>(p, grid, pdl, stream)
+              : launch_one<BS, false, false, MH>(p, grid, pdl, stream);
+}
+
+template <int BS>
+cudaError_t launch_mh(const GemmParams &p, dim3 grid, int mh, bool sf32, bool pdl,
+                      cudaStream_t stream) {
+  return mh == 2 ? launch_flags<BS, 2>(p, grid, sf32, pdl, stream)
+                 : launch_flags<BS, 1>(p, grid, sf32, pdl, stream);
 }
 
 }  // namespace
@@ -428,6 +461,10 @@ bool gemm_supports(const MatmulArgs &a) {
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   if (!gemm_supports(a)) return cudaErrorNotSupported;
   GemmParams p{};
+  // 256-row tiles (two MMAs per B tile) once they still give every SM two
+  // CTAs; 128-row tiles otherwise.
+  const int64_t tiles256 = ceil_div(a.M, 2 * kBH) * ceil_div(a.N, kBN);
+  const int mh = tiles256 >= 2 * int64_t(sm_count()) ? 2 : 1;
   const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
   const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
   const uint64_t es = a.scale_f32 ? 4 : 2;
@@ -437,7 +474,7 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
-    const uint32_t box[2] = {kBK, kBM};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(kBH * mh)};
     e = make_tmap(&p.tma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.A, dims, strides, box,
                   CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
@@ -478,13 +515,13 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   p.has_zp = a.zp != nullptr;
   p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
   const dim3 grid(static_cast<unsigned>(ceil_div(a.N, kBN)),
-                  static_cast<unsigned>(ceil_div(a.M, kBM)), 1);
+                  static_cast<unsigned>(ceil_div(a.M, int64_t(kBH) * mh)), 1);
   switch (a.bs) {
-    case 16: return launch_flags<16>(p, grid, a.scale_f32, a.pdl, stream);
-    case 32: return launch_flags<32>(p, grid, a.scale_f32, a.pdl, stream);
-    case 64: return launch_flags<64>(p, grid, a.scale_f32, a.pdl, stream);
-    case 128: return launch_flags<128>(p, grid, a.scale_f32, a.pdl, stream);
-    case 256: return launch_flags<256>(p, grid, a.scale_f32, a.pdl, stream);
+    case 16: return launch_mh<16>(p, grid, mh, a.scale_f32, a.pdl, stream);
+    case 32: return launch_mh<32>(p, grid, mh, a.scale_f32, a.pdl, stream);
+    case 64: return launch_mh<64>(p, grid, mh, a.scale_f32, a.pdl, stream);
+    case 128: return launch_mh<128>(p, grid, mh, a.scale_f32, a.pdl, stream);
+    case 256: return launch_mh<256>(p, grid, mh, a.scale_f32, a.pdl, stream);
     default: return cudaErrorNotSupported;
   }
 }

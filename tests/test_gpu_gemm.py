@@ -112,3 +112,22 @@ def test_gemm_bitwise_reproducible(dev):
     prob = make_problem(300, 1000, 2560, 128, dtype=torch.bfloat16, zero_points=True,
                         bias=True, seed=3)
     assert torch.equal(run(prob, dev, "gemm"), run(prob, dev, "gemm"))
+
+
+@pytest.mark.parametrize("bs,with_zp", [(32, True), (64, False), (256, True)])
+def test_gemm_256_row_tiles_with_tails(dev, bs, with_zp):
+    """Enough output tiles for the 256-row tile variant (two A halves per B
+    tile): ragged M (777 = 3*256 + 9) and N (12300 = 96*128 + 12), a partial
+    last block; seeded rows (incl. the first and the last) x columns (incl.
+    the ragged N tail) checked element by element."""
+    M, N, K = 777, 12300, 520
+    prob = make_problem(M, N, K, bs, dtype=torch.bfloat16, zero_points=with_zp, bias=True,
+                        seed=bs + 5)
+    Y = run(prob, dev, path="gemm")
+    rng = np.random.default_rng(bs)
+    rows = np.unique(np.concatenate([[0, 255, 256, 511, 767, 768, M - 1],
+                                     rng.choice(M, 9, replace=False)]))
+    cols = np.unique(np.concatenate([np.arange(N - 12, N), np.arange(0, 16),
+                                     rng.choice(N, 48, replace=False)]))
+    R, mag = ref(prob, rows=rows, cols=cols)
+    check(Y[rows][:, cols], R, mag, f"gemm256 bs{bs}")
