@@ -29,6 +29,12 @@
 //  * warps 2-9 then read the accumulators with tcgen05.ld (each warp its
 //    TMEM lane quarter and half of the columns), add the bias (staged in
 //    shared memory), round to bf16 and store Y.
+//  * Shapes with too few output tiles to fill the GPU split K over a
+//    cluster of up to 8 CTAs (128-row tiles): each CTA accumulates its k
+//    range, parks the accumulator in its own shared memory (the drained
+//    operand rings), and after a cluster barrier each CTA reduces one column
+//    slice of the tile over all ranks through distributed shared memory, in
+//    rank order (bitwise reproducible), then adds the bias and stores.
 // Every mbarrier wait is bounded; a wait that runs out records a fault bit
 // and the kernel abandons the tile.
 #include <cuda_bf16.h>
@@ -65,6 +71,7 @@ struct GemmParams {
   int has_zp;
   int y_vec;  // Y rows are 16-byte aligned: 16-byte stores
   int sc_bytes, zp_bytes;  // per stage
+  int ksplit, kps;  // CTAs splitting K (cluster along z), k stages per CTA
 };
 
 // Shared-memory plan (offsets from a 1024-aligned base).
@@ -198,6 +205,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   const int m0 = blockIdx.y * (kBH * MH);
   const int nt0 = blockIdx.x * kTilesN;  // first 16-row weight tile
   constexpr int kBpc = BS < kBK ? kBK / BS : 1;
+  // This CTA's k stages (its rank in the K-splitting cluster is blockIdx.z).
+  const int kb0 = blockIdx.z * p.kps;
+  const int nk = min(p.K64 - kb0, p.kps);
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -231,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   bool fault = false;
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < p.K64; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(empty + s, ((kb / kStages) - 1) & 1)) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kStages, kb = kb0 + i;
+        if (i >= kStages && !mbar_wait(empty + s, ((i / kStages) - 1) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           break;
         }
@@ -249,10 +259,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int kb = 0; kb < p.K64; ++kb) {
-        const int s = kb % kStages, b = kb % kBStages;
-        if (!mbar_wait(full + s, (kb / kStages) & 1) ||
-            !mbar_wait(bfull + b, (kb / kBStages) & 1)) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kStages, b = i % kBStages;
+        if (!mbar_wait(full + s, (i / kStages) & 1) ||
+            !mbar_wait(bfull + b, (i / kBStages) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           fault = true;
           break;
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
 #pragma unroll
           for (int h = 0; h < MH; ++h)
             umma_bf16(tmem + h * kBN, smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32),
-                      smem_desc_sw128(b_base + kk * 32), kb > 0 || kk > 0);
+                      smem_desc_sw128(b_base + kk * 32), i > 0 || kk > 0);
         umma_commit(empty + s);
         umma_commit(bempty + b);
       }
@@ -284,10 +294,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         sBias[e] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
       }
     }
-    for (int kb = 0; kb < p.K64; ++kb) {
-      const int s = kb % kStages, bslot = kb % kBStages;
-      if (!mbar_wait(full + s, (kb / kStages) & 1) ||
-          (kb >= kBStages && !mbar_wait(bempty + bslot, ((kb / kBStages) - 1) & 1))) {
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kStages, bslot = i % kBStages, kb = kb0 + i;
+      if (!mbar_wait(full + s, (i / kStages) & 1) ||
+          (i >= kBStages && !mbar_wait(bempty + bslot, ((i / kBStages) - 1) & 1))) {
         record_fault(&g_fault_gemm, kFaultGemmWait);
         fault = true;
         break;
@@ -354,7 +364,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
       fault = true;
     }
     named_barrier_sync(kBarEpi, 32 * kDqWarps);  // bias staged
-    if (!fault) {
+    if (!fault && MH == 1 && p.ksplit > 1) {
+      // Park the accumulator, column-major [col][row], in the drained
+      // operand rings.
+      tc_fence_after();
+      float *part = reinterpret_cast<float *>(smem);
+      const int quarter = warp & 3, half = (warp - 2) >> 2;
+      const int row = quarter * 32 + lane;
+#pragma unroll 1
+      for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
+        float v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part[(c * 32 + i) * kBH + row] = v[i];
+      }
+    } else if (!fault) {
       tc_fence_after();
       const int quarter = warp & 3;          // TMEM lanes this warp may read
       const int half = (warp - 2) >> 2;      // which half of the columns
@@ -393,6 +417,51 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
     }
   }
 
+  if (MH == 1 && p.ksplit > 1) {
+    // Split-K reduction: this CTA's slice of the tile's columns, summed over
+    // the cluster's partials in rank order.
+    cluster_sync_all();
+    if (warp >= 2) {
+      const float *part = reinterpret_cast<const float *>(smem);
+      const int cols = kBN / p.ksplit;  // 16, 32, 64 or 128
+      const int items = kBH * (cols / 16);
+      const int n_base = nt0 * kTileN;
+      for (int it = tid - 64; it < items; it += 32 * kDqWarps) {
+        const int row = it % kBH, c0 = blockIdx.z * cols + (it / kBH) * 16;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        for (int q = 0; q < p.ksplit; ++q)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[i] += ld_dsmem_f32(part + (c0 + i) * kBH + row, q);
+        const int m = m0 + row;
+        if (m < p.M) {
+          // Accumulator columns c0..c0+15 are output columns c0..c0+15,
+          // permuted within the 16.
+          float o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[out_col(i)] = acc[i] + sBias[c0 + out_col(i)];
+          uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
+          const int n0 = n_base + c0;
+          if (n0 + 16 <= p.N && p.y_vec) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = bf16_bits(o[i + 2 * e]) | (bf16_bits(o[i + 2 * e + 1]) << 16);
+              *reinterpret_cast<uint4 *>(yrow + n0 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            for (int i = 0; i < 16; ++i)
+              if (n0 + i < p.N) yrow[n0 + i] = static_cast<uint16_t>(bf16_bits(o[i]));
+          }
+        }
+      }
+    }
+    cluster_sync_all();  // peers are done reading this CTA's partials
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -419,11 +488,22 @@ cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t st
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (p.ksplit > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = p.ksplit;
+    ++na;
+  }
+  if (pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
@@ -444,6 +524,15 @@ cudaError_t launch_mh(const GemmParams &p, dim3 grid, int mh, bool sf32, bool pd
                  : launch_flags<BS, 1>(p, grid, sf32, pdl, stream);
 }
 
+// CTAs resident at once for a split-K cluster size: two per SM; clusters
+// pack per GPC, which on GB300 (152 SMs) leaves 8 CTA slots unused with
+// clusters of 4 and 16 with clusters of 8 (occupancy query for this kernel's
+// shared memory and 320 threads: 152, 74 and 36 clusters of 2, 4 and 8).
+int64_t resident_ctas(int c) {
+  const int64_t two = 2 * int64_t(sm_count());
+  return c <= 2 ? two : c == 4 ? two - two / 38 : two - two / 19;
+}
+
 }  // namespace
 
 cudaError_t gemm_take_fault(unsigned int *out) {
@@ -461,11 +550,39 @@ bool gemm_supports(const MatmulArgs &a) {
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   if (!gemm_supports(a)) return cudaErrorNotSupported;
   GemmParams p{};
-  // 256-row tiles (two MMAs per B tile) once they still give every SM two
-  // CTAs; 128-row tiles otherwise.
-  const int64_t tiles256 = ceil_div(a.M, 2 * kBH) * ceil_div(a.N, kBN);
-  const int mh = tiles256 >= 2 * int64_t(sm_count()) ? 2 : 1;
   const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
+  // Tile height (128 or 256 rows) and K split (cluster of 1..8 CTAs, 128-row
+  // tiles only) by a cost model fitted to GB300 measurements: a CTA spends
+  // about 0.77 us per 64-wide k stage with 128 rows and 1.12 us with 256
+  // rows (its dequantisation warps are latency-bound, so this hardly depends
+  // on a second CTA sharing the SM), plus a fixed cost that grows with the
+  // split (the partial tiles' reduction through distributed shared memory);
+  // CTAs run in rounds of what can be resident at once, clusters packing per
+  // GPC.
+  int mh = 1, ksplit = 1;
+  {
+    const int sms = sm_count();
+    double best = 0.0;
+    bool have = false;
+    for (int h = 1; h <= 2; ++h)
+      for (int c = 1; c <= (h == 1 ? 8 : 1); c *= 2) {
+        const int64_t kps = ceil_div(int64_t(K64), int64_t(c));
+        if (c > 1 && (kps < 4 || (c - 1) * kps >= int64_t(K64))) continue;
+        const int64_t ctas = ceil_div(a.M, int64_t(kBH) * h) * ceil_div(a.N, kBN) * c;
+        if (h == 2 && ctas < sms) continue;  // a lone 256-row CTA per SM is slower
+        const int64_t slots = resident_ctas(c);
+        if (slots <= 0) continue;
+        const double fixed = c == 1 ? 2.0 : c == 2 ? 4.0 : c == 4 ? 6.0 : 13.0;
+        const double cost = double(ceil_div(ctas, slots)) *
+                            (double(kps) * (h == 2 ? 1.12 : 0.77) + fixed);
+        if (!have || cost < best - 1e-9) {
+          best = cost;
+          mh = h;
+          ksplit = c;
+          have = true;
+        }
+      }
+  }
   const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
   const uint64_t es = a.scale_f32 ? 4 : 2;
   const uint32_t bpc = a.bs < kBK ? kBK / a.bs : 1;
@@ -514,8 +631,11 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   p.K64 = static_cast<int>(K64);
   p.has_zp = a.zp != nullptr;
   p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
+  p.ksplit = ksplit;
+  p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
   const dim3 grid(static_cast<unsigned>(ceil_div(a.N, kBN)),
-                  static_cast<unsigned>(ceil_div(a.M, int64_t(kBH) * mh)), 1);
+                  static_cast<unsigned>(ceil_div(a.M, int64_t(kBH) * mh)),
+                  static_cast<unsigned>(ksplit));
   switch (a.bs) {
     case 16: return launch_mh<16>(p, grid, mh, a.scale_f32, a.pdl, stream);
     case 32: return launch_mh<32>(p, grid, mh, a.scale_f32, a.pdl, stream);
