@@ -56,6 +56,9 @@ def load(path: str | None = None):
         lib.oracle_matmulnbits.restype = i32
         lib.oracle_dequantize.argtypes = [p, p, i32, p, i64, i64, i32, p]
         lib.oracle_dequantize.restype = i32
+        lib.oracle_qdq_matmul.argtypes = [p, i32, p, p, i32, p, p, i32, i64, i64,
+                                          i64, i32, p, i64, p, i64, p, p]
+        lib.oracle_qdq_matmul.restype = i32
         if path is None:
             _lib = lib
         return lib
@@ -143,3 +146,44 @@ def dequantize(B, scales, zero_points=None, *, N: int, K: int,
     if rc != 0:
         raise ValueError(f"oracle_dequantize rejected its arguments ({rc})")
     return W
+
+
+def qdq_matmul(A, Bq, scales, zero_points=None, bias=None, *, N: int, K: int,
+               block_size: int, axis: int = 0, rows=None, cols=None, lib=None):
+    """Y[m,n] = sum_k A[m,k] w[n,k] + bias[n] for the QDQ INT4 encoding: a
+    logical UINT4 matrix ([K, N] for axis 0, [N, K] for axis 1) stored
+    flattened, low nibble first, DequantizeLinear along that axis with
+    block_size (scales / zero points of the block-reduced shape; absent zero
+    points are 0). Returns (Y, absdot) like matmulnbits."""
+    lib = lib or load()
+    a, a_t = _as_array(A, "A")
+    b, _ = _as_array(Bq, "Bq")
+    s, s_t = _as_array(scales, "scales")
+    z = None if zero_points is None else _as_array(zero_points, "zero_points")[0]
+    bi = None
+    if bias is not None:
+        bi, bt = _as_array(bias, "bias")
+        if bt != F32:
+            raise TypeError("bias must be fp32")
+    if a.ndim != 2 or a.shape[1] != K:
+        raise ValueError("A must be a 2-D [M, K] array")
+    M = a.shape[0]
+    nb = (K + block_size - 1) // block_size
+    if b.size != (K * N + 1) // 2:
+        raise ValueError("Bq has the wrong number of bytes")
+    if s.size != N * nb:
+        raise ValueError("scales has the wrong number of elements")
+    if z is not None and z.size != (N * nb + 1) // 2:
+        raise ValueError("zero_points has the wrong number of bytes")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else r.size
+    nc = N if c is None else c.size
+    Y = np.zeros((nr, nc), dtype=np.float64)
+    mag = np.zeros((nr, nc), dtype=np.float64)
+    rc = lib.oracle_qdq_matmul(_ptr(a), a_t, _ptr(b), _ptr(s), s_t, _ptr(z), _ptr(bi), axis,
+                               M, N, K, block_size, _ptr(r), 0 if r is None else r.size,
+                               _ptr(c), 0 if c is None else c.size, _ptr(Y), _ptr(mag))
+    if rc != 0:
+        raise ValueError(f"oracle_qdq_matmul rejected its arguments ({rc})")
+    return Y, mag

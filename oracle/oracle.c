@@ -145,3 +145,69 @@ int oracle_matmulnbits(const void *A, int a_dtype, const uint8_t *B,
   }
   return 0;
 }
+
+/*
+ * The standard QDQ INT4 encoding (page "Qwen3 CPU Inference Critical Path",
+ * section "qwen3-int4-qdq"): a logical UINT4 matrix stored ONNX row-major,
+ * low nibble first (element i of the flattened matrix is nibble i of the
+ * byte stream), DequantizeLinear with a block size along one axis, then
+ * MatMul:
+ *
+ *   axis 0 (projections): the matrix is [K, N];  w[n,k] = (q[k,n] - z[k/bs,n]) * s[k/bs,n]
+ *   axis 1 (tied LM head): the matrix is [N, K]; w[n,k] = (q[n,k] - z[n,k/bs]) * s[n,k/bs]
+ *
+ *   Y[m,n] = sum_k A[m,k] * w[n,k] + bias[n]
+ *
+ * Scales and zero points have the block-reduced shape ([ceil(K/bs), N] or
+ * [N, ceil(K/bs)]); zero points are UINT4 stored like the codes, and absent
+ * zero points are 0 (the DequantizeLinear default). Everything in double, in
+ * increasing k.
+ */
+static int qdq_nibble(const uint8_t *p, int64_t i) {
+  uint8_t byte = p[i / 2];
+  return (i % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+}
+
+static double qdq_weight_at(const uint8_t *Bq, const void *scales, int scale_dtype,
+                            const uint8_t *zp, int axis, int64_t n, int64_t k,
+                            int64_t N, int64_t K, int64_t nb, int bs) {
+  int64_t b = k / bs;
+  int64_t ci = axis == 0 ? k * N + n : n * K + k;   /* code element */
+  int64_t si = axis == 0 ? b * N + n : n * nb + b;  /* scale / zero-point element */
+  int q = qdq_nibble(Bq, ci);
+  int z = zp ? qdq_nibble(zp, si) : 0;
+  return (double)(q - z) * widen(scales, si, scale_dtype);
+}
+
+int oracle_qdq_matmul(const void *A, int a_dtype, const uint8_t *Bq,
+                      const void *scales, int scale_dtype, const uint8_t *zp,
+                      const float *bias, int axis, int64_t M, int64_t N,
+                      int64_t K, int bs, const int64_t *rows, int64_t n_rows,
+                      const int64_t *cols, int64_t n_cols, double *Y,
+                      double *absdot) {
+  int rc = check_args(M, N, K, bs, a_dtype, scale_dtype);
+  if (rc) return rc;
+  if (axis != 0 && axis != 1) return -2;
+  if (rows == NULL) n_rows = M;
+  if (cols == NULL) n_cols = N;
+  int64_t nb = n_blocks(K, bs);
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t m = rows ? rows[i] : i;
+    if (m < 0 || m >= M) return -2;
+    for (int64_t j = 0; j < n_cols; ++j) {
+      int64_t n = cols ? cols[j] : j;
+      if (n < 0 || n >= N) return -2;
+      double acc = 0.0, mag = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        double a = widen(A, m * K + k, a_dtype);
+        double w = qdq_weight_at(Bq, scales, scale_dtype, zp, axis, n, k, N, K, nb, bs);
+        acc += a * w;
+        mag += fabs(a * w);
+      }
+      if (bias) acc += (double)bias[n];
+      Y[i * n_cols + j] = acc;
+      if (absdot) absdot[i * n_cols + j] = mag;
+    }
+  }
+  return 0;
+}
