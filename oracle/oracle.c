@@ -204,7 +204,7 @@ int oracle_qdq_matmul(const void *A, int a_dtype, const uint8_t *Bq,
         acc += a * w;
         mag += fabs(a * w);
       }
-      if (bias) acc += (double)bias[n];
+      if (bias != NULL) acc += (double)bias[n];
       Y[i * n_cols + j] = acc;
       if (absdot) absdot[i * n_cols + j] = mag;
     }

@@ -34,3 +34,13 @@ def dense_weights(Q, Z, S, block_size):
     N, K = Q.shape
     blk = np.arange(K) // block_size
     return (Q.astype(np.float64) - Z[:, blk].astype(np.float64)) * S[:, blk].astype(np.float64)
+
+
+def pack_flat(Q: np.ndarray) -> np.ndarray:
+    """Logical UINT4 array (any shape) -> uint8 bytes in ONNX row-major,
+    low-nibble-first storage: element i of the flattened array is nibble i;
+    an odd count leaves the last high nibble 0."""
+    flat = np.asarray(Q, dtype=np.uint8).reshape(-1)
+    if flat.size % 2:
+        flat = np.concatenate([flat, np.zeros(1, dtype=np.uint8)])
+    return (flat[0::2] | (flat[1::2] << 4)).astype(np.uint8)

@@ -5,9 +5,9 @@ axis 0 for the projections ([K, N] matrix, scales [ceil(K/bs), N]) or axis 1
 for the tied LM head ([N, K], scales [N, ceil(K/bs)]); zero points default to
 0 when absent).
 
-The packer below is written for the tests from that storage description
-alone (element i of the flattened matrix is nibble i, low nibble first) and
-shares no code with the oracle.
+The test-side packer (tests/packing.py, pack_flat) is written from that
+storage description alone (element i of the flattened matrix is nibble i,
+low nibble first) and shares no code with the oracle.
 """
 import os
 import shutil
@@ -18,17 +18,7 @@ import pytest
 import torch
 
 import oracle
-from tests.packing import pack_codes, pack_zero_points
-
-
-def pack_flat(Q: np.ndarray) -> np.ndarray:
-    """Logical UINT4 array (any shape) -> uint8 bytes, flattened row-major,
-    element i in nibble i (low nibble first); an odd count leaves the last
-    high nibble 0."""
-    flat = np.asarray(Q, dtype=np.uint8).reshape(-1)
-    if flat.size % 2:
-        flat = np.concatenate([flat, np.zeros(1, dtype=np.uint8)])
-    return (flat[0::2] | (flat[1::2] << 4)).astype(np.uint8)
+from tests.packing import pack_codes, pack_flat, pack_zero_points
 
 
 SHAPES = [(1, 1, 1, 16), (3, 7, 31, 16), (2, 5, 33, 32), (4, 3, 100, 32),
@@ -112,6 +102,7 @@ MUTATIONS = {
                                  "return (i % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
     "QDQ zero-point default 8": ("int z = zp ? qdq_nibble(zp, si) : 0;",
                                  "int z = zp ? qdq_nibble(zp, si) : 8;"),
+    "QDQ bias dropped": ("if (bias != NULL) acc += (double)bias[n];", ""),
     "QDQ zero point subtracted twice": ("return (double)(q - z) * widen(scales, si, scale_dtype);",
                                         "return (double)(q - 2 * z) * widen(scales, si, scale_dtype);"),
 }
@@ -124,10 +115,12 @@ def _pins_pass(lib):
         for axis in (0, 1):
             for with_zp in (False, True):
                 Q, Z, A_int, nb = _case(rng, M, N, K, bs, with_zp)
-                exact = A_int @ (Q - Z[:, np.arange(K) // bs]).T
+                bias = rng.integers(-5, 6, size=N)
+                exact = A_int @ (Q - Z[:, np.arange(K) // bs]).T + bias
                 Bq, S, zp = _qdq_inputs(Q, Z, np.ones((N, nb), dtype=np.float32), axis, with_zp)
                 Y, _ = oracle.qdq_matmul(torch.tensor(A_int, dtype=torch.float32), Bq, S, zp,
-                                         None, N=N, K=K, block_size=bs, axis=axis, lib=lib)
+                                         bias.astype(np.float32), N=N, K=K, block_size=bs,
+                                         axis=axis, lib=lib)
                 if not np.array_equal(Y, exact.astype(np.float64)):
                     return False
     return True
