@@ -123,6 +123,37 @@ MNB_API mnb_status mnb_prepack(const uint8_t *B, const void *scales,
                                mnb_stream_t stream);
 
 /*
+ * Offline re-layout of one weight in the standard QDQ INT4 encoding into the
+ * same prepacked form (page "Qwen3 CPU Inference Critical Path", section
+ * "qwen3-int4-qdq": a logical UINT4 initializer in ONNX row-major,
+ * low-nibble-first storage, DequantizeLinear with block_size along one axis,
+ * then MatMul). The packed weight then runs through mnb_matmul like any
+ * other, computing Y[m,n] = sum_k A[m,k] (q - z) s + bias[n] with
+ *   axis 0 (projections):   q = Bq[k, n] of a logical [K, N] matrix,
+ *                           s = scales[k / bs, n], z = zero_points[k / bs, n];
+ *   axis 1 (tied LM head):  q = Bq[n, k] of a logical [N, K] matrix,
+ *                           s = scales[n, k / bs], z = zero_points[n, k / bs].
+ *  B_qdq        uint8, ceil(K*N / 2) bytes: element i of the flattened
+ *               logical matrix is nibble i, low nibble first.
+ *  scales       [ceil(K/bs), N] (axis 0) or [N, ceil(K/bs)] (axis 1), in
+ *               scale_dtype (fp32, or bf16 as raw 16-bit words).
+ *  zero_points  UINT4 of the scales' shape, flattened low-nibble-first
+ *               (ceil(nb*N / 2) bytes), or NULL: every zero point is 0, the
+ *               DequantizeLinear default. packed_zp is always written.
+ *  packed_b, packed_scales, packed_zp: outputs of the sizes given by
+ *               mnb_prepacked_sizes(..., has_zero_points = 1), 16-byte
+ *               aligned.
+ * Use the packed weight with zero points (pass packed_zp to mnb_matmul).
+ * Errors: as mnb_prepack, and MNB_ERR_SHAPE for an axis other than 0 or 1.
+ */
+MNB_API mnb_status mnb_prepack_qdq(const uint8_t *B_qdq, const void *scales,
+                                   const uint8_t *zero_points, int axis,
+                                   int64_t N, int64_t K, int block_size,
+                                   mnb_dtype scale_dtype, void *packed_b,
+                                   void *packed_scales, void *packed_zp,
+                                   mnb_stream_t stream);
+
+/*
  * Inverse of mnb_prepack: writes B [N, nb, bs/2] (padding nibbles past K set
  * to 0), scales [N, nb] and, when packed_zp is not NULL, zero_points
  * [N, ceil(nb/2)] (an unused high nibble of an odd nb set to 0). Used to

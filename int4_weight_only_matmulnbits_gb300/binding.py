@@ -24,7 +24,8 @@ MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2}
 EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_prepacked_sizes", "mnb_prepack", "mnb_unprepack", "mnb_matmul",
            "mnb_matmul_path", "mnb_matmul_from_host",
-           "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped")
+           "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
+           "mnb_prepack_qdq")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,8 @@ def load(build_if_missing: bool = False):
         lib.mnb_prepacked_sizes.restype = i32
         lib.mnb_prepack.argtypes = [p, p, p, i64, i64, i32, i32, p, p, p, p]
         lib.mnb_prepack.restype = i32
+        lib.mnb_prepack_qdq.argtypes = [p, p, p, i32, i64, i64, i32, i32, p, p, p, p]
+        lib.mnb_prepack_qdq.restype = i32
         lib.mnb_unprepack.argtypes = [p, p, p, i64, i64, i32, i32, p, p, p, p]
         lib.mnb_unprepack.restype = i32
         lib.mnb_matmul.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32, i32, p]
@@ -176,6 +179,28 @@ def mnb_prepack(B: torch.Tensor, scales: torch.Tensor, zero_points: torch.Tensor
     _check(load().mnb_prepack(_ptr(B), _ptr(scales), _ptr(zero_points), N, K, block_size,
                               _dtype_code(scales.dtype), _ptr(packed_b), _ptr(packed_s),
                               _ptr(packed_z), _stream(stream)), "mnb_prepack")
+    return PackedWeight(packed_b, packed_s, packed_z, N, K, block_size, scales.dtype)
+
+
+def mnb_prepack_qdq(B_qdq: torch.Tensor, scales: torch.Tensor,
+                    zero_points: torch.Tensor | None, N: int, K: int, block_size: int, *,
+                    axis: int = 0, stream=None) -> PackedWeight:
+    """Prepack one weight given in the QDQ INT4 encoding (device tensors): a
+    logical UINT4 [K, N] (axis 0) or [N, K] (axis 1) matrix stored flattened
+    low-nibble-first, scales / zero points of the block-reduced shape, absent
+    zero points meaning 0. The result always carries packed zero points."""
+    for name, t in (("B_qdq", B_qdq), ("scales", scales), ("zero_points", zero_points)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    sb, ss, sz = mnb_prepacked_sizes(N, K, block_size, scales.dtype, True)
+    dev = B_qdq.device
+    packed_b = torch.empty(sb, dtype=torch.uint8, device=dev)
+    packed_s = torch.empty(ss, dtype=torch.uint8, device=dev)
+    packed_z = torch.empty(sz, dtype=torch.uint8, device=dev)
+    _check(load().mnb_prepack_qdq(_ptr(B_qdq), _ptr(scales), _ptr(zero_points), axis, N, K,
+                                  block_size, _dtype_code(scales.dtype), _ptr(packed_b),
+                                  _ptr(packed_s), _ptr(packed_z), _stream(stream)),
+           "mnb_prepack_qdq")
     return PackedWeight(packed_b, packed_s, packed_z, N, K, block_size, scales.dtype)
 
 

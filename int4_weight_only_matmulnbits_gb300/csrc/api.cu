@@ -262,6 +262,36 @@ mnb_status mnb_prepack(const uint8_t *B, const void *scales,
   return MNB_OK;
 }
 
+mnb_status mnb_prepack_qdq(const uint8_t *B_qdq, const void *scales,
+                           const uint8_t *zero_points, int axis, int64_t N, int64_t K,
+                           int block_size, mnb_dtype scale_dtype, void *packed_b,
+                           void *packed_scales, void *packed_zp, mnb_stream_t stream) {
+  if (!B_qdq || !scales || !packed_b || !packed_scales || !packed_zp) return MNB_ERR_NULL;
+  if (axis != 0 && axis != 1) return MNB_ERR_SHAPE;
+  mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  if (!aligned(packed_b, 16) || !aligned(packed_scales, 16) || !aligned(packed_zp, 16) ||
+      !aligned(scales, dtype_size(scale_dtype)))
+    return MNB_ERR_ALIGN;
+  const int64_t nb = ceil_div(K, block_size);
+  const Sizes out = packed_sizes(N, K, block_size, scale_dtype, true);
+  const void *const ins[3] = {B_qdq, scales, zero_points};
+  const size_t in_n[3] = {size_t((K * N + 1) / 2), size_t(N) * nb * dtype_size(scale_dtype),
+                          zero_points ? size_t((nb * N + 1) / 2) : 0};
+  void *const outs[3] = {packed_b, packed_scales, packed_zp};
+  const size_t out_n[3] = {out.b, out.s, out.z};
+  st = check_outputs_disjoint(outs, out_n, ins, in_n);
+  if (st != MNB_OK) return st;
+  st = check_device();
+  if (st != MNB_OK) return st;
+  PrepackArgs a{B_qdq, scales, zero_points, N, K, block_size,
+                scale_dtype == MNB_F32, packed_b, packed_scales, packed_zp};
+  a.qdq_axis = axis;
+  const cudaError_t e = launch_prepack(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_prepack_qdq");
+  return MNB_OK;
+}
+
 mnb_status mnb_unprepack(const void *packed_b, const void *packed_scales,
                          const void *packed_zp, int64_t N, int64_t K,
                          int block_size, mnb_dtype scale_dtype, uint8_t *B,

@@ -17,6 +17,7 @@ struct PrepackArgs {
   int bs;
   bool scale_f32;
   void *packed_b, *packed_scales, *packed_zp;
+  int qdq_axis = -1;  // -1: MatMulNBits storage; 0 / 1: QDQ UINT4 [K,N] / [N,K]
 };
 
 struct UnprepackArgs {

@@ -1,5 +1,7 @@
 // Offline re-layout of MatMulNBits weights into the prepacked form, and its
-// inverse. The layout is defined in mnb_common.cuh.
+// inverse; also the re-layout of the standard QDQ INT4 encoding (logical
+// UINT4 matrix + DequantizeLinear) into the same form. The layout is defined
+// in mnb_common.cuh.
 #include "mnb_common.cuh"
 #include "mnb_launch.h"
 
@@ -17,9 +19,35 @@ __device__ __forceinline__ uint32_t source_code(const uint8_t *B, int64_t n,
   return (within & 1) ? (byte >> 4) : (byte & 0x0F);
 }
 
-__global__ void pack_codes_kernel(const uint8_t *__restrict__ B,
-                                  uint32_t *__restrict__ out, int64_t N,
-                                  int64_t K, int64_t nb, int bs, int64_t K64,
+// Code source for the MatMulNBits storage.
+struct NBitsCodes {
+  const uint8_t *B;
+  int64_t N, K, nb;
+  int bs;
+  __device__ __forceinline__ uint32_t operator()(int64_t n, int64_t k) const {
+    return source_code(B, n, k, N, K, nb, bs);
+  }
+};
+
+// Code source for a logical UINT4 matrix in ONNX row-major, low-nibble-first
+// storage (page "Qwen3 CPU Inference Critical Path", section
+// "qwen3-int4-qdq"): element i of the flattened matrix is nibble i of the
+// byte stream, low nibble first. axis 0: the matrix is [K, N] (projections,
+// DequantizeLinear along K); axis 1: [N, K] (the tied LM-head weight).
+struct QdqCodes {
+  const uint8_t *B;
+  int64_t N, K;
+  int axis;
+  __device__ __forceinline__ uint32_t operator()(int64_t n, int64_t k) const {
+    if (n >= N || k >= K) return 0;
+    const int64_t i = axis == 0 ? k * N + n : n * K + k;
+    const uint8_t byte = B[i >> 1];
+    return (i & 1) ? (byte >> 4) : (byte & 0x0F);
+  }
+};
+
+template <typename Src>
+__global__ void pack_codes_kernel(Src src, uint32_t *__restrict__ out, int64_t K64,
                                   int64_t words) {
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < words;
        w += (int64_t)gridDim.x * blockDim.x) {
@@ -34,29 +62,51 @@ __global__ void pack_codes_kernel(const uint8_t *__restrict__ B,
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        word |= source_code(B, r0 + 8 * h, k0 + e, N, K, nb, bs)
-                << code_shift(e, h);
+        word |= src(r0 + 8 * h, k0 + e) << code_shift(e, h);
     out[w] = word;
   }
 }
 
+// Scales s[n, b] stored [N, nb] (k_major false) or [nb, N] (true).
 template <typename T>
 __global__ void pack_scales_kernel(const T *__restrict__ s, T *__restrict__ out,
-                                   int64_t N, int64_t nb, int64_t total) {
+                                   int64_t N, int64_t nb, bool k_major, int64_t total) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int r = static_cast<int>(i & 15);
     const int64_t tb = i >> 4;
     const int64_t tile = tb / nb, b = tb % nb;
     const int64_t n = tile * kTileN + r;
-    out[i] = n < N ? s[n * nb + b] : T(0);
+    out[i] = n < N ? s[k_major ? b * N + n : n * nb + b] : T(0);
   }
 }
 
-__global__ void pack_zp_kernel(const uint8_t *__restrict__ zp,
-                               uint64_t *__restrict__ out, int64_t N,
+// Zero-point sources: MatMulNBits [N, ceil(nb/2)] bytes, even block low;
+// QDQ UINT4 [nb, N] (axis 0) or [N, nb] (axis 1) flattened low-nibble-first;
+// QDQ without zero points: 0 (the DequantizeLinear default).
+struct NBitsZp {
+  const uint8_t *zp;
+  int64_t nb;
+  __device__ __forceinline__ uint32_t operator()(int64_t n, int64_t b) const {
+    const uint8_t byte = zp[n * ((nb + 1) / 2) + b / 2];
+    return (b & 1) ? (byte >> 4) : (byte & 0x0F);
+  }
+};
+struct QdqZp {
+  const uint8_t *zp;
+  int64_t N, nb;
+  int axis;
+  __device__ __forceinline__ uint32_t operator()(int64_t n, int64_t b) const {
+    if (zp == nullptr) return 0;
+    const int64_t i = axis == 0 ? b * N + n : n * nb + b;
+    const uint8_t byte = zp[i >> 1];
+    return (i & 1) ? (byte >> 4) : (byte & 0x0F);
+  }
+};
+
+template <typename Src>
+__global__ void pack_zp_kernel(Src src, uint64_t *__restrict__ out, int64_t N,
                                int64_t nb, int64_t nbz, int64_t total) {
-  const int64_t zbytes = (nb + 1) / 2;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t tile = i / nbz, b = i % nbz;
@@ -64,9 +114,7 @@ __global__ void pack_zp_kernel(const uint8_t *__restrict__ zp,
     for (int r = 0; r < kTileN && b < nb; ++r) {
       const int64_t n = tile * kTileN + r;
       if (n >= N) break;
-      const uint8_t byte = zp[n * zbytes + b / 2];
-      const uint64_t z = (b & 1) ? (byte >> 4) : (byte & 0x0F);
-      word |= z << (4 * r);
+      word |= static_cast<uint64_t>(src(n, b)) << (4 * r);
     }
     out[i] = word;
   }
@@ -152,22 +200,31 @@ cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream) {
   const int64_t nb = ceil_div(a.K, a.bs);
   const int64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
   const int64_t words = N16 * K64 * (kChunkBytes / 4);
-  pack_codes_kernel<<<grid_for(words), 256, 0, stream>>>(
-      a.B, static_cast<uint32_t *>(a.packed_b), a.N, a.K, nb, a.bs, K64, words);
+  const bool qdq = a.qdq_axis >= 0;
+  if (qdq)
+    pack_codes_kernel<<<grid_for(words), 256, 0, stream>>>(
+        QdqCodes{a.B, a.N, a.K, a.qdq_axis}, static_cast<uint32_t *>(a.packed_b), K64, words);
+  else
+    pack_codes_kernel<<<grid_for(words), 256, 0, stream>>>(
+        NBitsCodes{a.B, a.N, a.K, nb, a.bs}, static_cast<uint32_t *>(a.packed_b), K64, words);
   const int64_t ns = N16 * nb * kTileN;
+  const bool k_major = a.qdq_axis == 0;
   if (a.scale_f32)
     pack_scales_kernel<float><<<grid_for(ns), 256, 0, stream>>>(
         static_cast<const float *>(a.scales),
-        static_cast<float *>(a.packed_scales), a.N, nb, ns);
+        static_cast<float *>(a.packed_scales), a.N, nb, k_major, ns);
   else
     pack_scales_kernel<uint16_t><<<grid_for(ns), 256, 0, stream>>>(
         static_cast<const uint16_t *>(a.scales),
-        static_cast<uint16_t *>(a.packed_scales), a.N, nb, ns);
-  if (a.zp != nullptr) {
-    const int64_t nbz = ceil_div(nb, 2) * 2;
+        static_cast<uint16_t *>(a.packed_scales), a.N, nb, k_major, ns);
+  const int64_t nbz = ceil_div(nb, 2) * 2;
+  if (qdq)  // always packed: QDQ zero points default to 0, not 8
     pack_zp_kernel<<<grid_for(N16 * nbz), 256, 0, stream>>>(
-        a.zp, static_cast<uint64_t *>(a.packed_zp), a.N, nb, nbz, N16 * nbz);
-  }
+        QdqZp{a.zp, a.N, nb, a.qdq_axis}, static_cast<uint64_t *>(a.packed_zp), a.N, nb, nbz,
+        N16 * nbz);
+  else if (a.zp != nullptr)
+    pack_zp_kernel<<<grid_for(N16 * nbz), 256, 0, stream>>>(
+        NBitsZp{a.zp, nb}, static_cast<uint64_t *>(a.packed_zp), a.N, nb, nbz, N16 * nbz);
   prepack_fence_kernel<<<1, 32, 0, stream>>>();
   return cudaGetLastError();
 }

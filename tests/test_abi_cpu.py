@@ -116,3 +116,26 @@ def test_prepack_rejects_invalid_arguments_on_host(lib):
     assert call(pb=v(4096 + 16)) == -6  # packed output overlaps B
     assert call(ps=v((1 << 20) + 256)) == -6  # the two outputs overlap
     assert lib.mnb_prepacked_sizes(16, 64, 32, 0, 0, None, None, None) == -1
+
+
+def test_prepack_qdq_rejects_invalid_arguments_on_host(lib):
+    """QDQ re-layout: the same argument checks, plus the axis (0 or 1) and a
+    packed zero-point output that is always required."""
+    v = ctypes.c_void_p
+    ok = dict(B=v(4096), S=v(1 << 16), Z=None, axis=0, N=16, K=64, bs=32, st=1,
+              pb=v(1 << 20), ps=v(1 << 21), pz=v(1 << 22))
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.mnb_prepack_qdq(a["B"], a["S"], a["Z"], a["axis"], a["N"], a["K"], a["bs"],
+                                   a["st"], a["pb"], a["ps"], a["pz"], None)
+    assert call(B=None) == -1
+    assert call(pz=None) == -1
+    assert call(axis=2) == -2
+    assert call(axis=-1) == -2
+    assert call(K=0) == -2
+    assert call(bs=48) == -3
+    assert call(st=7) == -4
+    assert call(pz=v((1 << 22) + 4)) == -5
+    assert call(pb=v(4096)) == -6  # packed output overlaps B
