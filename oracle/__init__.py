@@ -187,3 +187,19 @@ def qdq_matmul(A, Bq, scales, zero_points=None, bias=None, *, N: int, K: int,
     if rc != 0:
         raise ValueError(f"oracle_qdq_matmul rejected its arguments ({rc})")
     return Y, mag
+
+
+def gate_up(A, gate, up, *, N: int, K: int, block_size: int, rows=None, cols=None, lib=None):
+    """Gated-MLP pair (page "Qwen3 CPU Inference Critical Path": the fusion
+    "gate projection, SiLU, and gate/up multiplication"; SiLU is x * Sigmoid(x)
+    in the audited graph): with g = the MatMulNBits result of A and gate and
+    u = that of A and up (each a tuple (B, scales, zero_points, bias)),
+    Y = g * sigmoid(g) * u, all in double.
+
+    Returns (Y, g, u, absdot_g, absdot_u)."""
+    g, mg = matmulnbits(A, *gate, N=N, K=K, block_size=block_size, rows=rows, cols=cols,
+                        lib=lib)
+    u, mu = matmulnbits(A, *up, N=N, K=K, block_size=block_size, rows=rows, cols=cols,
+                        lib=lib)
+    sig = 1.0 / (1.0 + np.exp(-g))
+    return g * sig * u, g, u, mg, mu
