@@ -249,6 +249,28 @@ MNB_API mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,
                                         mnb_stream_t stream);
 
 /*
+ * Gated-MLP projection pair in one call (page "Qwen3 CPU Inference Critical
+ * Path": the graph-level fusion "gate projection, SiLU, and gate/up
+ * multiplication", with SiLU computed as x * Sigmoid(x) in FP32 as in the
+ * audited graph):
+ *   g = A * dequant(gate)^T + bias_gate,  u = A * dequant(up)^T + bias_up,
+ *   Y[m,n] = g * sigmoid(g) * u  (fp32, then A's dtype; bf16 to nearest even).
+ * gate and up are two prepacked weights of the same N, K, block_size, scale
+ * dtype and zero-point presence; each CTA streams matching rows of both, so
+ * neither projection is written to memory. All pointers DEVICE; Y [M, N].
+ * Arguments and errors as mnb_matmul (both zero-point pointers set, or both
+ * NULL: MNB_ERR_NULL otherwise); Y must not overlap any input.
+ */
+MNB_API mnb_status mnb_matmul_gate_up(const void *A, const void *packed_gate,
+                                      const void *scales_gate, const void *zp_gate,
+                                      const float *bias_gate, const void *packed_up,
+                                      const void *scales_up, const void *zp_up,
+                                      const float *bias_up, int64_t M, int64_t N,
+                                      int64_t K, int block_size, void *Y,
+                                      mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                      mnb_stream_t stream);
+
+/*
  * Programmatic dependent launch (on by default): each matmul kernel lets the
  * next kernel on the stream launch early and starts streaming its own
  * (constant) prepacked weights before the previous kernel has finished; it

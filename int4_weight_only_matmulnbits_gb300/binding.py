@@ -25,7 +25,7 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_prepacked_sizes", "mnb_prepack", "mnb_unprepack", "mnb_matmul",
            "mnb_matmul_path", "mnb_matmul_from_host",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
-           "mnb_prepack_qdq")
+           "mnb_prepack_qdq", "mnb_matmul_gate_up")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,9 @@ def load(build_if_missing: bool = False):
         lib.mnb_prepacked_sizes.restype = i32
         lib.mnb_prepack.argtypes = [p, p, p, i64, i64, i32, i32, p, p, p, p]
         lib.mnb_prepack.restype = i32
+        lib.mnb_matmul_gate_up.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i64, i32, p,
+                                           i32, i32, p]
+        lib.mnb_matmul_gate_up.restype = i32
         lib.mnb_prepack_qdq.argtypes = [p, p, p, i32, i64, i64, i32, i32, p, p, p, p]
         lib.mnb_prepack_qdq.restype = i32
         lib.mnb_unprepack.argtypes = [p, p, p, i64, i64, i32, i32, p, p, p, p]
@@ -278,3 +281,28 @@ def mnb_matmul_grouped(A: torch.Tensor, ws: list[PackedWeight],
         _dtype_code(A.dtype), _dtype_code(ws[0].scale_dtype), _stream(stream)),
         "mnb_matmul_grouped")
     return outs
+
+
+def mnb_matmul_gate_up(A: torch.Tensor, gate: PackedWeight, up: PackedWeight,
+                       bias_gate: torch.Tensor | None = None,
+                       bias_up: torch.Tensor | None = None, *,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = silu(A @ gate^T + bias_gate) * (A @ up^T + bias_up), silu(x) =
+    x * sigmoid(x), in one launch per 16 rows."""
+    if (gate.N, gate.K, gate.block_size, gate.scale_dtype) != (up.N, up.K, up.block_size,
+                                                              up.scale_dtype):
+        raise ValueError("gate and up must have the same N, K, block size and scale dtype")
+    if A.dim() != 2 or A.shape[1] != gate.K or not A.is_cuda or not A.is_contiguous():
+        raise ValueError(f"A must be a contiguous CUDA [M, {gate.K}] tensor")
+    for b in (bias_gate, bias_up):
+        if b is not None and (b.dtype != torch.float32 or not b.is_cuda):
+            raise ValueError("biases must be fp32 CUDA tensors")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty(M, gate.N, dtype=A.dtype, device=A.device)
+    _check(load().mnb_matmul_gate_up(
+        _ptr(A), _ptr(gate.packed_b), _ptr(gate.packed_scales), _ptr(gate.packed_zp),
+        _ptr(bias_gate), _ptr(up.packed_b), _ptr(up.packed_scales), _ptr(up.packed_zp),
+        _ptr(bias_up), M, gate.N, gate.K, gate.block_size, _ptr(out), _dtype_code(A.dtype),
+        _dtype_code(gate.scale_dtype), _stream(stream)), "mnb_matmul_gate_up")
+    return out

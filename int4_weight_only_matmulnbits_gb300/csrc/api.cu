@@ -3,6 +3,7 @@
 // on the host before anything is enqueued; nothing here falls back to a CPU
 // computation.
 #include <atomic>
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -417,6 +418,56 @@ mnb_status mnb_matmul_grouped(const void *A, int count,
     return MNB_ERR_UNSUPPORTED;
   }
   if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_grouped");
+  return MNB_OK;
+}
+
+mnb_status mnb_matmul_gate_up(const void *A, const void *packed_gate,
+                              const void *scales_gate, const void *zp_gate,
+                              const float *bias_gate, const void *packed_up,
+                              const void *scales_up, const void *zp_up,
+                              const float *bias_up, int64_t M, int64_t N, int64_t K,
+                              int block_size, void *Y, mnb_dtype a_dtype,
+                              mnb_dtype scale_dtype, mnb_stream_t stream) {
+  if ((zp_gate != nullptr) != (zp_up != nullptr)) return MNB_ERR_NULL;
+  mnb_status st = validate_matmul(A, packed_gate, scales_gate, zp_gate, bias_gate, M, N, K,
+                                  block_size, Y, a_dtype, scale_dtype, MNB_PATH_AUTO);
+  if (st != MNB_OK) return st;
+  st = validate_matmul(A, packed_up, scales_up, zp_up, bias_up, M, N, K, block_size, Y,
+                       a_dtype, scale_dtype, MNB_PATH_AUTO);
+  if (st != MNB_OK) return st;
+  const size_t es = dtype_size(a_dtype);
+  GroupArgs g{};
+  g.count = 2;
+  g.paired = true;
+  g.packed_b[0] = packed_gate;
+  g.packed_b[1] = packed_up;
+  g.scales[0] = scales_gate;
+  g.scales[1] = scales_up;
+  g.zp[0] = zp_gate;
+  g.zp[1] = zp_up;
+  g.bias[0] = bias_gate;
+  g.bias[1] = bias_up;
+  g.N[0] = g.N[1] = N;
+  g.K = K;
+  g.bs = block_size;
+  g.a_f32 = a_dtype == MNB_F32;
+  g.scale_f32 = scale_dtype == MNB_F32;
+  g.has_zp = zp_gate != nullptr;
+  g.pdl = g_pdl.load() != 0;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The decode kernel takes up to 16 rows per launch.
+  for (int64_t m0 = 0; m0 < M; m0 += kGemvMaxM) {
+    g.M = std::min<int64_t>(kGemvMaxM, M - m0);
+    g.A = static_cast<const char *>(A) + m0 * K * es;
+    g.Y[0] = static_cast<char *>(Y) + m0 * N * es;
+    const cudaError_t e = launch_gemv_group(g, s);
+    if (e == cudaErrorNotSupported) {
+      std::snprintf(g_last_error, sizeof g_last_error,
+                    "no gate/up kernel for K=%lld bs=%d", (long long)K, block_size);
+      return MNB_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_gate_up");
+  }
   return MNB_OK;
 }
 

@@ -38,6 +38,11 @@
 //    through shared memory, CTAs of a cluster through distributed shared
 //    memory; a warp that owns all of K stores its tile directly. No global
 //    workspace, no atomics on results: outputs are bitwise reproducible.
+//  * Gated-MLP pairs (page "Qwen3 CPU Inference Critical Path", the
+//    graph-level fusion "gate projection, SiLU, and gate/up multiplication"):
+//    a tile group holds tpc/2 tiles of the gate weight and the same rows of
+//    the up weight, and the epilogue stores silu(gate) * up, with
+//    silu(x) = x * sigmoid(x) in fp32.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -75,6 +80,8 @@ struct GemvParams {
   int M, K, K64, nb;
   int a_f32, a_vec;
   int a_bulk;  // bf16 rows TMA can copy (16-byte aligned, K % 8 == 0)
+  int paired;  // gate (weight 0) and up (weight 1) tiles share each tile group
+  int sc_up, zp_up;  // paired: offsets of the up halves of a stage's scales / zero points
   int ksw, tpc, cluster, R;  // k slices per CTA, tiles per group, stages per tile group
   int cpw, scs;              // chunks per warp and stage; chunks per stage and tile (ksw*cpw)
   int krp, sg;               // staged activation row stride, block sums per row
@@ -138,6 +145,20 @@ __device__ __forceinline__ void store_y(const GemvParams &p, int q, int m, int n
     static_cast<float *>(p.Y[q])[(int64_t)m * p.N[q] + n] = v;
   else
     static_cast<uint16_t *>(p.Y[q])[(int64_t)m * p.N[q] + n] =
+        static_cast<uint16_t>(bf16_bits(v));
+}
+
+// Gated-MLP output: with g = gate + bias_g and u = up + bias_u,
+// Y[m][n] = g * sigmoid(g) * u, in fp32, stored in A's dtype.
+__device__ __forceinline__ void store_gate_up(const GemvParams &p, int m, int n, float g,
+                                              float u) {
+  if (p.bias[0]) g += __ldg(p.bias[0] + n);
+  if (p.bias[1]) u += __ldg(p.bias[1] + n);
+  const float v = g / (1.f + expf(-g)) * u;
+  if (p.a_f32)
+    static_cast<float *>(p.Y[0])[(int64_t)m * p.N[0] + n] = v;
+  else
+    static_cast<uint16_t *>(p.Y[0])[(int64_t)m * p.N[0] + n] =
         static_cast<uint16_t>(bf16_bits(v));
 }
 
@@ -227,9 +248,23 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           const int c = clo + j * p.scs;  // first chunk of the stage
           const int b = (c * kChunkK) >> G::kLog2;
           mbar_arrive_expect_tx(bar, p.stage_tx);
-          tma_load_3d(st, &p.tmw[q], 0, c, tile0, bar);
-          tma_load_3d(st + p.st_sc, &p.tms[q], 0, b, tile0, bar);
-          if (HAS_ZP) tma_load_3d(st + p.st_zp, &p.tmz[q], 0, b >> 1, tile0, bar);
+          if (p.paired) {
+            // Gate tiles fill the first half of the stage, up tiles (same rows)
+            // the second.
+            const int h = p.tpc / 2, t0 = (gi - p.tg_begin[0]) * h;
+            tma_load_3d(st, &p.tmw[0], 0, c, t0, bar);
+            tma_load_3d(st + h * p.scs * kChunkBytes, &p.tmw[1], 0, c, t0, bar);
+            tma_load_3d(st + p.st_sc, &p.tms[0], 0, b, t0, bar);
+            tma_load_3d(st + p.st_sc + p.sc_up, &p.tms[1], 0, b, t0, bar);
+            if (HAS_ZP) {
+              tma_load_3d(st + p.st_zp, &p.tmz[0], 0, b >> 1, t0, bar);
+              tma_load_3d(st + p.st_zp + p.zp_up, &p.tmz[1], 0, b >> 1, t0, bar);
+            }
+          } else {
+            tma_load_3d(st, &p.tmw[q], 0, c, tile0, bar);
+            tma_load_3d(st + p.st_sc, &p.tms[q], 0, b, tile0, bar);
+            if (HAS_ZP) tma_load_3d(st + p.st_zp, &p.tmz[q], 0, b >> 1, tile0, bar);
+          }
         }
         __syncwarp();
         if (++slot == p.nst) {
@@ -360,12 +395,17 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         const int m = mt * 8 + 2 * t + h;
         srow[mt][h] = sS + (m < p.M ? m : 0) * p.sg - blo;
       }
-    const bool direct = p.ksw == 1 && p.cluster == 1;
+    const bool direct = p.ksw == 1 && p.cluster == 1 && !p.paired;
     // This warp's slices of a stage: its chunks, and its tile's scales and
     // zero-point pairs (stage block b0s = first block of the stage).
     const int cofs = (tau * p.scs + ks * p.cpw) * kChunkBytes + lane * 16;
-    const int sofs = p.st_sc + tau * p.nbs * kTileN * kEs;
-    const int zofs = p.st_zp + tau * p.nps * 16;
+    // A pair keeps the up tiles' scales and zero points in 128-byte-aligned
+    // halves of their stage regions.
+    const int ht = p.tpc / 2;
+    const bool up_half = p.paired && tau >= ht;
+    const int sofs = p.st_sc + (up_half ? p.sc_up + (tau - ht) * p.nbs * kTileN * kEs
+                                        : tau * p.nbs * kTileN * kEs);
+    const int zofs = p.st_zp + (up_half ? p.zp_up + (tau - ht) * p.nps * 16 : tau * p.nps * 16);
     uint2 bfrag0 = make_uint2(0, 0), bfrag1 = make_uint2(0, 0);
     int slot = 0;
     uint32_t phase = 0;
@@ -519,6 +559,43 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         }
       }
       named_barrier_sync(kBarConsumers, kConsumers);
+      if (p.paired) {
+        // Rows r < rows/2 are gate rows, r + rows/2 the same rows of up.
+        const int half = rows / 2, ht = p.tpc / 2;
+        const int n_base = (gi - p.tg_begin[0]) * half;
+        const int total = p.M * half;
+        for (int e = tid; e < total; e += kConsumers) {
+          const int m = e / half, r = e - m * half;
+          const int tt = r >> 4, row = r & 15;
+          float vg = 0.f, vu = 0.f;
+          for (int k2 = 0; k2 < p.ksw; ++k2) {
+            vg += sRed[((tt * p.ksw + k2) * kTileN + row) * MC + m];
+            vu += sRed[(((tt + ht) * p.ksw + k2) * kTileN + row) * MC + m];
+          }
+          if (p.cluster == 1) {
+            if (n_base + r < p.N[0]) store_gate_up(p, m, n_base + r, vg, vu);
+          } else {
+            sPart[e] = vg;
+            sPart[total + e] = vu;
+          }
+        }
+        if (p.cluster > 1) {
+          cluster_sync_all();
+          for (int e = tid * p.cluster + crank; e < total; e += kConsumers * p.cluster) {
+            float vg = 0.f, vu = 0.f;
+            for (int r = 0; r < p.cluster; ++r) {
+              vg += ld_dsmem_f32(sPart + e, r);
+              vu += ld_dsmem_f32(sPart + total + e, r);
+            }
+            const int m = e / half, r = e - m * half;
+            if (n_base + r < p.N[0]) store_gate_up(p, m, n_base + r, vg, vu);
+          }
+          cluster_sync_all();
+        } else {
+          named_barrier_sync(kBarConsumers, kConsumers);
+        }
+        continue;
+      }
       const int n_base = (gi - p.tg_begin[q]) * rows;
       const int total = p.M * rows;
       for (int e = tid; e < total; e += kConsumers) {
@@ -572,11 +649,15 @@ bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   // covers K with them.
   if (cpw < min_cpw(a.bs) || (cpw > min_cpw(a.bs) && int64_t(KS) * cpw > K64)) return false;
   const int tpc = kConsumerWarps / ksw;
+  if (a.paired && tpc < 2) return false;  // a gate and an up tile per group
   const int scs = ksw * cpw;
   // Every CTA of a cluster starts inside K.
   if (int64_t(cluster - 1) * scs * ceil_div(K64, int64_t(KS) * cpw) >= K64) return false;
   int64_t tg = 0;
-  for (int i = 0; i < a.count; ++i) tg += ceil_div(ceil_div(a.N[i], kTileN), tpc);
+  if (a.paired)
+    tg = ceil_div(ceil_div(a.N[0], kTileN), tpc / 2);
+  else
+    for (int i = 0; i < a.count; ++i) tg += ceil_div(ceil_div(a.N[i], kTileN), tpc);
   const int MT = a.M <= 8 ? 1 : 2;
   const int R = static_cast<int>(ceil_div(K64, int64_t(KS) * cpw));
   const int64_t kr = int64_t(scs) * R * kChunkK;  // staged activations per row
@@ -593,8 +674,14 @@ bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   L.nbs = nbs;
   L.nps = nps;
   L.st_sc = scs * tpc * kChunkBytes;  // cpw * 8 KB: 128-byte aligned
-  L.st_zp = static_cast<int>(align128(L.st_sc + size_t(tpc) * nbs * kTileN * es));
-  L.stage_bytes = static_cast<int>(align128(L.st_zp + (a.has_zp ? size_t(tpc) * nps * 16 : 0)));
+  // Every TMA destination starts on 128 bytes: a pair's up halves of the
+  // scale and zero-point regions start at aligned offsets.
+  const size_t sc_all = size_t(tpc) * nbs * kTileN * es;
+  const size_t zp_all = a.has_zp ? size_t(tpc) * nps * 16 : 0;
+  L.sc_up = a.paired ? static_cast<int>(align128(sc_all / 2)) : 0;
+  L.zp_up = a.paired ? static_cast<int>(align128(zp_all / 2)) : 0;
+  L.st_zp = static_cast<int>(align128(L.st_sc + (a.paired ? L.sc_up + sc_all / 2 : sc_all)));
+  L.stage_bytes = static_cast<int>(align128(L.st_zp + (a.paired ? L.zp_up + zp_all / 2 : zp_all)));
   L.stage_tx = tpc * (scs * kChunkBytes + nbs * kTileN * es + (a.has_zp ? nps * 16 : 0));
   size_t off = align16(size_t(a.M) * krp * 2);
   L.off_alo = static_cast<int>(off);
@@ -703,7 +790,7 @@ cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int scs, GemvParams 
     const uint64_t dims[3] = {kChunkBytes / 4, K64, N16};
     const uint64_t strides[2] = {kChunkBytes, K64 * kChunkBytes};
     const uint32_t box[3] = {kChunkBytes / 4, static_cast<uint32_t>(scs),
-                             static_cast<uint32_t>(tpc)};
+                             static_cast<uint32_t>(a.paired ? tpc / 2 : tpc)};
     cudaError_t e = make_tmap(&p.tmw[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.packed_b[i],
                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
@@ -712,7 +799,8 @@ cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int scs, GemvParams 
     const uint64_t words = kTileN * es / 4;
     const uint64_t dims[3] = {words, nb, N16};
     const uint64_t strides[2] = {kTileN * es, nb * kTileN * es};
-    const uint32_t box[3] = {static_cast<uint32_t>(words), nbs, static_cast<uint32_t>(tpc)};
+    const uint32_t box[3] = {static_cast<uint32_t>(words), nbs,
+                             static_cast<uint32_t>(a.paired ? tpc / 2 : tpc)};
     cudaError_t e = make_tmap(&p.tms[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.scales[i],
                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
@@ -720,7 +808,7 @@ cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int scs, GemvParams 
   if (a.has_zp) {
     const uint64_t dims[3] = {4, nbz / 2, N16};
     const uint64_t strides[2] = {16, nbz * 8};
-    const uint32_t box[3] = {4, nps, static_cast<uint32_t>(tpc)};
+    const uint32_t box[3] = {4, nps, static_cast<uint32_t>(a.paired ? tpc / 2 : tpc)};
     cudaError_t e = make_tmap(&p.tmz[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.zp[i], dims,
                               strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
@@ -769,7 +857,8 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
 
   GemvParams p = best.layout;
   p.A = a.A;
-  p.nprob = a.count;
+  p.nprob = a.paired ? 1 : a.count;  // a pair walks the gate's tile groups
+  p.paired = a.paired;
   int64_t tg = 0;
   for (int i = 0; i < a.count; ++i) {
     const cudaError_t e = weight_maps(a, i, best.tpc, best.ksw * best.cpw, p);
@@ -779,8 +868,9 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
     p.N[i] = static_cast<int>(a.N[i]);
     p.N16[i] = static_cast<int>(ceil_div(a.N[i], kTileN));
     p.tg_begin[i] = static_cast<int>(tg);
-    tg += ceil_div(p.N16[i], best.tpc);
+    if (!a.paired) tg += ceil_div(p.N16[i], best.tpc);
   }
+  if (a.paired) tg = ceil_div(p.N16[0], best.tpc / 2);
   p.tg_total = static_cast<int>(tg);
   p.M = static_cast<int>(a.M);
   p.K = static_cast<int>(a.K);

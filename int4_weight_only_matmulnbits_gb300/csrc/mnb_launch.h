@@ -58,6 +58,9 @@ struct GroupArgs {
   int bs;
   bool a_f32, scale_f32, has_zp;
   bool pdl;
+  // Gated-MLP pair: weight 0 = gate, weight 1 = up (same N), one output
+  // Y[0] = silu(gate) * up; bias[0] / bias[1] apply before the product.
+  bool paired = false;
 };
 
 // Small-M split-K kernel (M <= kGemvMaxM). Returns cudaErrorNotSupported when
