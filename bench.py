@@ -8,10 +8,11 @@ U[0.002, 0.01]): q 2560->4096, k/v 2560->1024, o 4096->2560, gate/up
 own seeded codes and scales, all resident in HBM before timing.
 
 The step follows the model's data flow: q, k and v read one activation row
-and run as one fused-N launch (mnb_matmul_grouped), as do gate and up; o,
-down and lm_head each read their own row. That is 4 launches per layer and
-145 per step, replayed as one CUDA graph. The step's bytes exceed the
-129 MB L2 many times over, so no flush is needed.
+and run as one fused-N launch (mnb_matmul_grouped); gate and up run as one
+gated-MLP launch that stores SiLU(gate) * up (mnb_matmul_gate_up); o, down
+and lm_head each read their own row. That is 4 launches per layer and 145
+per step, replayed as one CUDA graph. The step's bytes exceed the 129 MB L2
+many times over, so no flush is needed.
 
 Also measured, outside the timed region of the headline number: the prefill
 GEMM at M = 2048 over the seven Qwen3-4B projection shapes (TFLOP/s), when
@@ -199,7 +200,9 @@ def build_decode_step(dev, seed_base=5000):
     bs = 128
     g = torch.Generator(device=dev)
     a_total = sum(ps[0].K for _, ps in plan)
-    y_total = sum(p.N for _, ps in plan for p in ps)
+    # The gated-MLP launch writes one output for its two weights.
+    y_total = sum(ps[0].N if name.endswith("gate_up") else sum(p.N for p in ps)
+                  for name, ps in plan)
     A_all = torch.empty(a_total, dtype=torch.bfloat16, device=dev)
     Y_all = torch.empty(y_total, dtype=torch.bfloat16, device=dev)
     ao = yo = 0
@@ -215,7 +218,8 @@ def build_decode_step(dev, seed_base=5000):
         ao += K
         algo_bytes += K * 2
         ws, Ys = [], []
-        for p in ps:
+        paired = name.endswith("gate_up")
+        for i, p in enumerate(ps):
             seed += 1
             g.manual_seed(seed)
             B = torch.randint(0, 256, (p.N, nb, bs // 2), dtype=torch.uint8, device=dev,
@@ -223,13 +227,25 @@ def build_decode_step(dev, seed_base=5000):
             S = (torch.rand(p.N, nb, device=dev, generator=g) * 0.008 + 0.002).to(torch.bfloat16)
             ws.append(mnb.mnb_prepack(B, S, None, p.N, K, bs))
             del B, S
-            Ys.append(Y_all[yo:yo + p.N].view(1, p.N))
-            yo += p.N
-            algo_bytes += p.N * nb * bs // 2 + p.N * nb * 2 + p.N * 2
+            algo_bytes += p.N * nb * bs // 2 + p.N * nb * 2
+            if not paired or i == 0:
+                Ys.append(Y_all[yo:yo + p.N].view(1, p.N))
+                yo += p.N
+                algo_bytes += p.N * 2
         launches.append((name, ws, A, Ys))
         seed += 1
     torch.cuda.synchronize()
     return launches, A_all, Y_all, algo_bytes
+
+
+def run_launch(mnb, name, ws, A, Ys):
+    """One launch of the decode step."""
+    if name.endswith("gate_up"):
+        mnb.mnb_matmul_gate_up(A, ws[0], ws[1], out=Ys[0])
+    elif len(ws) == 1:
+        mnb.mnb_matmul(A, ws[0], None, out=Ys[0])
+    else:
+        mnb.mnb_matmul_grouped(A, ws, outs=Ys)
 
 
 def time_region(fn, steps, stream):
@@ -301,11 +317,8 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.synchronize()
 
     def step_eager():
-        for _, ws, A, Ys in launches:
-            if len(ws) == 1:
-                mnb.mnb_matmul(A, ws[0], None, out=Ys[0])
-            else:
-                mnb.mnb_matmul_grouped(A, ws, outs=Ys)
+        for name, ws, A, Ys in launches:
+            run_launch(mnb, name, ws, A, Ys)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -376,8 +389,9 @@ def run_gpu(args, rank, world, dist):
                    "launches_per_step": launches_per_step,
                    "algorithmic_bytes_per_step": algo_bytes,
                    "l2": "inputs larger than L2 (2.08 GB per step vs 129 MB)",
-                   "launch": "one CUDA graph per step: per layer fused qkv, o, fused gate+up, "
-                             "down, then lm_head (145 launches), programmatic dependent launch",
+                   "launch": "one CUDA graph per step: per layer fused qkv, o, gated-MLP "
+                             "gate+up (SiLU(gate)*up), down, then lm_head (145 launches), "
+                             "programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
         "hbm_fraction": per_gpu / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": hbm_peak,
@@ -458,11 +472,8 @@ def run_case(args):
     if args.case == "step":
         launches, _, _, algo_bytes = build_decode_step(dev)
         for _ in range(args.steps):
-            for _, ws, A, Ys in launches:
-                if len(ws) == 1:
-                    mnb.mnb_matmul(A, ws[0], None, out=Ys[0])
-                else:
-                    mnb.mnb_matmul_grouped(A, ws, outs=Ys)
+            for name, ws, A, Ys in launches:
+                run_launch(mnb, name, ws, A, Ys)
         torch.cuda.synchronize()
         print(json.dumps({"case": "step", "launches": len(launches) * args.steps,
                           "algorithmic_bytes_per_step": algo_bytes}))
