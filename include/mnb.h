@@ -257,7 +257,10 @@ MNB_API mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,
  *   Y[m,n] = g * sigmoid(g) * u  (fp32, then A's dtype; bf16 to nearest even).
  * gate and up are two prepacked weights of the same N, K, block_size, scale
  * dtype and zero-point presence; each CTA streams matching rows of both, so
- * neither projection is written to memory. All pointers DEVICE; Y [M, N].
+ * neither projection is written to memory (M <= 16: the decode kernel; more
+ * rows: the tensor-core kernel for bf16 activations with 16-byte-aligned
+ * rows, else the decode kernel over 16-row slices). All pointers DEVICE;
+ * Y [M, N].
  * Arguments and errors as mnb_matmul (both zero-point pointers set, or both
  * NULL: MNB_ERR_NULL otherwise); Y must not overlap any input.
  */

@@ -455,6 +455,21 @@ mnb_status mnb_matmul_gate_up(const void *A, const void *packed_gate,
   g.has_zp = zp_gate != nullptr;
   g.pdl = g_pdl.load() != 0;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M > kGemvMaxM) {
+    // The tensor-core kernel's paired mode, when it takes these activations.
+    MatmulArgs t{A, packed_gate, scales_gate, zp_gate, bias_gate, Y, M, N, K, block_size,
+                 a_dtype == MNB_F32, scale_dtype == MNB_F32, g_pdl.load() != 0};
+    t.paired = true;
+    t.packed_b2 = packed_up;
+    t.scales2 = scales_up;
+    t.zp2 = zp_up;
+    t.bias2 = bias_up;
+    if (gemm_supports(t)) {
+      const cudaError_t e = launch_gemm(t, s);
+      if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_gate_up");
+      return MNB_OK;
+    }
+  }
   // The decode kernel takes up to 16 rows per launch.
   for (int64_t m0 = 0; m0 < M; m0 += kGemvMaxM) {
     g.M = std::min<int64_t>(kGemvMaxM, M - m0);

@@ -29,6 +29,10 @@
 //  * warps 2-9 then read the accumulators with tcgen05.ld (each warp its
 //    TMEM lane quarter and half of the columns), add the bias (staged in
 //    shared memory), round to bf16 and store Y.
+//  * Gated-MLP pairs (the fusion "gate projection, SiLU, and gate/up
+//    multiplication"): a CTA covers 64 output columns; its B tile holds 64
+//    rows of the gate weight and the same 64 rows of the up weight, and the
+//    epilogue stores silu(g) * u from accumulator columns c and 64 + c.
 //  * Shapes with too few output tiles to fill the GPU split K over a
 //    cluster of up to 8 CTAs (128-row tiles): each CTA accumulates its k
 //    range, parks the accumulator in its own shared memory (the drained
@@ -38,6 +42,8 @@
 // Every mbarrier wait is bounded; a wait that runs out records a fault bit
 // and the kernel abandons the tile.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "mnb_common.cuh"
 #include "mnb_launch.h"
@@ -65,13 +71,16 @@ struct GemmParams {
   CUtensorMap tmw;  // codes: {128 words, K64, N16}, box {128, 1, 8}
   CUtensorMap tms;  // scales: {16 scales as words, nb, N16}, box {.., bpc, 8}
   CUtensorMap tmz;  // zero points: {4 words, nbz/2, N16}, box {4, ppc, 8}
-  const float *bias;
+  CUtensorMap tmw2, tms2, tmz2;  // a pair's up weight (boxes of 4 tiles, as the gate's)
+  const float *bias, *bias2;
   void *Y;
   int M, N, K64;
   int has_zp;
   int y_vec;  // Y rows are 16-byte aligned: 16-byte stores
   int sc_bytes, zp_bytes;  // per stage
   int ksplit, kps;  // CTAs splitting K (cluster along z), k stages per CTA
+  int paired;       // gate (tiles 0-3 of the B tile) and up (tiles 4-7)
+  int sc_up, zp_up;  // paired: byte offsets of the up halves in a stage's scales / zero points
 };
 
 // Shared-memory plan (offsets from a 1024-aligned base).
@@ -251,10 +260,24 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         mbar_arrive_expect_tx(bar, S::kATileBytes + kCodeBytes + p.sc_bytes + p.zp_bytes);
         const int blk = (kb * kBK) / BS;
         tma_load_2d(smem + S::kA + s * S::kATileBytes, &p.tma, kb * kBK, m0, bar);
-        tma_load_3d(smem + S::kCodes + s * kCodeBytes, &p.tmw, 0, kb, nt0, bar);
-        tma_load_3d(smem + S::kSc + s * S::kScBytes, &p.tms, 0, blk, nt0, bar);
-        if (HAS_ZP)
-          tma_load_3d(smem + S::kZp + s * S::kZpBytes, &p.tmz, 0, blk >> 1, nt0, bar);
+        unsigned char *cd = smem + S::kCodes + s * kCodeBytes;
+        unsigned char *sd = smem + S::kSc + s * S::kScBytes;
+        unsigned char *zd = smem + S::kZp + s * S::kZpBytes;
+        if (p.paired) {
+          const int t0 = blockIdx.x * (kTilesN / 2);  // 4 tiles of each weight
+          tma_load_3d(cd, &p.tmw, 0, kb, t0, bar);
+          tma_load_3d(cd + (kTilesN / 2) * kChunkBytes, &p.tmw2, 0, kb, t0, bar);
+          tma_load_3d(sd, &p.tms, 0, blk, t0, bar);
+          tma_load_3d(sd + p.sc_up, &p.tms2, 0, blk, t0, bar);
+          if (HAS_ZP) {
+            tma_load_3d(zd, &p.tmz, 0, blk >> 1, t0, bar);
+            tma_load_3d(zd + p.zp_up, &p.tmz2, 0, blk >> 1, t0, bar);
+          }
+        } else {
+          tma_load_3d(cd, &p.tmw, 0, kb, nt0, bar);
+          tma_load_3d(sd, &p.tms, 0, blk, nt0, bar);
+          if (HAS_ZP) tma_load_3d(zd, &p.tmz, 0, blk >> 1, nt0, bar);
+        }
       }
     }
   } else if (warp == 1) {
@@ -290,8 +313,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
     {
       const int e = tid - 64;  // 0..255
       if (e < kBN) {
-        const int n = nt0 * kTileN + e;
-        sBias[e] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
+        if (p.paired) {  // gate biases, then up biases, of the CTA's 64 columns
+          const int n = blockIdx.x * (kBN / 2) + (e & (kBN / 2 - 1));
+          const float *b = e < kBN / 2 ? p.bias : p.bias2;
+          sBias[e] = (b && n < p.N) ? __ldg(b + n) : 0.f;
+        } else {
+          const int n = nt0 * kTileN + e;
+          sBias[e] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
+        }
       }
     }
     for (int i = 0; i < nk; ++i) {
@@ -328,7 +357,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         if (HAS_ZP) {
           const int b = blk0 + bi;
           const int pairs = BS < 32 ? 2 : 1;
-          const uint2 zw = zp[(tile * pairs + (BS < 32 ? bi >> 1 : 0)) * 2 + (b & 1)];
+          // A pair's up tiles (4-7) start at zp_up bytes.
+          const int zt = (p.paired && tile >= kTilesN / 2)
+                             ? p.zp_up / 16 + (tile - kTilesN / 2) * pairs
+                             : tile * pairs;
+          const uint2 zw = zp[(zt + (BS < 32 ? bi >> 1 : 0)) * 2 + (b & 1)];
           zc0[bi] = (0x4300u | ((zw.x >> (4 * g)) & 15)) * 0x10001u;
           zc1[bi] = (0x4300u | ((zw.y >> (4 * g)) & 15)) * 0x10001u;
         }
@@ -378,6 +411,43 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
 #pragma unroll
         for (int i = 0; i < 32; ++i) part[(c * 32 + i) * kBH + row] = v[i];
       }
+    } else if (!fault && p.paired) {
+      // Output columns 32 h .. 32 h + 31 of the CTA's 64: gate sums in
+      // accumulator columns 32 h + i, up sums in 64 + 32 h + i.
+      tc_fence_after();
+      const int quarter = warp & 3, h = (warp - 2) >> 2;
+      const int n0 = blockIdx.x * (kBN / 2) + 32 * h;
+#pragma unroll 1
+      for (int mh = 0; mh < MH; ++mh) {
+        const int m = m0 + mh * kBH + quarter * 32 + lane;
+        float vg[32], vu[32];
+        const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
+        tmem_ld32(tmem + lanes + mh * kBN + 32 * h, vg);
+        tmem_ld32(tmem + lanes + mh * kBN + kBN / 2 + 32 * h, vu);
+        if (m < p.M) {
+          float o[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int j = out_col(i);
+            const float gg = vg[i] + sBias[32 * h + j];
+            o[j] = gg / (1.f + expf(-gg)) * (vu[i] + sBias[kBN / 2 + 32 * h + j]);
+          }
+          uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
+          if (n0 + 32 <= p.N && p.y_vec) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = bf16_bits(o[i + 2 * e]) | (bf16_bits(o[i + 2 * e + 1]) << 16);
+              *reinterpret_cast<uint4 *>(yrow + n0 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            for (int i = 0; i < 32; ++i)
+              if (n0 + i < p.N) yrow[n0 + i] = static_cast<uint16_t>(bf16_bits(o[i]));
+          }
+        }
+      }
     } else if (!fault) {
       tc_fence_after();
       const int quarter = warp & 3;          // TMEM lanes this warp may read
@@ -421,7 +491,51 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
     // Split-K reduction: this CTA's slice of the tile's columns, summed over
     // the cluster's partials in rank order.
     cluster_sync_all();
-    if (warp >= 2) {
+    if (warp >= 2 && p.paired) {
+      // Gate column groups only (16, 32 or 64 columns per CTA); the up sums
+      // sit 64 columns further.
+      const float *part = reinterpret_cast<const float *>(smem);
+      const int cols = (kBN / 2) / p.ksplit;
+      const int items = kBH * (cols / 16);
+      const int n_base = blockIdx.x * (kBN / 2);
+      for (int it = tid - 64; it < items; it += 32 * kDqWarps) {
+        const int row = it % kBH, c0 = blockIdx.z * cols + (it / kBH) * 16;
+        float vg[16], vu[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) vg[i] = vu[i] = 0.f;
+        for (int q = 0; q < p.ksplit; ++q)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            vg[i] += ld_dsmem_f32(part + (c0 + i) * kBH + row, q);
+            vu[i] += ld_dsmem_f32(part + (kBN / 2 + c0 + i) * kBH + row, q);
+          }
+        const int m = m0 + row;
+        if (m < p.M) {
+          float o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = out_col(i);
+            const float gg = vg[i] + sBias[c0 + j];
+            o[j] = gg / (1.f + expf(-gg)) * (vu[i] + sBias[kBN / 2 + c0 + j]);
+          }
+          uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
+          const int n0 = n_base + c0;
+          if (n0 + 16 <= p.N && p.y_vec) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = bf16_bits(o[i + 2 * e]) | (bf16_bits(o[i + 2 * e + 1]) << 16);
+              *reinterpret_cast<uint4 *>(yrow + n0 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            for (int i = 0; i < 16; ++i)
+              if (n0 + i < p.N) yrow[n0 + i] = static_cast<uint16_t>(bf16_bits(o[i]));
+          }
+        }
+      }
+    } else if (warp >= 2) {
       const float *part = reinterpret_cast<const float *>(smem);
       const int cols = kBN / p.ksplit;  // 16, 32, 64 or 128
       const int items = kBH * (cols / 16);
@@ -551,6 +665,9 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   if (!gemm_supports(a)) return cudaErrorNotSupported;
   GemmParams p{};
   const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
+  // Output columns per CTA: 128, or 64 for a gated-MLP pair (64 gate and 64
+  // up rows fill the B tile).
+  const int64_t cols = a.paired ? kBN / 2 : kBN;
   // Tile height (128 or 256 rows) and K split (cluster of 1..8 CTAs, 128-row
   // tiles only) by a cost model fitted to GB300 measurements: a CTA spends
   // about 0.77 us per 64-wide k stage with 128 rows and 1.12 us with 256
@@ -565,10 +682,10 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
     double best = 0.0;
     bool have = false;
     for (int h = 1; h <= 2; ++h)
-      for (int c = 1; c <= (h == 1 ? 8 : 1); c *= 2) {
+      for (int c = 1; c <= (h == 1 ? (a.paired ? 4 : 8) : 1); c *= 2) {
         const int64_t kps = ceil_div(int64_t(K64), int64_t(c));
         if (c > 1 && (kps < 4 || (c - 1) * kps >= int64_t(K64))) continue;
-        const int64_t ctas = ceil_div(a.M, int64_t(kBH) * h) * ceil_div(a.N, kBN) * c;
+        const int64_t ctas = ceil_div(a.M, int64_t(kBH) * h) * ceil_div(a.N, cols) * c;
         if (h == 2 && ctas < sms) continue;  // a lone 256-row CTA per SM is slower
         const int64_t slots = resident_ctas(c);
         if (slots <= 0) continue;
@@ -596,35 +713,53 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
                   CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
   }
-  {
-    const uint64_t dims[3] = {kChunkBytes / 4, K64, N16};
-    const uint64_t strides[2] = {kChunkBytes, K64 * kChunkBytes};
-    const uint32_t box[3] = {kChunkBytes / 4, 1, kTilesN};
-    e = make_tmap(&p.tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.packed_b, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (e != cudaSuccess) return e;
-  }
-  {
-    const uint64_t words = kTileN * es / 4;
-    const uint64_t dims[3] = {words, nb, N16};
-    const uint64_t strides[2] = {kTileN * es, nb * kTileN * es};
-    const uint32_t box[3] = {static_cast<uint32_t>(words), bpc, kTilesN};
-    e = make_tmap(&p.tms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.scales, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (e != cudaSuccess) return e;
-  }
+  // Weight maps: one weight in boxes of 8 tiles, or each of a pair in boxes
+  // of 4 tiles.
+  const uint32_t bt = a.paired ? kTilesN / 2 : kTilesN;
+  auto weight_maps = [&](const void *pb, const void *sc, const void *zp, CUtensorMap *mw,
+                         CUtensorMap *ms, CUtensorMap *mz) -> cudaError_t {
+    {
+      const uint64_t dims[3] = {kChunkBytes / 4, K64, N16};
+      const uint64_t strides[2] = {kChunkBytes, K64 * kChunkBytes};
+      const uint32_t box[3] = {kChunkBytes / 4, 1, bt};
+      const cudaError_t r = make_tmap(mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, pb, dims, strides,
+                                      box, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (r != cudaSuccess) return r;
+    }
+    {
+      const uint64_t words = kTileN * es / 4;
+      const uint64_t dims[3] = {words, nb, N16};
+      const uint64_t strides[2] = {kTileN * es, nb * kTileN * es};
+      const uint32_t box[3] = {static_cast<uint32_t>(words), bpc, bt};
+      const cudaError_t r = make_tmap(ms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, sc, dims, strides,
+                                      box, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (r != cudaSuccess) return r;
+    }
+    if (zp) {
+      const uint64_t dims[3] = {4, nbz / 2, N16};
+      const uint64_t strides[2] = {16, nbz * 8};
+      const uint32_t box[3] = {4, ppc, bt};
+      const cudaError_t r = make_tmap(mz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, zp, dims, strides,
+                                      box, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  };
+  e = weight_maps(a.packed_b, a.scales, a.zp, &p.tmw, &p.tms, &p.tmz);
+  if (e != cudaSuccess) return e;
   p.sc_bytes = static_cast<int>(kTilesN * bpc * kTileN * es);
-  p.zp_bytes = 0;
-  if (a.zp) {
-    const uint64_t dims[3] = {4, nbz / 2, N16};
-    const uint64_t strides[2] = {16, nbz * 8};
-    const uint32_t box[3] = {4, ppc, kTilesN};
-    e = make_tmap(&p.tmz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.zp, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  p.zp_bytes = a.zp ? static_cast<int>(kTilesN * ppc * 16) : 0;
+  if (a.paired) {
+    e = weight_maps(a.packed_b2, a.scales2, a.zp2, &p.tmw2, &p.tms2, &p.tmz2);
     if (e != cudaSuccess) return e;
-    p.zp_bytes = static_cast<int>(kTilesN * ppc * 16);
+    p.paired = 1;
+    // The up halves start where tile 4 would (a multiple of 128 bytes for the
+    // scales); zero points start at 128 bytes at least.
+    p.sc_up = static_cast<int>((kTilesN / 2) * bpc * kTileN * es);
+    p.zp_up = static_cast<int>(std::max<uint64_t>(128, (kTilesN / 2) * ppc * 16));
   }
   p.bias = a.bias;
+  p.bias2 = a.bias2;
   p.Y = a.Y;
   p.M = static_cast<int>(a.M);
   p.N = static_cast<int>(a.N);
@@ -633,7 +768,7 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
   p.ksplit = ksplit;
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
-  const dim3 grid(static_cast<unsigned>(ceil_div(a.N, kBN)),
+  const dim3 grid(static_cast<unsigned>(ceil_div(a.N, cols)),
                   static_cast<unsigned>(ceil_div(a.M, int64_t(kBH) * mh)),
                   static_cast<unsigned>(ksplit));
   switch (a.bs) {

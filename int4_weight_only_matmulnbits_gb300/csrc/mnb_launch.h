@@ -39,6 +39,11 @@ struct MatmulArgs {
   int bs;
   bool a_f32, scale_f32;
   bool pdl;  // programmatic dependent launch
+  // Gated-MLP pair for the tensor-core kernel: the "up" weight (same shape);
+  // Y = silu(A gate^T + bias) * (A up^T + bias2).
+  bool paired = false;
+  const void *packed_b2 = nullptr, *scales2 = nullptr, *zp2 = nullptr;
+  const float *bias2 = nullptr;
 };
 
 cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream);

@@ -97,3 +97,32 @@ def test_gate_up_matches_two_projections(dev):
 def test_gate_up_bitwise_reproducible(dev):
     g, u = pair(2, 2560, 9728, 128, torch.bfloat16, False, bias=True, seed=13)
     assert torch.equal(run(dev, g, u), run(dev, g, u))
+
+
+@pytest.mark.parametrize("bs", [32, 128, 256])
+@pytest.mark.parametrize("with_zp", [False, True])
+def test_gate_up_tensor_core_path(dev, bs, with_zp):
+    """M > 16 with bf16 activations: the tensor-core kernel's paired mode
+    (64 output columns per CTA; ragged M and N; the split-K variant for the
+    small shapes). The per-weight bf16 rounding of this path averages out at
+    K >= 256, where the stated bound applies."""
+    i = 0
+    for (M, N, K) in ((40, 1000, 512), (300, 777, 1024), (129, 2560, 256), (2048, 130, 768)):
+        i += 1
+        g, u = pair(M, N, K, bs, torch.bfloat16, with_zp, bias=(i % 2 == 1), seed=90 * bs + i)
+        Y = run(dev, g, u)
+        rng = np.random.default_rng(i)
+        rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, 7, replace=False)]))
+        cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 40, replace=False)]))
+        check_pair(Y, g, u, f"tensor-core M{M} N{N} K{K} bs{bs}", rows=rows, cols=cols)
+
+
+def test_gate_up_qwen3_4b_prefill_sampled(dev):
+    """Qwen3-4B gate/up at M = 2048 (bf16, bs 128, zero points, bias):
+    8 rows x 64 columns sampled."""
+    g, u = pair(2048, 9728, 2560, 128, torch.bfloat16, True, bias=True, seed=21)
+    Y = run(dev, g, u)
+    rng = np.random.default_rng(2)
+    rows = np.sort(rng.choice(2048, 8, replace=False))
+    cols = np.sort(rng.choice(9728, 64, replace=False))
+    check_pair(Y, g, u, "qwen3-4b prefill gate/up", rows=rows, cols=cols)
