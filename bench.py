@@ -238,6 +238,36 @@ def build_decode_step(dev, seed_base=5000):
     return launches, A_all, Y_all, algo_bytes
 
 
+def build_decode_chain(mnb, launches):
+    """The decode step as one chain (mnb_chain_build): the same weights,
+    activations and outputs as `launches`, with the decoder's dependencies:
+    q, k, v after the previous layer's down projection, o after q, k and v,
+    the gated-MLP pair after o, down after the pair, lm_head after the last
+    down. Each op still reads its own activation row."""
+    ops = []
+    prev_down = qkv = o_idx = gu_idx = None
+    for name, ws, A, Ys in launches:
+        kind = name.split(".")[-1]
+        if kind == "qkv":
+            deps = () if prev_down is None else (prev_down,)
+            first = len(ops)
+            for w, Y in zip(ws, Ys):
+                ops.append(mnb.ChainOp(A, w, Y, deps=deps))
+            qkv = tuple(range(first, len(ops)))
+        elif kind == "o":
+            ops.append(mnb.ChainOp(A, ws[0], Ys[0], deps=qkv))
+            o_idx = len(ops) - 1
+        elif kind == "gate_up":
+            ops.append(mnb.ChainOp(A, ws[0], Ys[0], up=ws[1], deps=(o_idx,)))
+            gu_idx = len(ops) - 1
+        elif kind == "down":
+            ops.append(mnb.ChainOp(A, ws[0], Ys[0], deps=(gu_idx,)))
+            prev_down = len(ops) - 1
+        else:
+            ops.append(mnb.ChainOp(A, ws[0], Ys[0], deps=(prev_down,)))
+    return mnb.mnb_chain_build(ops)
+
+
 def run_launch(mnb, name, ws, A, Ys):
     """One launch of the decode step."""
     if name.endswith("gate_up"):
@@ -362,10 +392,17 @@ def run_gpu(args, rank, world, dist):
         step_e2e()
     t_e2e = time_region(step_e2e, args.steps, cur)
 
-    ts = torch.tensor([t, t_e2e], device=dev, dtype=torch.float64)
+    # The same step as one persistent launch (mnb_chain_run), for comparison;
+    # not the headline: the graph of launches is faster on this workload.
+    chain = build_decode_chain(mnb, launches)
+    for _ in range(3):
+        chain.run()
+    t_chain = time_region(chain.run, args.steps, cur)
+
+    ts = torch.tensor([t, t_e2e, t_chain], device=dev, dtype=torch.float64)
     if dist:
         dist.all_reduce(ts, op=dist.ReduceOp.MAX)
-    t, t_e2e = ts.tolist()
+    t, t_e2e, t_chain = ts.tolist()
 
     if rank != 0:
         return
@@ -409,6 +446,10 @@ def run_gpu(args, rank, world, dist):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": prefill,
+        "decode_chain": {"value": algo_bytes * args.steps / t_chain / 1e9, "unit": "GB/s",
+                         "ms_per_step": 1e3 * t_chain / args.steps, "launches_per_step": 1,
+                         "note": "the same step and dependencies as one persistent "
+                                 "cooperative launch (mnb_chain_run)"},
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

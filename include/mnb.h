@@ -291,10 +291,106 @@ MNB_API void mnb_set_programmatic_launch(int enable);
  * runs out records a bit in a device fault word, abandons its tile and
  * exits instead of hanging. This call waits for the current device to be
  * idle, returns the fault bits seen since the last call in *fault_bits
- * (HOST; 0 = none; 1 = decode kernel, 2 = tensor-core kernel) and clears
+ * (HOST; 0 = none; 1 = decode kernel, 2 = tensor-core kernel, 4 = decode
+ * chain) and clears
  * them. Errors: MNB_ERR_NULL, MNB_ERR_CUDA.
  */
 MNB_API mnb_status mnb_fault_status(unsigned int *fault_bits);
+
+/*
+ * Decode chain: a sequence of MatMulNBits projections with declared data
+ * dependencies, run as ONE persistent cooperative kernel launch.
+ *
+ * The page "Qwen3 CPU Inference Critical Path" (section "Prepared
+ * weight-only plan") describes one operator call per projection; a decode
+ * step of a transformer runs hundreds of them back to back (per layer
+ * q/k/v, o, gate/up and down, then the LM head), each small enough that a
+ * kernel launch's fixed start and drain cost rivals its weight streaming.
+ * This entry point has no counterpart in the pages: it is the GB300
+ * executor for such a sequence. Every op computes exactly what
+ * mnb_matmul (or, for a gated-MLP pair, mnb_matmul_gate_up) computes for
+ * its arguments; results are bitwise identical from run to run.
+ *
+ * Execution: one CTA per resident slot of every SM (cooperative launch, so
+ * all CTAs run at once). Each CTA streams the packed weights of its share
+ * of every op, in op order, through a ring of shared-memory stages, across
+ * op boundaries; an op's activations are read only after every op listed in
+ * its deps[] has stored all of its Y (device-scope release/acquire on a
+ * per-op completion counter in the plan buffer). Every wait is bounded: a
+ * wait that runs out records fault bit 4 (mnb_fault_status), makes every
+ * other wait of the launch give up at once, and the launch ends with the
+ * plan's counters reset.
+ */
+typedef struct {
+  const void *A;         /* [M, K] activations, a_dtype                      */
+  void *Y;               /* [M, N] output, a_dtype                           */
+  const void *packed_b;  /* prepacked weight (mnb_prepack / mnb_prepack_qdq) */
+  const void *packed_scales;
+  const void *packed_zp; /* NULL: zero point 8                               */
+  const float *bias;     /* [N] fp32 or NULL                                 */
+  /* Gated-MLP pair: the up weight (same N, K), else all four NULL; then
+   * Y = silu(A gate^T + bias) * (A up^T + bias_up), silu(x) = x sigmoid(x). */
+  const void *packed_b_up;
+  const void *packed_scales_up;
+  const void *packed_zp_up;
+  const float *bias_up;
+  int64_t N, K;
+  /* Indices of EARLIER ops whose Y must be complete before this op reads
+   * A; -1 = unused slot. */
+  int32_t deps[4];
+} mnb_chain_op;
+
+/* Launch description filled by mnb_chain_build (HOST struct; pass it
+ * unchanged to mnb_chain_run together with the plan buffer it was built
+ * for). */
+typedef struct {
+  uint64_t plan_bytes;  /* device bytes the plan buffer needs             */
+  int32_t n_ops, n_segments, grid, smem_bytes;
+  int32_t M, block_size, a_dtype, scale_dtype, has_zero_points;
+  int32_t ring_stages, k_max, tiles_per_segment, ctas_per_sm;
+  uint64_t check;       /* checksum of the fields above                   */
+} mnb_chain_info;
+
+/*
+ * Plans a chain. ops: HOST array of n_ops (1..4096) op descriptors, all with
+ * the same block_size, activation dtype, scale dtype and zero-point presence
+ * (DEVICE pointers inside). M: activation rows, 1..8.
+ *
+ * With plan == NULL only *info is filled (info->plan_bytes tells how large
+ * the plan buffer must be). Otherwise plan is a caller-owned DEVICE buffer
+ * of plan_bytes >= info->plan_bytes bytes, 256-byte aligned; the schedule
+ * (which CTA streams which 16-row tiles of which op), the op table and the
+ * completion counters are written into it with a copy on `stream`, and the
+ * call returns after that copy finished (the host image it copies from is
+ * freed on return). The plan holds the op descriptors' device pointers: the
+ * buffers must stay allocated while the plan is used. A plan runs on one
+ * stream at a time.
+ *
+ * Hazards are checked: op j may read an earlier op's Y, overwrite an
+ * earlier op's A or Y, only if that op is among j's (transitive) deps;
+ * no Y may overlap any packed weight or bias of the chain, nor its own A.
+ * Errors: MNB_ERR_NULL, MNB_ERR_SHAPE (M, N, K, n_ops, a deps entry not an
+ * earlier op), MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE, MNB_ERR_ALIGN (as
+ * mnb_matmul; plan not 256-byte aligned), MNB_ERR_ALIAS (a hazard above,
+ * or the plan overlaps a buffer of an op), MNB_ERR_SHAPE also for
+ * plan_bytes too small, MNB_ERR_UNSUPPORTED (the shared-memory layout
+ * does not fit: M or K too large), MNB_ERR_DEVICE, MNB_ERR_CUDA.
+ */
+MNB_API mnb_status mnb_chain_build(const mnb_chain_op *ops, int32_t n_ops,
+                                   int64_t M, int block_size,
+                                   mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                   void *plan, size_t plan_bytes,
+                                   mnb_chain_info *info, mnb_stream_t stream);
+
+/*
+ * Runs a built chain: one cooperative launch on `stream`. plan: DEVICE
+ * buffer written by mnb_chain_build; info: HOST, from the same build.
+ * Errors: MNB_ERR_NULL, MNB_ERR_SHAPE (info altered: checksum mismatch),
+ * MNB_ERR_DEVICE, MNB_ERR_CUDA (the launch failed, e.g. the device cannot
+ * hold every CTA at once).
+ */
+MNB_API mnb_status mnb_chain_run(const void *plan, const mnb_chain_info *info,
+                                 mnb_stream_t stream);
 
 #ifdef __cplusplus
 }

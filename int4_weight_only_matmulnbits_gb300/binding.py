@@ -25,10 +25,30 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_prepacked_sizes", "mnb_prepack", "mnb_unprepack", "mnb_matmul",
            "mnb_matmul_path", "mnb_matmul_from_host",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
-           "mnb_prepack_qdq", "mnb_matmul_gate_up")
+           "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run")
 
 _lock = threading.Lock()
 _lib = None
+
+
+class ChainOpC(ctypes.Structure):
+    """mnb_chain_op (include/mnb.h)."""
+    _fields_ = [("A", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("packed_b", ctypes.c_void_p), ("packed_scales", ctypes.c_void_p),
+                ("packed_zp", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("packed_b_up", ctypes.c_void_p), ("packed_scales_up", ctypes.c_void_p),
+                ("packed_zp_up", ctypes.c_void_p), ("bias_up", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("deps", ctypes.c_int32 * 4)]
+
+
+class ChainInfoC(ctypes.Structure):
+    """mnb_chain_info (include/mnb.h)."""
+    _fields_ = [("plan_bytes", ctypes.c_uint64)] + [
+        (f, ctypes.c_int32) for f in ("n_ops", "n_segments", "grid", "smem_bytes", "M",
+                                      "block_size", "a_dtype", "scale_dtype",
+                                      "has_zero_points", "ring_stages", "k_max",
+                                      "tiles_per_segment", "ctas_per_sm")] + [
+        ("check", ctypes.c_uint64)]
 
 
 class MnbError(RuntimeError):
@@ -93,6 +113,11 @@ def load(build_if_missing: bool = False):
         lib.mnb_matmul_grouped.restype = i32
         lib.mnb_fault_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.mnb_fault_status.restype = i32
+        lib.mnb_chain_build.argtypes = [ctypes.POINTER(ChainOpC), i32, i64, i32, i32, i32, p,
+                                        sz, ctypes.POINTER(ChainInfoC), p]
+        lib.mnb_chain_build.restype = i32
+        lib.mnb_chain_run.argtypes = [p, ctypes.POINTER(ChainInfoC), p]
+        lib.mnb_chain_run.restype = i32
         _lib = lib
         return lib
 
@@ -306,3 +331,90 @@ def mnb_matmul_gate_up(A: torch.Tensor, gate: PackedWeight, up: PackedWeight,
         _ptr(bias_up), M, gate.N, gate.K, gate.block_size, _ptr(out), _dtype_code(A.dtype),
         _dtype_code(gate.scale_dtype), _stream(stream)), "mnb_matmul_gate_up")
     return out
+
+
+@dataclass
+class ChainOp:
+    """One projection of a decode chain: out = A @ dequant(weight)^T + bias,
+    or, with `up`, silu(A @ gate^T + bias) * (A @ up^T + bias_up). `deps`
+    lists earlier ops (indices) whose outputs must be complete before this
+    op reads A."""
+    A: torch.Tensor
+    weight: PackedWeight
+    out: torch.Tensor
+    bias: torch.Tensor | None = None
+    up: PackedWeight | None = None
+    bias_up: torch.Tensor | None = None
+    deps: tuple = ()
+
+
+class MnbChain:
+    """A built decode chain: the device plan buffer (torch-allocated) and its
+    launch description. Holds references to every tensor of its ops."""
+
+    def __init__(self, ops: list, plan: torch.Tensor, info: ChainInfoC):
+        self.ops = list(ops)
+        self.plan = plan
+        self.info = info
+
+    def describe(self) -> dict:
+        return {f: getattr(self.info, f) for f, _ in ChainInfoC._fields_}
+
+    def run(self, stream=None) -> None:
+        mnb_chain_run(self, stream=stream)
+
+
+def _chain_structs(ops: list):
+    arr = (ChainOpC * len(ops))()
+    first = ops[0]
+    M = first.A.shape[0]
+    for j, o in enumerate(ops):
+        w, up = o.weight, o.up
+        if o.A.dim() != 2 or o.A.shape != (M, w.K) or not o.A.is_contiguous():
+            raise ValueError(f"op {j}: A must be a contiguous [{M}, {w.K}] tensor")
+        if o.out.shape != (M, w.N) or o.out.dtype != first.A.dtype or not o.out.is_contiguous():
+            raise ValueError(f"op {j}: out must be a contiguous [{M}, {w.N}] tensor of A's dtype")
+        if len(o.deps) > 4:
+            raise ValueError(f"op {j}: at most 4 deps")
+        if up is not None and (up.N, up.K) != (w.N, w.K):
+            raise ValueError(f"op {j}: up must match the gate's N and K")
+        deps = list(o.deps) + [-1] * (4 - len(o.deps))
+        c = arr[j]
+        c.A, c.Y = o.A.data_ptr(), o.out.data_ptr()
+        c.packed_b, c.packed_scales = w.packed_b.data_ptr(), w.packed_scales.data_ptr()
+        c.packed_zp = None if w.packed_zp is None else w.packed_zp.data_ptr()
+        c.bias = None if o.bias is None else o.bias.data_ptr()
+        if up is not None:
+            c.packed_b_up, c.packed_scales_up = up.packed_b.data_ptr(), up.packed_scales.data_ptr()
+            c.packed_zp_up = None if up.packed_zp is None else up.packed_zp.data_ptr()
+            c.bias_up = None if o.bias_up is None else o.bias_up.data_ptr()
+        c.N, c.K = w.N, w.K
+        for k in range(4):
+            c.deps[k] = deps[k]
+    return arr, M
+
+
+def mnb_chain_build(ops: list, *, stream=None) -> MnbChain:
+    """Plan a chain of projections (one persistent launch per run). All ops
+    share the block size, activation dtype, scale dtype and zero-point
+    presence; M (rows of A) is 1..8."""
+    if not ops:
+        raise ValueError("empty chain")
+    lib = load()
+    arr, M = _chain_structs(ops)
+    w0 = ops[0].weight
+    info = ChainInfoC()
+    args = (arr, len(ops), M, w0.block_size, _dtype_code(ops[0].A.dtype),
+            _dtype_code(w0.scale_dtype))
+    _check(lib.mnb_chain_build(*args, None, 0, ctypes.byref(info), _stream(stream)),
+           "mnb_chain_build")
+    plan = torch.empty(int(info.plan_bytes), dtype=torch.uint8, device=ops[0].A.device)
+    _check(lib.mnb_chain_build(*args, ctypes.c_void_p(plan.data_ptr()), plan.numel(),
+                               ctypes.byref(info), _stream(stream)), "mnb_chain_build")
+    return MnbChain(ops, plan, info)
+
+
+def mnb_chain_run(chain: MnbChain, *, stream=None) -> None:
+    """Run every op of a built chain in one cooperative launch on `stream`."""
+    _check(load().mnb_chain_run(ctypes.c_void_p(chain.plan.data_ptr()), ctypes.byref(chain.info),
+                                _stream(stream)), "mnb_chain_run")

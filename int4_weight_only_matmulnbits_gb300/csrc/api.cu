@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/mnb.h"
 #include "mnb_common.cuh"
@@ -161,6 +162,50 @@ mnb_status run_matmul(const void *A, const void *packed_b, const void *scales,
   return MNB_OK;
 }
 
+// The Python binding mirrors these two structs field by field.
+static_assert(sizeof(mnb_chain_op) == 112, "mnb_chain_op layout");
+static_assert(sizeof(mnb_chain_info) == 72, "mnb_chain_info layout");
+
+uint64_t chain_checksum(const mnb_chain_info &i) {
+  const int64_t f[] = {static_cast<int64_t>(i.plan_bytes), i.n_ops, i.n_segments, i.grid,
+                       i.smem_bytes, i.M, i.block_size, i.a_dtype, i.scale_dtype,
+                       i.has_zero_points, i.ring_stages, i.k_max, i.tiles_per_segment,
+                       i.ctas_per_sm};
+  uint64_t h = 1469598103934665603ull;  // FNV-1a over the fields
+  for (int64_t v : f)
+    for (int b = 0; b < 8; ++b) {
+      h ^= static_cast<uint64_t>(v >> (8 * b)) & 0xFFu;
+      h *= 1099511628211ull;
+    }
+  return h;
+}
+
+// Memory ranges an op reads (A, weights, biases) and writes (Y).
+struct OpRanges {
+  const void *a, *y, *w[8];
+  size_t na, ny, nw[8];
+};
+
+OpRanges op_ranges(const mnb_chain_op &o, int64_t M, int bs, int a_dtype, int scale_dtype) {
+  OpRanges r{};
+  const size_t es = dtype_size(a_dtype);
+  r.a = o.A;
+  r.na = size_t(M) * o.K * es;
+  r.y = o.Y;
+  r.ny = size_t(M) * o.N * es;
+  const Sizes sz = packed_sizes(o.N, o.K, bs, scale_dtype, o.packed_zp != nullptr);
+  const void *w[8] = {o.packed_b, o.packed_scales, o.packed_zp, o.bias,
+                      o.packed_b_up, o.packed_scales_up, o.packed_zp_up, o.bias_up};
+  const size_t nw[8] = {sz.b, sz.s, sz.z, o.bias ? size_t(o.N) * 4 : 0,
+                        o.packed_b_up ? sz.b : 0, o.packed_b_up ? sz.s : 0,
+                        o.packed_zp_up ? sz.z : 0, o.bias_up ? size_t(o.N) * 4 : 0};
+  for (int i = 0; i < 8; ++i) {
+    r.w[i] = w[i];
+    r.nw[i] = w[i] ? nw[i] : 0;
+  }
+  return r;
+}
+
 }  // namespace
 
 int sm_count() {
@@ -210,8 +255,10 @@ mnb_status mnb_fault_status(unsigned int *fault_bits) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = gemv_take_fault(&a);
   if (e == cudaSuccess) e = gemm_take_fault(&b);
+  unsigned int c = 0;
+  if (e == cudaSuccess) e = chain_take_fault(&c);
   if (e != cudaSuccess) return cuda_fail(e, "mnb_fault_status");
-  *fault_bits = a | b;
+  *fault_bits = a | b | c;
   return MNB_OK;
 }
 
@@ -509,6 +556,149 @@ mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,
   if (rs != MNB_OK) return rs;
   e = cudaMemcpyAsync(Y_host, Y_dev, size_t(M) * N * es, cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_from_host (Y copy)");
+  return MNB_OK;
+}
+
+mnb_status mnb_chain_build(const mnb_chain_op *ops, int32_t n_ops, int64_t M,
+                           int block_size, mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                           void *plan, size_t plan_bytes, mnb_chain_info *info,
+                           mnb_stream_t stream) {
+  if (!ops || !info) return MNB_ERR_NULL;
+  if (n_ops < 1 || n_ops > kChainMaxOps || M < 1 || M > kChainMaxM) return MNB_ERR_SHAPE;
+  if (!valid_block_size(block_size)) return MNB_ERR_BLOCKSIZE;
+  if (!valid_dtype(a_dtype) || !valid_dtype(scale_dtype)) return MNB_ERR_DTYPE;
+  const bool has_zp = ops[0].packed_zp != nullptr;
+  const size_t es = dtype_size(a_dtype);
+  std::vector<ChainOp> cops(n_ops);
+  std::vector<OpRanges> rg(n_ops);
+  for (int j = 0; j < n_ops; ++j) {
+    const mnb_chain_op &o = ops[j];
+    if (!o.A || !o.Y || !o.packed_b || !o.packed_scales) return MNB_ERR_NULL;
+    if ((o.packed_zp != nullptr) != has_zp) return MNB_ERR_NULL;
+    const bool paired = o.packed_b_up != nullptr;
+    if (paired && (!o.packed_scales_up || (o.packed_zp_up != nullptr) != has_zp))
+      return MNB_ERR_NULL;
+    if (!paired && (o.packed_scales_up || o.packed_zp_up || o.bias_up)) return MNB_ERR_NULL;
+    mnb_status st = check_shape(o.N, o.K, block_size, scale_dtype);
+    if (st != MNB_OK) return st;
+    const void *al16[6] = {o.packed_b, o.packed_scales, o.packed_zp,
+                           o.packed_b_up, o.packed_scales_up, o.packed_zp_up};
+    for (const void *q : al16)
+      if (q && !aligned(q, 16)) return MNB_ERR_ALIGN;
+    if (!aligned(o.A, es) || !aligned(o.Y, es) || (o.bias && !aligned(o.bias, 4)) ||
+        (o.bias_up && !aligned(o.bias_up, 4)))
+      return MNB_ERR_ALIGN;
+    for (int k = 0; k < kChainMaxDeps; ++k)
+      if (o.deps[k] < -1 || o.deps[k] >= j) return MNB_ERR_SHAPE;
+    rg[j] = op_ranges(o, M, block_size, a_dtype, scale_dtype);
+    ChainOp &c = cops[j];
+    c.A = o.A;
+    c.Y = o.Y;
+    c.b[0] = o.packed_b;
+    c.s[0] = o.packed_scales;
+    c.z[0] = o.packed_zp;
+    c.bias[0] = o.bias;
+    c.b[1] = o.packed_b_up;
+    c.s[1] = o.packed_scales_up;
+    c.z[1] = o.packed_zp_up;
+    c.bias[1] = o.bias_up;
+    c.N = o.N;
+    c.K = o.K;
+    c.paired = paired;
+    for (int k = 0; k < kChainMaxDeps; ++k) c.dep[k] = o.deps[k];
+  }
+  // Hazards: transitive dependencies as bit sets.
+  const int words = (n_ops + 63) / 64;
+  std::vector<uint64_t> reach(size_t(n_ops) * words, 0);
+  for (int j = 0; j < n_ops; ++j) {
+    uint64_t *rj = reach.data() + size_t(j) * words;
+    for (int k = 0; k < kChainMaxDeps; ++k) {
+      const int d = ops[j].deps[k];
+      if (d < 0) continue;
+      const uint64_t *rd = reach.data() + size_t(d) * words;
+      for (int w = 0; w < words; ++w) rj[w] |= rd[w];
+      rj[d / 64] |= uint64_t(1) << (d % 64);
+    }
+  }
+  for (int j = 0; j < n_ops; ++j) {
+    const OpRanges &a = rg[j];
+    if (overlap(a.y, a.ny, a.a, a.na)) return MNB_ERR_ALIAS;
+    for (int i = 0; i < n_ops; ++i)
+      for (int w = 0; w < 8; ++w)
+        if (overlap(a.y, a.ny, rg[i].w[w], rg[i].nw[w])) return MNB_ERR_ALIAS;
+    const uint64_t *rj = reach.data() + size_t(j) * words;
+    for (int i = 0; i < j; ++i) {
+      const bool ordered = (rj[i / 64] >> (i % 64)) & 1u;
+      if (ordered) continue;
+      if (overlap(rg[i].y, rg[i].ny, a.a, a.na) || overlap(a.y, a.ny, rg[i].a, rg[i].na) ||
+          overlap(a.y, a.ny, rg[i].y, rg[i].ny))
+        return MNB_ERR_ALIAS;
+    }
+  }
+  mnb_status st = check_device();
+  if (st != MNB_OK) return st;
+  const ChainShape sh{static_cast<int>(M), block_size, a_dtype == MNB_F32,
+                      scale_dtype == MNB_F32, has_zp};
+  ChainGeom g{};
+  std::vector<unsigned char> image;
+  cudaError_t e = chain_plan(cops.data(), n_ops, sh, g, plan ? &image : nullptr);
+  if (e == cudaErrorNotSupported) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "no chain layout for M=%lld, largest K=%d, bs=%d", (long long)M, g.kmax,
+                  block_size);
+    return MNB_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_chain_build (plan)");
+  mnb_chain_info inf{};
+  inf.plan_bytes = g.plan_bytes;
+  inf.n_ops = n_ops;
+  inf.n_segments = g.n_segs;
+  inf.grid = g.grid;
+  inf.smem_bytes = g.smem;
+  inf.M = static_cast<int32_t>(M);
+  inf.block_size = block_size;
+  inf.a_dtype = a_dtype;
+  inf.scale_dtype = scale_dtype;
+  inf.has_zero_points = has_zp ? 1 : 0;
+  inf.ring_stages = g.nst;
+  inf.k_max = g.kmax;
+  inf.tiles_per_segment = g.tmax;
+  inf.ctas_per_sm = g.per_sm;
+  inf.check = chain_checksum(inf);
+  if (plan) {
+    if (!aligned(plan, 256)) return MNB_ERR_ALIGN;
+    if (plan_bytes < g.plan_bytes) return MNB_ERR_SHAPE;
+    for (int j = 0; j < n_ops; ++j) {
+      const OpRanges &a = rg[j];
+      bool hit = overlap(plan, plan_bytes, a.a, a.na) || overlap(plan, plan_bytes, a.y, a.ny);
+      for (int w = 0; w < 8; ++w) hit = hit || overlap(plan, plan_bytes, a.w[w], a.nw[w]);
+      if (hit) return MNB_ERR_ALIAS;
+    }
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaMemcpyAsync(plan, image.data(), g.plan_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "mnb_chain_build (plan copy)");
+  }
+  *info = inf;
+  return MNB_OK;
+}
+
+mnb_status mnb_chain_run(const void *plan, const mnb_chain_info *info, mnb_stream_t stream) {
+  if (!plan || !info) return MNB_ERR_NULL;
+  if (chain_checksum(*info) != info->check) return MNB_ERR_SHAPE;
+  if (!aligned(plan, 256)) return MNB_ERR_ALIGN;
+  const ChainShape sh{info->M, info->block_size, info->a_dtype == MNB_F32,
+                      info->scale_dtype == MNB_F32, info->has_zero_points != 0};
+  ChainGeom g{};
+  if (!chain_geom(sh, info->n_ops, info->k_max, info->grid, info->ctas_per_sm,
+                  info->ring_stages, info->n_segments, g) ||
+      g.plan_bytes != info->plan_bytes || g.smem != info->smem_bytes ||
+      g.tmax != info->tiles_per_segment)
+    return MNB_ERR_SHAPE;
+  mnb_status st = check_device();
+  if (st != MNB_OK) return st;
+  const cudaError_t e = chain_launch(plan, sh, g, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_chain_run");
   return MNB_OK;
 }
 

@@ -232,5 +232,6 @@ __device__ __forceinline__ void record_fault(unsigned int *word,
 
 constexpr unsigned int kFaultGemvWait = 1u;
 constexpr unsigned int kFaultGemmWait = 2u;
+constexpr unsigned int kFaultChainWait = 4u;
 
 }  // namespace mnb

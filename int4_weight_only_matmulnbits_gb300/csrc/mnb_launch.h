@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <vector>
+
 namespace mnb {
 
 struct PrepackArgs {
@@ -78,6 +80,45 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream);
 // are 16-byte aligned (K % 8 == 0). Returns cudaErrorNotSupported otherwise.
 bool gemm_supports(const MatmulArgs &a);
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream);
+
+// Decode chain (chain.cu): ops validated by the C ABI.
+constexpr int kChainMaxDeps = 4;
+constexpr int kChainMaxOps = 4096;
+constexpr int kChainMaxM = 8;
+struct ChainOp {
+  const void *A;
+  void *Y;
+  const void *b[2], *s[2], *z[2];  // [1] = up weight of a gated-MLP pair
+  const float *bias[2];
+  int64_t N, K;
+  bool paired;
+  int dep[kChainMaxDeps];
+};
+struct ChainShape {
+  int M, bs;
+  bool a_f32, scale_f32, has_zp;
+};
+// Launch geometry and plan-buffer layout of a chain (a pure function of the
+// shape, the largest K, the grid and the schedule's size).
+struct ChainGeom {
+  int grid, per_sm, nst, tmax, kmax, smem;
+  int n_ops, n_segs;
+  size_t off_ctaseg, off_segs, off_count, off_ctl, plan_bytes;
+};
+// Plans the chain: fills g and, if image != nullptr, the plan's host image
+// (g.plan_bytes bytes). cudaErrorNotSupported if no layout fits.
+cudaError_t chain_plan(const ChainOp *ops, int n, const ChainShape &sh, ChainGeom &g,
+                       std::vector<unsigned char> *image);
+// The schedule part of chain_plan for a fixed g.grid, g.tmax (host only).
+void chain_schedule(const ChainOp *ops, int n, const ChainShape &sh, ChainGeom &g,
+                    std::vector<unsigned char> *image);
+// Recomputes the geometry of a built plan from its recorded sizes; false if
+// they are inconsistent.
+bool chain_geom(const ChainShape &sh, int n_ops, int kmax, int grid, int per_sm, int nst,
+                int n_segs, ChainGeom &g);
+cudaError_t chain_launch(const void *plan, const ChainShape &sh, const ChainGeom &g,
+                         cudaStream_t stream);
+cudaError_t chain_take_fault(unsigned int *out);
 
 int sm_count();
 

@@ -139,3 +139,85 @@ def test_prepack_qdq_rejects_invalid_arguments_on_host(lib):
     assert call(st=7) == -4
     assert call(pz=v((1 << 22) + 4)) == -5
     assert call(pb=v(4096)) == -6  # packed output overlaps B
+
+
+# --- decode chain: host-side validation -------------------------------------------
+
+def _chain_ops(n, deps=None, over=None):
+    """n independent ops of N=16, K=64 (bf16, bs 32) on disjoint fake device
+    addresses; `over` maps op index -> dict of field overrides."""
+    from int4_weight_only_matmulnbits_gb300.binding import ChainOpC
+    arr = (ChainOpC * n)()
+    for j in range(n):
+        base = (j + 1) << 24
+        c = arr[j]
+        c.A, c.Y = base, base + (1 << 20)
+        c.packed_b, c.packed_scales = base + (2 << 20), base + (3 << 20)
+        c.N, c.K = 16, 64
+        for k in range(4):
+            c.deps[k] = -1
+        for k, d in enumerate((deps or {}).get(j, ())):
+            c.deps[k] = d
+        for name, val in (over or {}).get(j, {}).items():
+            setattr(c, name, val)
+    return arr
+
+
+def _build(lib, arr, n=None, M=1, bs=32, a_t=1, s_t=1, plan=None, plan_bytes=0):
+    from int4_weight_only_matmulnbits_gb300.binding import ChainInfoC
+    info = ChainInfoC()
+    n = len(arr) if n is None else n
+    return lib.mnb_chain_build(arr, n, M, bs, a_t, s_t,
+                               None if plan is None else ctypes.c_void_p(plan), plan_bytes,
+                               ctypes.byref(info), None)
+
+
+NO_DEVICE = (-7, -9)  # validation passed; the call then needs a device
+
+
+def test_chain_build_rejects_invalid_arguments_on_host(lib):
+    assert lib.mnb_chain_build(None, 1, 1, 32, 1, 1, None, 0, None, None) == -1
+    assert _build(lib, _chain_ops(2), n=0) == -2
+    assert _build(lib, _chain_ops(2), M=9) == -2
+    assert _build(lib, _chain_ops(2), M=0) == -2
+    assert _build(lib, _chain_ops(2), bs=48) == -3
+    assert _build(lib, _chain_ops(2), a_t=3) == -4
+    assert _build(lib, _chain_ops(2, over={1: {"A": None}})) == -1
+    assert _build(lib, _chain_ops(2, over={1: {"packed_zp": 1 << 30}})) == -1  # mixed zp
+    assert _build(lib, _chain_ops(2, over={0: {"packed_scales_up": 1 << 30}})) == -1
+    assert _build(lib, _chain_ops(2, over={1: {"K": 0}})) == -2
+    assert _build(lib, _chain_ops(2, over={1: {"packed_b": (2 << 24) + (2 << 20) + 8}})) == -5
+    assert _build(lib, _chain_ops(2, over={0: {"A": (1 << 24) + 1}})) == -5
+    assert _build(lib, _chain_ops(2, deps={0: (0,)})) == -2   # not an earlier op
+    assert _build(lib, _chain_ops(2, deps={1: (2,)})) == -2
+    assert _build(lib, _chain_ops(2, deps={1: (-2,)})) == -2
+
+
+def test_chain_build_checks_hazards_on_host(lib):
+    y0 = (1 << 24) + (1 << 20)
+    a0 = 1 << 24
+    # op 1 reads op 0's output: needs the dependency
+    assert _build(lib, _chain_ops(2, over={1: {"A": y0}})) == -6
+    assert _build(lib, _chain_ops(2, deps={1: (0,)}, over={1: {"A": y0}})) in NO_DEVICE
+    # op 1 overwrites op 0's activations, or its output: needs the dependency
+    assert _build(lib, _chain_ops(2, over={1: {"Y": a0}})) == -6
+    assert _build(lib, _chain_ops(2, over={1: {"Y": y0}})) == -6
+    assert _build(lib, _chain_ops(2, deps={1: (0,)}, over={1: {"Y": a0}})) in NO_DEVICE
+    # a transitive dependency is enough
+    y1 = (2 << 24) + (1 << 20)
+    assert _build(lib, _chain_ops(3, deps={1: (0,), 2: (1,)},
+                                  over={2: {"A": y0}})) in NO_DEVICE
+    assert _build(lib, _chain_ops(3, deps={2: (1,)}, over={2: {"A": y0}})) == -6
+    assert _build(lib, _chain_ops(3, deps={2: (1,)}, over={2: {"A": y1}})) in NO_DEVICE
+    # an output over any weight of the chain, or over its own activations
+    assert _build(lib, _chain_ops(2, over={1: {"Y": (1 << 24) + (2 << 20)}})) == -6
+    assert _build(lib, _chain_ops(2, over={0: {"Y": a0 + 32}})) == -6
+
+
+def test_chain_run_rejects_an_altered_description(lib):
+    from int4_weight_only_matmulnbits_gb300.binding import ChainInfoC
+    info = ChainInfoC()
+    assert lib.mnb_chain_run(None, ctypes.byref(info), None) == -1
+    assert lib.mnb_chain_run(ctypes.c_void_p(1 << 20), None, None) == -1
+    info.n_ops, info.grid, info.check = 3, 304, 12345
+    assert lib.mnb_chain_run(ctypes.c_void_p(1 << 20), ctypes.byref(info), None) == -2
