@@ -392,6 +392,35 @@ MNB_API mnb_status mnb_chain_build(const mnb_chain_op *ops, int32_t n_ops,
 MNB_API mnb_status mnb_chain_run(const void *plan, const mnb_chain_info *info,
                                  mnb_stream_t stream);
 
+/*
+ * Decode chain without a caller-provided plan buffer. The paper has no
+ * counterpart for this call: it exists for callers that cannot call
+ * cudaMalloc, for example a plugin whose host runtime owns every device
+ * allocation through its own pool and forbids direct allocation, or a
+ * process whose device memory is fully reserved up front (weights, KV
+ * cache) so that no allocation may happen while it serves.
+ *
+ * Same ops, rules and errors as mnb_chain_build followed by mnb_chain_run,
+ * with the plan written into a fixed array inside the library (1 MiB on
+ * every GPU that loads the library, held until the process exits) instead
+ * of a caller buffer; the library allocates no device memory. Each call
+ * plans again (host work), copies the plan into the array and waits for
+ * that copy on `stream`, then launches; the copy also clears the
+ * completion counters the launch starts from. A chain whose plan exceeds
+ * the array is rejected with MNB_ERR_UNSUPPORTED and a message giving both
+ * sizes (the Qwen3-4B decode step needs about 0.6 MB).
+ *
+ * Every call shares the one array: calls whose work overlaps on the GPU
+ * (two streams, or two host threads) race and must be serialised by the
+ * caller. The first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.
+ */
+MNB_API mnb_status mnb_chain_run_noalloc(const mnb_chain_op *ops, int32_t n_ops,
+                                         int64_t M, int block_size,
+                                         mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                         mnb_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

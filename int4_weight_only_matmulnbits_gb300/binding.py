@@ -25,7 +25,7 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_prepacked_sizes", "mnb_prepack", "mnb_unprepack", "mnb_matmul",
            "mnb_matmul_path", "mnb_matmul_from_host",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
-           "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run")
+           "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -118,6 +118,9 @@ def load(build_if_missing: bool = False):
         lib.mnb_chain_build.restype = i32
         lib.mnb_chain_run.argtypes = [p, ctypes.POINTER(ChainInfoC), p]
         lib.mnb_chain_run.restype = i32
+        lib.mnb_chain_run_noalloc.argtypes = [ctypes.POINTER(ChainOpC), i32, i64, i32, i32,
+                                              i32, p]
+        lib.mnb_chain_run_noalloc.restype = i32
         _lib = lib
         return lib
 
@@ -418,3 +421,16 @@ def mnb_chain_run(chain: MnbChain, *, stream=None) -> None:
     """Run every op of a built chain in one cooperative launch on `stream`."""
     _check(load().mnb_chain_run(ctypes.c_void_p(chain.plan.data_ptr()), ctypes.byref(chain.info),
                                 _stream(stream)), "mnb_chain_run")
+
+
+def mnb_chain_run_noalloc(ops: list, *, stream=None) -> None:
+    """Plan and run a chain with the plan in the library's fixed device
+    array: no device memory is allocated (for callers that cannot allocate;
+    at most one such call in flight at a time)."""
+    if not ops:
+        raise ValueError("empty chain")
+    arr, M = _chain_structs(ops)
+    w0 = ops[0].weight
+    _check(load().mnb_chain_run_noalloc(arr, len(ops), M, w0.block_size,
+                                        _dtype_code(ops[0].A.dtype), _dtype_code(w0.scale_dtype),
+                                        _stream(stream)), "mnb_chain_run_noalloc")

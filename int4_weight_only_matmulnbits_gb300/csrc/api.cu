@@ -702,4 +702,30 @@ mnb_status mnb_chain_run(const void *plan, const mnb_chain_info *info, mnb_strea
   return MNB_OK;
 }
 
+mnb_status mnb_chain_run_noalloc(const mnb_chain_op *ops, int32_t n_ops, int64_t M,
+                                 int block_size, mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                 mnb_stream_t stream) {
+  // Plan (query only), check it fits the library's fixed array, plan into
+  // the array, run: the two public chain calls with library-owned storage.
+  mnb_chain_info info{};
+  mnb_status st = mnb_chain_build(ops, n_ops, M, block_size, a_dtype, scale_dtype, nullptr, 0,
+                                  &info, stream);
+  if (st != MNB_OK) return st;
+  void *scratch = nullptr;
+  size_t cap = 0;
+  const cudaError_t e = chain_scratch(&scratch, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_chain_run_noalloc (scratch address)");
+  if (info.plan_bytes > cap) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "mnb_chain_run_noalloc: this chain's plan needs %llu bytes, the library's "
+                  "fixed plan array holds %zu; pass a buffer to mnb_chain_build instead",
+                  (unsigned long long)info.plan_bytes, cap);
+    return MNB_ERR_UNSUPPORTED;
+  }
+  st = mnb_chain_build(ops, n_ops, M, block_size, a_dtype, scale_dtype, scratch, cap, &info,
+                       stream);
+  if (st != MNB_OK) return st;
+  return mnb_chain_run(scratch, &info, stream);
+}
+
 }  // extern "C"

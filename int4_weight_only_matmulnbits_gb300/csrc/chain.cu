@@ -47,6 +47,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <queue>
 #include <utility>
 #include <vector>
@@ -810,6 +811,34 @@ struct Seg {
 };
 
 }  // namespace
+
+// Plan storage owned by the library, for callers that cannot allocate
+// device memory (mnb_chain_run_noalloc). Every GPU that loads the library
+// holds this array until the process exits; every call shares it.
+constexpr size_t kChainScratchBytes = size_t(1) << 20;
+constexpr int kScratchDevices = 64;
+static __device__ __align__(256) unsigned char g_chain_scratch[kChainScratchBytes];
+
+cudaError_t chain_scratch(void **ptr, size_t *bytes) {
+  // The array's host-side name is not a device address: look the address
+  // up once per device, with that device current.
+  static std::mutex mu;
+  static void *addr[kScratchDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_chain_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = a;
+  }
+  *ptr = addr[dev];
+  *bytes = kChainScratchBytes;
+  return cudaSuccess;
+}
 
 cudaError_t chain_take_fault(unsigned int *out) {
   unsigned int zero = 0;

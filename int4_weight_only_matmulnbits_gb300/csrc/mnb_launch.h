@@ -119,6 +119,9 @@ bool chain_geom(const ChainShape &sh, int n_ops, int kmax, int grid, int per_sm,
 cudaError_t chain_launch(const void *plan, const ChainShape &sh, const ChainGeom &g,
                          cudaStream_t stream);
 cudaError_t chain_take_fault(unsigned int *out);
+// Device address and size of the library-owned plan array (looked up once
+// per device, with that device current).
+cudaError_t chain_scratch(void **ptr, size_t *bytes);
 
 int sm_count();
 
