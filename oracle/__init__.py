@@ -25,7 +25,7 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 _lock = threading.Lock()
 _lib = None
 
@@ -59,6 +59,8 @@ def load(path: str | None = None):
         lib.oracle_qdq_matmul.argtypes = [p, i32, p, p, i32, p, p, i32, i64, i64,
                                           i64, i32, p, i64, p, i64, p, p]
         lib.oracle_qdq_matmul.restype = i32
+        lib.oracle_rms_normalize.argtypes = [p, i32, p, ctypes.c_double, i64, i64, p]
+        lib.oracle_rms_normalize.restype = i32
         if path is None:
             _lib = lib
         return lib
@@ -74,6 +76,8 @@ def _as_array(x, name):
                 return x.view(torch.int16).numpy().view(np.uint16), BF16
             if x.dtype == torch.float32:
                 return x.numpy(), F32
+            if x.dtype == torch.float64:
+                return x.numpy(), F64
             if x.dtype == torch.uint8:
                 return x.numpy(), None
             raise TypeError(f"{name}: unsupported torch dtype {x.dtype}")
@@ -82,6 +86,8 @@ def _as_array(x, name):
     x = np.ascontiguousarray(x)
     if x.dtype == np.float32:
         return x, F32
+    if x.dtype == np.float64:
+        return x, F64
     if x.dtype == np.uint16:
         return x, BF16
     if x.dtype == np.uint8:
@@ -203,3 +209,43 @@ def gate_up(A, gate, up, *, N: int, K: int, block_size: int, rows=None, cols=Non
                         lib=lib)
     sig = 1.0 / (1.0 + np.exp(-g))
     return g * sig * u, g, u, mg, mu
+
+
+def rms_normalize(A, gamma=None, *, eps: float = 1e-6, lib=None):
+    """RMS-style row normalization (page "Qwen3 CPU Inference Critical Path":
+    SimplifiedLayerNormalization / RMSNormalization, FP32 over the last axis,
+    epsilon 1e-6): out[m,k] = A[m,k] / sqrt(mean_k A[m,k]^2 + eps) * gamma[k],
+    in double. Returns a float64 [M, K] array."""
+    lib = lib or load()
+    a, a_t = _as_array(A, "A")
+    if a.ndim != 2:
+        raise ValueError("A must be a 2-D [M, K] array")
+    M, K = a.shape
+    g = None
+    if gamma is not None:
+        g, gt = _as_array(gamma, "gamma")
+        if gt != F32 or g.size != K:
+            raise TypeError("gamma must be fp32 [K]")
+    out = np.zeros((M, K), dtype=np.float64)
+    rc = lib.oracle_rms_normalize(_ptr(a), a_t, _ptr(g), float(eps), M, K, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_rms_normalize rejected its arguments ({rc})")
+    return out
+
+
+def rmsnorm_matmul(A, gamma, eps, B, scales, zero_points=None, bias=None, *, N: int, K: int,
+                   block_size: int, rows=None, cols=None, lib=None):
+    """The projection of a normalized row (the page's fusion "RMSNorm into
+    packed projection input"): matmulnbits of rms_normalize(A, gamma, eps).
+    Returns (Y, absdot) with absdot = sum_k |a'[m,k] w[n,k]| over the
+    normalized activations a'."""
+    An = rms_normalize(A, gamma, eps=eps, lib=lib)
+    return matmulnbits(An, B, scales, zero_points, bias, N=N, K=K, block_size=block_size,
+                       rows=rows, cols=cols, lib=lib)
+
+
+def lm_head_argmax(Y):
+    """Greedy token choice (the page's fusion "final RMSNorm, LM-head GEMV, and
+    greedy ArgMax"): the index of the largest logit of each row, the first
+    one on ties (numpy's argmax)."""
+    return np.argmax(np.asarray(Y), axis=1)

@@ -44,6 +44,7 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F64 2 /* activations only: an exact double input (e.g. a normalized row) */
 
 /* Exact widening of one stored element to double. A bf16 value is the upper
  * half of the fp32 with the same bit pattern, so shifting the 16 stored bits
@@ -51,6 +52,9 @@
 static double widen(const void *base, int64_t i, int dtype) {
   if (dtype == ORACLE_F32) {
     return (double)((const float *)base)[i];
+  }
+  if (dtype == ORACLE_F64) {
+    return ((const double *)base)[i];
   }
   uint32_t bits = ((uint32_t)((const uint16_t *)base)[i]) << 16;
   float f;
@@ -93,7 +97,7 @@ static int check_args(int64_t M, int64_t N, int64_t K, int bs, int a_dtype,
                       int scale_dtype) {
   if (M < 0 || N < 0 || K < 0) return -2;
   if (bs < 2 || (bs % 2) != 0) return -3;
-  if ((a_dtype != ORACLE_F32 && a_dtype != ORACLE_BF16) ||
+  if ((a_dtype != ORACLE_F32 && a_dtype != ORACLE_BF16 && a_dtype != ORACLE_F64) ||
       (scale_dtype != ORACLE_F32 && scale_dtype != ORACLE_BF16))
     return -4;
   return 0;
@@ -207,6 +211,37 @@ int oracle_qdq_matmul(const void *A, int a_dtype, const uint8_t *Bq,
       if (bias != NULL) acc += (double)bias[n];
       Y[i * n_cols + j] = acc;
       if (absdot) absdot[i * n_cols + j] = mag;
+    }
+  }
+  return 0;
+}
+
+/*
+ * RMS-style normalization of each activation row (page "Qwen3 CPU Inference
+ * Critical Path": ai.onnx::SimplifiedLayerNormalization in the exact kernel
+ * inventory, FP32 RMS-style normalization over the last axis with
+ * epsilon 1e-6, and RMSNormalization v23 among the P1 operators; the fusion
+ * list puts it into the packed projection input):
+ *
+ *   r[m]      = 1 / sqrt( (sum_k A[m,k]^2) / K + eps )
+ *   out[m,k]  = A[m,k] * r[m] * gamma[k]        (gamma NULL: 1)
+ *
+ * in double, the sum in increasing k. out is [M, K] row-major double.
+ */
+int oracle_rms_normalize(const void *A, int a_dtype, const float *gamma, double eps,
+                         int64_t M, int64_t K, double *out) {
+  if (M < 0 || K < 1 || eps < 0.0) return -2;
+  if (a_dtype != ORACLE_F32 && a_dtype != ORACLE_BF16 && a_dtype != ORACLE_F64) return -4;
+  for (int64_t m = 0; m < M; ++m) {
+    double sumsq = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      double x = widen(A, m * K + k, a_dtype);
+      sumsq += x * x;
+    }
+    double r = 1.0 / sqrt(sumsq / (double)K + eps);
+    for (int64_t k = 0; k < K; ++k) {
+      double g = gamma ? (double)gamma[k] : 1.0;
+      out[m * K + k] = widen(A, m * K + k, a_dtype) * r * g;
     }
   }
   return 0;
