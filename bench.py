@@ -43,9 +43,9 @@ WORKLOAD = "Qwen3-4B decode step projections, M=1, bf16 A, bs 128, no zp"
 # capture of the 145 launches (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the decode-kernel sources it was measured on.
 STEP_TRAFFIC = {
-    "bytes_per_launch": 14388845,
+    "bytes_per_launch": 14399996,
     "sources": ("gemv.cu", "mnb_common.cuh", "mnb_launch.h"),
-    "sha256": "d1447e0593df2c9d9744c62f580a6c7ebfc500fd922be20ac1db542a562fa435",
+    "sha256": "137849bab058a0576993eb584b2e164b917bc748e2e844ae255f055da61b5386",
 }
 
 
@@ -291,6 +291,29 @@ def time_region(fn, steps, stream):
     return start.elapsed_time(end) / 1e3
 
 
+def lm_head_fusions(mnb, lm_launch, dev, steps=50):
+    """The step's lm_head launch alone and with the fused final RMSNorm and
+    greedy ArgMax (mnb_matmul_rmsnorm), us per call on the same stream;
+    the weight (200 MB) exceeds L2, so every call streams it from HBM."""
+    import torch
+    _, ws, A, Ys = lm_launch
+    w, Y = ws[0], Ys[0]
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321)
+    gamma = torch.rand(w.K, device=dev, generator=g) + 0.5
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, fn in (("lm_head", lambda: mnb.mnb_matmul(A, w, None, out=Y)),
+                     ("rmsnorm_lm_head", lambda: mnb.mnb_matmul_rmsnorm(A, w, gamma=gamma, out=Y)),
+                     ("rmsnorm_lm_head_argmax",
+                      lambda: mnb.mnb_matmul_rmsnorm(A, w, gamma=gamma, logits=False,
+                                                     argmax=True))):
+        for _ in range(3):
+            fn()
+        out[name + "_us"] = time_region(fn, steps, stream) * 1e6 / steps
+    return out
+
+
 def prefill_measure(dev, steps=5, warmup=3):
     """TFLOP/s of the tensor-core path at M=2048 over the seven Qwen3-4B
     projection shapes (bf16 A, bs 128, zero points, bias), each timed alone;
@@ -411,6 +434,7 @@ def run_gpu(args, rank, world, dist):
     per_gpu = algo_bytes * args.steps / t / 1e9
 
     prefill = None if args.skip_prefill else prefill_measure(dev)
+    fusions = lm_head_fusions(mnb, launches[-1], dev)
     cpu = None
     if world == 1 and not args.skip_cpu:
         nbytes, secs, desc = oracle_sample(args.cpu_budget)
@@ -446,6 +470,7 @@ def run_gpu(args, rank, world, dist):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "prefill": prefill,
+        "lm_head_fusions": fusions,
         "decode_chain": {"value": algo_bytes * args.steps / t_chain / 1e9, "unit": "GB/s",
                          "ms_per_step": 1e3 * t_chain / args.steps, "launches_per_step": 1,
                          "note": "the same step and dependencies as one persistent "

@@ -298,6 +298,40 @@ MNB_API void mnb_set_programmatic_launch(int enable);
 MNB_API mnb_status mnb_fault_status(unsigned int *fault_bits);
 
 /*
+ * Projection of an RMS-normalized row, optionally followed by greedy ArgMax
+ * (page "Qwen3 CPU Inference Critical Path": the fusions "RMSNorm into packed
+ * projection input" and "final RMSNorm, LM-head GEMV, and greedy ArgMax";
+ * the normalization is the inventory's SimplifiedLayerNormalization, FP32
+ * RMS-style normalization over the last axis, epsilon 1e-6 in the audited
+ * graph):
+ *
+ *   a'[m,k] = A[m,k] / sqrt(mean_k A[m,k]^2 + epsilon) * gamma[k]   (normalize = 1)
+ *   a'      = A                                                     (normalize = 0)
+ *   Y[m,n]  = sum_k a'[m,k] * dequant(B)[n,k] + bias[n]
+ *   argmax[m] = the smallest n with the largest Y[m,n]
+ *
+ * in one decode-kernel launch (plus a one-thread-per-row finishing kernel
+ * for the ArgMax). gamma: fp32 [K] DEVICE or NULL (1); the sum of squares
+ * and the scale are fp32; a normalized bf16 row is rounded to bf16 once
+ * before the products (as the unfused graph rounds the normalization's
+ * output). Y [M, N] in A's dtype, or NULL when only argmax is wanted (the
+ * logits are then never written). argmax: int64 [M] DEVICE or NULL; the
+ * comparison uses the fp32 value of each output before it is rounded to
+ * A's dtype. M <= 16 (the decode path). Other arguments as mnb_matmul.
+ * Errors: as mnb_matmul; MNB_ERR_NULL if Y and argmax are both NULL;
+ * MNB_ERR_SHAPE for normalize not 0/1 or a negative or non-finite epsilon;
+ * MNB_ERR_ALIGN for gamma (4 bytes) or argmax (8 bytes); MNB_ERR_ALIAS if Y
+ * or argmax overlaps an input or each other; MNB_ERR_UNSUPPORTED for M > 16.
+ */
+MNB_API mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
+                                      float epsilon, const void *packed_b,
+                                      const void *scales, const void *zero_points,
+                                      const float *bias, int64_t M, int64_t N, int64_t K,
+                                      int block_size, void *Y, int64_t *argmax,
+                                      mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                      mnb_stream_t stream);
+
+/*
  * Decode chain: a sequence of MatMulNBits projections with declared data
  * dependencies, run as ONE persistent cooperative kernel launch.
  *

@@ -25,7 +25,8 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_prepacked_sizes", "mnb_prepack", "mnb_unprepack", "mnb_matmul",
            "mnb_matmul_path", "mnb_matmul_from_host",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
-           "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc")
+           "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc",
+           "mnb_matmul_rmsnorm")
 
 _lock = threading.Lock()
 _lib = None
@@ -121,6 +122,9 @@ def load(build_if_missing: bool = False):
         lib.mnb_chain_run_noalloc.argtypes = [ctypes.POINTER(ChainOpC), i32, i64, i32, i32,
                                               i32, p]
         lib.mnb_chain_run_noalloc.restype = i32
+        lib.mnb_matmul_rmsnorm.argtypes = [p, i32, p, ctypes.c_float, p, p, p, p, i64, i64,
+                                           i64, i32, p, p, i32, i32, p]
+        lib.mnb_matmul_rmsnorm.restype = i32
         _lib = lib
         return lib
 
@@ -434,3 +438,30 @@ def mnb_chain_run_noalloc(ops: list, *, stream=None) -> None:
     _check(load().mnb_chain_run_noalloc(arr, len(ops), M, w0.block_size,
                                         _dtype_code(ops[0].A.dtype), _dtype_code(w0.scale_dtype),
                                         _stream(stream)), "mnb_chain_run_noalloc")
+
+
+def mnb_matmul_rmsnorm(A: torch.Tensor, w: PackedWeight, bias: torch.Tensor | None = None, *,
+                       gamma: torch.Tensor | None = None, eps: float = 1e-6,
+                       normalize: bool = True, logits: bool = True, argmax: bool = False,
+                       out: torch.Tensor | None = None, stream=None):
+    """Y = rmsnorm(A; gamma, eps) @ dequant(w)^T + bias (normalize=False: plain
+    A), and optionally the greedy ArgMax of each row, in one decode launch
+    (M <= 16). Returns (Y or None, argmax int64 [M] or None)."""
+    if A.dim() != 2 or A.shape[1] != w.K or not A.is_cuda or not A.is_contiguous():
+        raise ValueError(f"A must be a contiguous CUDA [M, {w.K}] tensor")
+    for name, t in (("bias", bias), ("gamma", gamma)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_cuda):
+            raise ValueError(f"{name} must be an fp32 CUDA tensor")
+    if not logits and not argmax:
+        raise ValueError("ask for the logits, the argmax or both")
+    M = A.shape[0]
+    Y = None
+    if logits:
+        Y = out if out is not None else torch.empty(M, w.N, dtype=A.dtype, device=A.device)
+    idx = torch.empty(M, dtype=torch.int64, device=A.device) if argmax else None
+    _check(load().mnb_matmul_rmsnorm(
+        _ptr(A), 1 if normalize else 0, _ptr(gamma), float(eps), _ptr(w.packed_b),
+        _ptr(w.packed_scales), _ptr(w.packed_zp), _ptr(bias), M, w.N, w.K, w.block_size,
+        _ptr(Y), _ptr(idx), _dtype_code(A.dtype), _dtype_code(w.scale_dtype), _stream(stream)),
+        "mnb_matmul_rmsnorm")
+    return Y, idx

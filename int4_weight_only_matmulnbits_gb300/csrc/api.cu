@@ -559,6 +559,80 @@ mnb_status mnb_matmul_from_host(const void *A_host, void *A_dev,
   return MNB_OK;
 }
 
+mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
+                              float epsilon, const void *packed_b, const void *scales,
+                              const void *zero_points, const float *bias, int64_t M, int64_t N,
+                              int64_t K, int block_size, void *Y, int64_t *argmax,
+                              mnb_dtype a_dtype, mnb_dtype scale_dtype, mnb_stream_t stream) {
+  if (!A || !packed_b || !scales || (!Y && !argmax)) return MNB_ERR_NULL;
+  if (normalize != 0 && normalize != 1) return MNB_ERR_SHAPE;
+  if (M < 1 || M > kMaxDim) return MNB_ERR_SHAPE;
+  mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  if (!valid_dtype(a_dtype)) return MNB_ERR_DTYPE;
+  if (normalize && !(epsilon >= 0.f && epsilon <= 3.0e38f)) return MNB_ERR_SHAPE;
+  const size_t es = dtype_size(a_dtype);
+  if (!aligned(A, es) || (Y && !aligned(Y, es)) || !aligned(packed_b, 16) ||
+      !aligned(scales, 16) || (zero_points && !aligned(zero_points, 16)) ||
+      (bias && !aligned(bias, 4)) || (gamma && !aligned(gamma, 4)) ||
+      (argmax && !aligned(argmax, 8)))
+    return MNB_ERR_ALIGN;
+  if (M > kGemvMaxM) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "mnb_matmul_rmsnorm serves the decode path, M <= %d (M=%lld)", kGemvMaxM,
+                  (long long)M);
+    return MNB_ERR_UNSUPPORTED;
+  }
+  const Sizes in = packed_sizes(N, K, block_size, scale_dtype, zero_points != nullptr);
+  const void *ins[6] = {A, packed_b, scales, zero_points, bias, normalize ? gamma : nullptr};
+  const size_t in_n[6] = {size_t(M) * K * es, in.b, in.s, in.z, bias ? size_t(N) * 4 : 0,
+                          (normalize && gamma) ? size_t(K) * 4 : 0};
+  const size_t y_bytes = Y ? size_t(M) * N * es : 0, k_bytes = argmax ? size_t(M) * 8 : 0;
+  for (int j = 0; j < 6; ++j)
+    if (overlap(Y, y_bytes, ins[j], in_n[j]) || overlap(argmax, k_bytes, ins[j], in_n[j]))
+      return MNB_ERR_ALIAS;
+  if (overlap(Y, y_bytes, argmax, k_bytes)) return MNB_ERR_ALIAS;
+  st = check_device();
+  if (st != MNB_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (argmax)
+    e = launch_argmax_init(reinterpret_cast<unsigned long long *>(argmax), static_cast<int>(M),
+                           s);
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_rmsnorm (ArgMax keys)");
+  GroupArgs g{};
+  g.A = A;
+  g.count = 1;
+  g.packed_b[0] = packed_b;
+  g.scales[0] = scales;
+  g.zp[0] = zero_points;
+  g.bias[0] = bias;
+  g.Y[0] = Y;
+  g.N[0] = N;
+  g.M = M;
+  g.K = K;
+  g.bs = block_size;
+  g.a_f32 = a_dtype == MNB_F32;
+  g.scale_f32 = scale_dtype == MNB_F32;
+  g.has_zp = zero_points != nullptr;
+  g.pdl = g_pdl.load() != 0;
+  g.norm = normalize != 0;
+  g.gamma = normalize ? gamma : nullptr;
+  g.eps = epsilon;
+  g.amax = reinterpret_cast<unsigned long long *>(argmax);
+  e = launch_gemv_group(g, s);
+  if (e == cudaErrorNotSupported) {
+    std::snprintf(g_last_error, sizeof g_last_error, "no kernel for M=%lld N=%lld K=%lld bs=%d",
+                  (long long)M, (long long)N, (long long)K, block_size);
+    return MNB_ERR_UNSUPPORTED;
+  }
+  if (e == cudaSuccess && argmax)
+    e = launch_argmax_finalize(reinterpret_cast<unsigned long long *>(argmax),
+                               static_cast<int>(M), g.pdl, s);
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_rmsnorm");
+  return MNB_OK;
+}
+
 mnb_status mnb_chain_build(const mnb_chain_op *ops, int32_t n_ops, int64_t M,
                            int block_size, mnb_dtype a_dtype, mnb_dtype scale_dtype,
                            void *plan, size_t plan_bytes, mnb_chain_info *info,

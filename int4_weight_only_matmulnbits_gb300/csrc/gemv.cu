@@ -86,10 +86,30 @@ struct GemvParams {
   int cpw, scs;              // chunks per warp and stage; chunks per stage and tile (ksw*cpw)
   int krp, sg;               // staged activation row stride, block sums per row
   int nst, stage_bytes, stage_tx;  // ring depth, stage stride, bytes per stage
+  // RMS-normalized activations (the fusion "RMSNorm into packed projection
+  // input"): the staged row is A * gamma and every output is scaled by
+  // r[m] = 1 / sqrt(mean_k A[m,k]^2 + eps). norm = 0: plain A.
+  int norm;
+  const float *gamma;  // [K] or null (1)
+  float eps;
+  // Greedy ArgMax over the outputs of weight 0 (the fusion "final RMSNorm,
+  // LM-head GEMV, and greedy ArgMax"): keys [M], or null. Y[0] may then be
+  // null (logits not stored).
+  unsigned long long *amax;
   int st_sc, st_zp;  // offsets of scales and zero points in a stage (128-aligned)
   int nbs, nps;      // blocks and zero-point word pairs per stage and tile
   int off_alo, off_s, off_red, off_part, off_bar, off_ring;
+  int off_nrm;  // r[m] and the ArgMax keys (norm or amax)
 };
+
+// ArgMax key of output (v, n): larger keys for larger v (an order-preserving
+// map of the fp32 bits) and, among equal v, for smaller n.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) |
+         static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(n));
+}
 
 template <int BS>
 struct BlockGeom {
@@ -137,10 +157,21 @@ __device__ __forceinline__ void load8(const GemvParams &p, int m, int64_t k,
   }
 }
 
-// Y[m][n] = v + bias[n], in A's dtype (bf16 rounded to nearest even).
-__device__ __forceinline__ void store_y(const GemvParams &p, int q, int m, int n,
-                                        float v) {
+// Y[m][n] = r[m] v + bias[n], in A's dtype (bf16 rounded to nearest even);
+// with the ArgMax epilogue the fp32 value also competes for the row's key
+// (sNrm: r[m] in the first 16 floats, then the rows' best keys as 64-bit
+// words).
+__device__ __forceinline__ void store_y(const GemvParams &p, int q, int m, int n, float v,
+                                        float *sNrm) {
+  if (p.norm) v *= sNrm[m];
   if (p.bias[q]) v += __ldg(p.bias[q] + n);
+  if (p.amax && q == 0) {
+    // Only a value above the CTA's current best pays for the atomic.
+    unsigned long long *best = reinterpret_cast<unsigned long long *>(sNrm + kGemvMaxM) + m;
+    const unsigned long long key = argmax_key(v, n);
+    if (key > *reinterpret_cast<volatile unsigned long long *>(best)) atomicMax(best, key);
+  }
+  if (!p.Y[q]) return;
   if (p.a_f32)
     static_cast<float *>(p.Y[q])[(int64_t)m * p.N[q] + n] = v;
   else
@@ -151,7 +182,11 @@ __device__ __forceinline__ void store_y(const GemvParams &p, int q, int m, int n
 // Gated-MLP output: with g = gate + bias_g and u = up + bias_u,
 // Y[m][n] = g * sigmoid(g) * u, in fp32, stored in A's dtype.
 __device__ __forceinline__ void store_gate_up(const GemvParams &p, int m, int n, float g,
-                                              float u) {
+                                              float u, const float *sNrm) {
+  if (p.norm) {
+    g *= sNrm[m];
+    u *= sNrm[m];
+  }
   if (p.bias[0]) g += __ldg(p.bias[0] + n);
   if (p.bias[1]) u += __ldg(p.bias[1] + n);
   const float v = g / (1.f + expf(-g)) * u;
@@ -173,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   float *sS = reinterpret_cast<float *>(smem + p.off_s);
   float *sRed = reinterpret_cast<float *>(smem + p.off_red);
   float *sPart = reinterpret_cast<float *>(smem + p.off_part);
+  float *sNrm = reinterpret_cast<float *>(smem + p.off_nrm);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
   uint64_t *empty = full + kMaxStages;
   uint64_t *abar = empty + kMaxStages;  // activation copy
@@ -298,6 +334,32 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     const int npieces = p.M * ppr;
     constexpr int gp = BS / 8;  // pieces per block, consecutive lanes
     bool fault = false;
+    if (p.amax && tid < kGemvMaxM)
+      reinterpret_cast<unsigned long long *>(sNrm + kGemvMaxM)[tid] = 0ull;
+    if (p.norm) {
+      // r[m] from the whole row (this CTA may stage only part of K): per-warp
+      // partial sums of squares, then a fixed-order sum over the warps.
+      const int pr = (p.K + 7) / 8;
+      for (int m = 0; m < p.M; ++m) {
+        float ss = 0.f;
+#pragma unroll 2
+        for (int pc = tid; pc < pr; pc += kConsumers) {
+          float v[8];
+          load8(p, m, int64_t(pc) * 8, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) sRed[warp * kGemvMaxM + m] = ss;
+      }
+      named_barrier_sync(kBarConsumers, kConsumers);
+      if (tid < p.M) {
+        float ss = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) ss += sRed[w * kGemvMaxM + tid];
+        sNrm[tid] = 1.f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
+      }
+    }
     if (p.a_bulk) {
       // bf16 rows: the producer copies the part inside K with one bulk copy
       // per row; zeros past K.
@@ -338,7 +400,13 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           const int pc2 = base + q * kConsumers + tid;
           if (pc2 < npieces) {
             const int m = pc2 / ppr;
-            load8(p, m, (int64_t)clo * kChunkK + (pc2 - m * ppr) * 8, v[q]);
+            const int64_t k = (int64_t)clo * kChunkK + (pc2 - m * ppr) * 8;
+            load8(p, m, k, v[q]);
+            if (p.norm && p.gamma) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                v[q][e] *= (k + e < p.K) ? __ldg(p.gamma + k + e) : 0.f;
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[q][e] = 0.f;
@@ -360,7 +428,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             const float f0 = bf16_bits_to_f32(h0), f1 = bf16_bits_to_f32(h1);
             const uint32_t l0 = bf16_bits(v[q][2 * e] - f0), l1 = bf16_bits(v[q][2 * e + 1] - f1);
             lo[e] = l0 | (l1 << 16);
-            part += (f0 + bf16_bits_to_f32(l0)) + (f1 + bf16_bits_to_f32(l1));
+            // The block sums cover exactly what the MMAs see: hi + lo for fp32
+            // activations, hi alone otherwise (a normalized bf16 row is
+            // rounded to bf16 here).
+            part += p.a_f32 ? (f0 + bf16_bits_to_f32(l0)) + (f1 + bf16_bits_to_f32(l1))
+                            : f0 + f1;
           }
           if (ok) {
             const int off = m * p.krp + kp * 8;
@@ -541,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           for (int e = 0; e < 4; ++e) {
             const int m = mt * 8 + 2 * t + (e & 1);
             const int nn = n0 + 8 * (e >> 1);
-            if (m < p.M && nn < p.N[q]) store_y(p, q, m, nn, acc[mt][e]);
+            if (m < p.M && nn < p.N[q]) store_y(p, q, m, nn, acc[mt][e], sNrm);
           }
         continue;
       }
@@ -573,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             vu += sRed[(((tt + ht) * p.ksw + k2) * kTileN + row) * MC + m];
           }
           if (p.cluster == 1) {
-            if (n_base + r < p.N[0]) store_gate_up(p, m, n_base + r, vg, vu);
+            if (n_base + r < p.N[0]) store_gate_up(p, m, n_base + r, vg, vu, sNrm);
           } else {
             sPart[e] = vg;
             sPart[total + e] = vu;
@@ -588,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
               vu += ld_dsmem_f32(sPart + total + e, r);
             }
             const int m = e / half, r = e - m * half;
-            if (n_base + r < p.N[0]) store_gate_up(p, m, n_base + r, vg, vu);
+            if (n_base + r < p.N[0]) store_gate_up(p, m, n_base + r, vg, vu, sNrm);
           }
           cluster_sync_all();
         } else {
@@ -605,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         for (int k2 = 0; k2 < p.ksw; ++k2)
           v += sRed[((tt * p.ksw + k2) * kTileN + row) * MC + m];
         if (p.cluster == 1) {
-          if (n_base + r < p.N[q]) store_y(p, q, m, n_base + r, v);
+          if (n_base + r < p.N[q]) store_y(p, q, m, n_base + r, v, sNrm);
         } else {
           sPart[e] = v;
         }
@@ -618,13 +690,42 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           float v = 0.f;
           for (int r = 0; r < p.cluster; ++r) v += ld_dsmem_f32(sPart + e, r);
           const int m = e / rows, r = e - m * rows;
-          if (n_base + r < p.N[q]) store_y(p, q, m, n_base + r, v);
+          if (n_base + r < p.N[q]) store_y(p, q, m, n_base + r, v, sNrm);
         }
         cluster_sync_all();
       } else {
         named_barrier_sync(kBarConsumers, kConsumers);
       }
     }
+    if (p.amax) {
+      // This CTA's best key of each row joins the grid-wide maximum.
+      named_barrier_sync(kBarConsumers, kConsumers);
+      if (tid < p.M) {
+        const unsigned long long key =
+            reinterpret_cast<const unsigned long long *>(sNrm + kGemvMaxM)[tid];
+        if (key) atomicMax(p.amax + tid, key);
+      }
+    }
+  }
+}
+
+// Clears the ArgMax keys. The decode kernel launched after it (programmatic
+// dependent launch) starts streaming weights at once and reaches its first
+// atomic only after its dependency wait, i.e. after this kernel.
+__global__ void argmax_init_kernel(unsigned long long *amax, int M) {
+  grid_dependents_launch();
+  if (static_cast<int>(threadIdx.x) < M) amax[threadIdx.x] = 0ull;
+}
+
+// Turns the ArgMax keys into indices in place (one thread per row); launched
+// as a programmatic dependent of the decode kernel, it is resident before
+// that kernel ends and waits for its results.
+__global__ void argmax_finalize_kernel(unsigned long long *amax, int M) {
+  grid_dependency_wait();
+  const int m = threadIdx.x;
+  if (m < M) {
+    const unsigned long long key = amax[m];
+    amax[m] = static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(key));
   }
 }
 
@@ -692,6 +793,8 @@ bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   off += align16(size_t(kConsumerWarps) * kTileN * MT * 8 * 4);
   L.off_part = static_cast<int>(off);
   if (cluster > 1) off += align16(size_t(tpc) * kTileN * a.M * 4);
+  L.off_nrm = static_cast<int>(off);
+  off += align16(kGemvMaxM * 4 + kGemvMaxM * 8);  // r[m], then the ArgMax keys
   L.off_bar = static_cast<int>(off);
   off += (2 * kMaxStages + 1) * 8;
   off = align128(off);
@@ -879,7 +982,12 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   p.a_f32 = a.a_f32;
   const int vec_elems = a.a_f32 ? 4 : 8;
   p.a_vec = (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) && (a.K % vec_elems == 0);
-  p.a_bulk = !a.a_f32 && p.a_vec;
+  p.norm = a.norm ? 1 : 0;
+  p.gamma = a.gamma;
+  p.eps = a.eps;
+  p.amax = a.amax;
+  // A normalized row is scaled by gamma while it is staged: not a raw copy.
+  p.a_bulk = !a.a_f32 && p.a_vec && !a.norm;
   p.ksw = best.ksw;
   p.tpc = best.tpc;
   p.cluster = best.cluster;
@@ -896,6 +1004,25 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
 
   return MT == 2 ? launch_bs<2>(p, best, grid, a.bs, a.has_zp, a.scale_f32, a.pdl, stream)
                  : launch_bs<1>(p, best, grid, a.bs, a.has_zp, a.scale_f32, a.pdl, stream);
+}
+
+cudaError_t launch_argmax_init(unsigned long long *amax, int M, cudaStream_t stream) {
+  argmax_init_kernel<<<1, 32, 0, stream>>>(amax, M);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_argmax_finalize(unsigned long long *amax, int M, bool pdl,
+                                   cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, argmax_finalize_kernel, amax, M);
 }
 
 cudaError_t launch_gemv(const MatmulArgs &a, cudaStream_t stream) {

@@ -68,7 +68,18 @@ struct GroupArgs {
   // Gated-MLP pair: weight 0 = gate, weight 1 = up (same N), one output
   // Y[0] = silu(gate) * up; bias[0] / bias[1] apply before the product.
   bool paired = false;
+  // RMS-normalized activations: A * gamma staged, outputs scaled by
+  // 1 / sqrt(mean(A^2) + eps) (gamma null: 1).
+  bool norm = false;
+  const float *gamma = nullptr;
+  float eps = 0.f;
+  // Greedy ArgMax keys [M] over weight 0's outputs (zeroed by the caller;
+  // launch_argmax_finalize turns them into indices). Y[0] may be null.
+  unsigned long long *amax = nullptr;
 };
+cudaError_t launch_argmax_init(unsigned long long *amax, int M, cudaStream_t stream);
+cudaError_t launch_argmax_finalize(unsigned long long *amax, int M, bool pdl,
+                                   cudaStream_t stream);
 
 // Small-M split-K kernel (M <= kGemvMaxM). Returns cudaErrorNotSupported when
 // no launch configuration fits this shape.

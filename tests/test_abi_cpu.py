@@ -221,3 +221,32 @@ def test_chain_run_rejects_an_altered_description(lib):
     assert lib.mnb_chain_run(ctypes.c_void_p(1 << 20), None, None) == -1
     info.n_ops, info.grid, info.check = 3, 304, 12345
     assert lib.mnb_chain_run(ctypes.c_void_p(1 << 20), ctypes.byref(info), None) == -2
+
+
+def test_matmul_rmsnorm_rejects_invalid_arguments_on_host(lib):
+    v = ctypes.c_void_p
+    ok = dict(A=v(1 << 16), nrm=1, gamma=v(1 << 17), eps=1e-6, pb=v(1 << 20), ps=v(1 << 21),
+              pz=None, bias=None, M=1, N=16, K=64, bs=32, Y=v(1 << 22), am=v(1 << 23),
+              a_t=1, s_t=1)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.mnb_matmul_rmsnorm(a["A"], a["nrm"], a["gamma"], a["eps"], a["pb"], a["ps"],
+                                      a["pz"], a["bias"], a["M"], a["N"], a["K"], a["bs"],
+                                      a["Y"], a["am"], a["a_t"], a["s_t"], None)
+    assert call(A=None) == -1
+    assert call(Y=None, am=None) == -1
+    assert call(nrm=2) == -2
+    assert call(eps=-1.0) == -2
+    assert call(eps=float("inf")) == -2
+    assert call(M=0) == -2
+    assert call(bs=40) == -3
+    assert call(a_t=5) == -4
+    assert call(gamma=v((1 << 17) + 2)) == -5
+    assert call(am=v((1 << 23) + 4)) == -5
+    assert call(M=17) == -8
+    assert call(Y=v(1 << 16)) == -6            # Y over A
+    assert call(am=v((1 << 22) + 8)) == -6     # argmax over Y
+    assert call(gamma=v(1 << 22)) == -6        # Y over gamma
+    assert call(nrm=0, gamma=v(1 << 22)) in (-7, -9)  # gamma unused without normalize
