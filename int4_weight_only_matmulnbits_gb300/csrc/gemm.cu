@@ -586,6 +586,360 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   }
 }
 
+// ---- fp32 activations: tf32 tensor-core products ---------------------------
+//
+// The same pipeline for fp32 activations, one 128 x 128 output tile per CTA:
+// TMA stages the fp32 A tile as is (two 32-wide, 128-byte-swizzled boxes per
+// 64-wide k stage), the dequantisation warps write (q - z) * s as fp32
+// rounded to tf32 (nearest, ties away) into two K-major swizzled halves of
+// the B tile, and tcgen05.mma kind::tf32 (K = 8 per instruction) multiplies
+// them into the TMEM accumulator. The tensor core reads A with a tf32
+// significand, so a product carries at most 2^-10 + 2^-11 relative error;
+// with fp32 accumulation the stated bound 2e-3 * sum|a w| + 1e-5 holds. One
+// CTA per SM (the fp32 tiles need about 180 KB of shared memory).
+struct SmemT {
+  static constexpr int kStages = 3;
+  static constexpr int kATile = kBH * kBK * 4;  // 32 KB: two 16 KB halves
+  static constexpr int kBTile = kBN * kBK * 4;  // 32 KB: two 16 KB halves
+  static constexpr int kHalf = 16 * 1024;
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + kStages * kATile;
+  static constexpr int kCodes = kB + kBStages * kBTile;
+  static constexpr int kSc = kCodes + kStages * kCodeBytes;
+  static constexpr int kScBytes = 2048;
+  static constexpr int kZp = kSc + kStages * kScBytes;
+  static constexpr int kZpBytes = 256;
+  static constexpr int kBias = kZp + kStages * kZpBytes;
+  static constexpr int kBar = kBias + kBN * 4;
+  static constexpr int kTmemSlot = kBar + (2 * kStages + 2 * kBStages + 1) * 8;
+  static constexpr int kTotal = kTmemSlot + 16;
+};
+static_assert(SmemT::kTotal + 1024 <= 227 * 1024, "one CTA per SM");
+
+// D fp32, A and B tf32, both K-major, M = 128, N = kBN.
+constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) |
+                                (static_cast<uint32_t>(kBN >> 3) << 17) |
+                                (static_cast<uint32_t>(kBH >> 4) << 24);
+
+__device__ __forceinline__ void umma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdescTf32), "r"(static_cast<int>(accumulate))
+      : "memory");
+}
+
+// fp32 -> tf32, round to nearest (ties away from zero), as fp32 bits.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+template <int BS, bool HAS_ZP, bool SF32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tf32_kernel(const __grid_constant__ GemmParams p) {
+  using S = SmemT;
+  constexpr int kStages = S::kStages;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBar);
+  uint64_t *empty = full + kStages;
+  uint64_t *bfull = empty + kStages;
+  uint64_t *bempty = bfull + kBStages;
+  uint64_t *acc_full = bempty + kBStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kTmemSlot);
+  float *sBias = reinterpret_cast<float *>(smem + S::kBias);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.y * kBH;
+  const int nt0 = blockIdx.x * kTilesN;
+  constexpr int kBpc = BS < kBK ? kBK / BS : 1;
+  // This CTA's k stages (its rank in the K-splitting cluster is blockIdx.z).
+  const int kb0 = blockIdx.z * p.kps;
+  const int nk = min(p.K64 - kb0, p.kps);
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(bfull + i, kDqWarps);
+      mbar_init(bempty + i, 1);
+    }
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kBN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  grid_dependents_launch();
+  grid_dependency_wait();
+
+  bool fault = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kStages;
+        if (i >= kStages && !mbar_wait(empty + s, ((i / kStages) - 1) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          break;
+        }
+        uint64_t *bar = full + s;
+        mbar_arrive_expect_tx(bar, S::kATile + kCodeBytes + p.sc_bytes + p.zp_bytes);
+        const int kb = kb0 + i;
+        const int blk = (kb * kBK) / BS;
+        unsigned char *ad = smem + S::kA + s * S::kATile;
+        tma_load_2d(ad, &p.tma, kb * kBK, m0, bar);
+        tma_load_2d(ad + S::kHalf, &p.tma, kb * kBK + kBK / 2, m0, bar);
+        tma_load_3d(smem + S::kCodes + s * kCodeBytes, &p.tmw, 0, kb, nt0, bar);
+        tma_load_3d(smem + S::kSc + s * S::kScBytes, &p.tms, 0, blk, nt0, bar);
+        if (HAS_ZP) tma_load_3d(smem + S::kZp + s * S::kZpBytes, &p.tmz, 0, blk >> 1, nt0, bar);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kStages, b = i % kBStages;
+        if (!mbar_wait(full + s, (i / kStages) & 1) ||
+            !mbar_wait(bfull + b, (i / kBStages) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          fault = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_addr(smem + S::kA + s * S::kATile);
+        const uint32_t b_base = smem_addr(smem + S::kB + b * S::kBTile);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 8; ++kk) {
+          const uint32_t off = (kk >> 2) * S::kHalf + (kk & 3) * 32;
+          umma_tf32(tmem, smem_desc_sw128(a_base + off), smem_desc_sw128(b_base + off),
+                    i > 0 || kk > 0);
+        }
+        umma_commit(empty + s);
+        umma_commit(bempty + b);
+      }
+      if (!fault) umma_commit(acc_full);
+    }
+  } else {
+    const int tile = warp - 2;
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = tile * kTileN + 2 * g;  // B rows 2g, 2g + 1 of weight rows g, g + 8
+    {
+      const int e = tid - 64;
+      if (e < kBN) {
+        const int n = nt0 * kTileN + e;
+        sBias[e] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
+      }
+    }
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kStages, bslot = i % kBStages;
+      if (!mbar_wait(full + s, (i / kStages) & 1) ||
+          (i >= kBStages && !mbar_wait(bempty + bslot, ((i / kBStages) - 1) & 1))) {
+        record_fault(&g_fault_gemm, kFaultGemmWait);
+        fault = true;
+        break;
+      }
+      const unsigned char *codes = smem + S::kCodes + s * kCodeBytes;
+      const unsigned char *sc = smem + S::kSc + s * S::kScBytes;
+      const uint2 *zp = reinterpret_cast<const uint2 *>(smem + S::kZp + s * S::kZpBytes);
+      unsigned char *btile = smem + S::kB + bslot * S::kBTile;
+      const int blk0 = ((kb0 + i) * kBK) / BS;
+      float s0[kBpc], s1[kBpc], z0[kBpc], z1[kBpc];
+#pragma unroll
+      for (int bi = 0; bi < kBpc; ++bi) {
+        if (SF32) {
+          const float *s4 = reinterpret_cast<const float *>(sc) + (tile * kBpc + bi) * kTileN;
+          s0[bi] = s4[g];
+          s1[bi] = s4[g + 8];
+        } else {
+          const uint16_t *s2 = reinterpret_cast<const uint16_t *>(sc) + (tile * kBpc + bi) * kTileN;
+          s0[bi] = bf16_bits_to_f32(s2[g]);
+          s1[bi] = bf16_bits_to_f32(s2[g + 8]);
+        }
+        z0[bi] = z1[bi] = 136.f;  // 128 + 8
+        if (HAS_ZP) {
+          const int b = blk0 + bi;
+          const int pairs = BS < 32 ? 2 : 1;
+          const uint2 zw = zp[(tile * pairs + (BS < 32 ? bi >> 1 : 0)) * 2 + (b & 1)];
+          z0[bi] = static_cast<float>(128 + ((zw.x >> (4 * g)) & 15));
+          z1[bi] = static_cast<float>(128 + ((zw.y >> (4 * g)) & 15));
+        }
+      }
+      const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + tile * kChunkBytes + lane * 16);
+      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int bi = BS < kBK ? (16 * j) / BS : 0;
+        uint32_t r[4];
+        codes_to_bf16x2(wv[j], r);
+        // r[0], r[2]: row g at k0 .. k0 + 3; r[1], r[3]: row g + 8.
+        auto w = [&](uint32_t pair, int hi, float z, float sc1) {
+          const float v = bf16_bits_to_f32(hi ? (pair >> 16) : (pair & 0xFFFFu));
+          return to_tf32((v - z) * sc1);  // q - z exact, one rounding in the product
+        };
+        const uint4 row0 = make_uint4(w(r[0], 0, z0[bi], s0[bi]), w(r[0], 1, z0[bi], s0[bi]),
+                                      w(r[2], 0, z0[bi], s0[bi]), w(r[2], 1, z0[bi], s0[bi]));
+        const uint4 row1 = make_uint4(w(r[1], 0, z1[bi], s1[bi]), w(r[1], 1, z1[bi], s1[bi]),
+                                      w(r[3], 0, z1[bi], s1[bi]), w(r[3], 1, z1[bi], s1[bi]));
+        // K-major 128-byte swizzle over 32 fp32 per row: 16-byte chunk
+        // ((k % 32) / 4) XOR (row % 8), in the half holding k.
+        const int k0 = 16 * j + 4 * t;
+        unsigned char *half = btile + (k0 >> 5) * S::kHalf;
+        const int c = (k0 & 31) >> 2;
+        *reinterpret_cast<uint4 *>(half + r0 * 128 + ((c ^ (r0 & 7)) * 16)) = row0;
+        *reinterpret_cast<uint4 *>(half + (r0 + 1) * 128 + ((c ^ ((r0 + 1) & 7)) * 16)) = row1;
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bfull + bslot);
+    }
+
+    if (!fault && !mbar_wait(acc_full, 0)) {
+      record_fault(&g_fault_gemm, kFaultGemmWait);
+      fault = true;
+    }
+    named_barrier_sync(kBarEpi, 32 * kDqWarps);  // bias staged
+    if (!fault && p.ksplit > 1) {
+      // Park the accumulator, column-major [col][row], in the drained A ring.
+      tc_fence_after();
+      float *part = reinterpret_cast<float *>(smem + S::kA);
+      const int quarter = warp & 3, half = (warp - 2) >> 2;
+      const int row = quarter * 32 + lane;
+#pragma unroll 1
+      for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
+        float v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) part[(c * 32 + q) * kBH + row] = v[q];
+      }
+    } else if (!fault) {
+      tc_fence_after();
+      const int quarter = warp & 3, half = (warp - 2) >> 2;
+      const int m = m0 + quarter * 32 + lane;
+      const int n_base = nt0 * kTileN;
+      const bool y4 = (p.N % 4) == 0 && (reinterpret_cast<uintptr_t>(p.Y) % 16) == 0;
+#pragma unroll 1
+      for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
+        float v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, v);
+        if (m < p.M) {
+          const int n0 = n_base + c * 32;
+          float *yrow = static_cast<float *>(p.Y) + static_cast<int64_t>(m) * p.N;
+          float o[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o[out_col(q)] = v[q] + sBias[c * 32 + out_col(q)];
+          if (n0 + 32 <= p.N && y4) {
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+              *reinterpret_cast<float4 *>(yrow + n0 + q) =
+                  make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+          } else {
+            for (int q = 0; q < 32; ++q)
+              if (n0 + q < p.N) yrow[n0 + q] = o[q];
+          }
+        }
+      }
+    }
+  }
+
+  if (p.ksplit > 1) {
+    // Split-K reduction: this CTA's slice of the tile's columns, summed over
+    // the cluster's partials in rank order (bitwise reproducible).
+    cluster_sync_all();
+    if (warp >= 2) {
+      const float *part = reinterpret_cast<const float *>(smem + S::kA);
+      const int cols = kBN / p.ksplit;  // 16, 32, 64 or 128
+      const int items = kBH * (cols / 16);
+      const int n_base = nt0 * kTileN;
+      for (int it = tid - 64; it < items; it += 32 * kDqWarps) {
+        const int row = it % kBH, c0 = blockIdx.z * cols + (it / kBH) * 16;
+        float acc[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+        for (int r = 0; r < p.ksplit; ++r)
+#pragma unroll
+          for (int q = 0; q < 16; ++q) acc[q] += ld_dsmem_f32(part + (c0 + q) * kBH + row, r);
+        const int m = m0 + row;
+        if (m < p.M) {
+          float *yrow = static_cast<float *>(p.Y) + static_cast<int64_t>(m) * p.N;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int n = n_base + c0 + out_col(q);
+            if (n < p.N) yrow[n] = acc[q] + sBias[c0 + out_col(q)];
+          }
+        }
+      }
+    }
+    cluster_sync_all();  // peers are done reading this CTA's partials
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN)
+                 : "memory");
+  }
+}
+
+template <int BS, bool HAS_ZP, bool SF32>
+cudaError_t launch_tf32_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
+  auto kernel = gemm_tf32_kernel<BS, HAS_ZP, SF32>;
+  const int smem = SmemT::kTotal + 1024;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (p.ksplit > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = p.ksplit;
+    ++na;
+  }
+  if (pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <int BS>
+cudaError_t launch_tf32_flags(const GemmParams &p, dim3 grid, bool sf32, bool pdl,
+                              cudaStream_t stream) {
+  if (p.has_zp)
+    return sf32 ? launch_tf32_one<BS, true, true>(p, grid, pdl, stream)
+                : launch_tf32_one<BS, true, false>(p, grid, pdl, stream);
+  return sf32 ? launch_tf32_one<BS, false, true>(p, grid, pdl, stream)
+              : launch_tf32_one<BS, false, false>(p, grid, pdl, stream);
+}
+
 template <int BS, bool HAS_ZP, bool SF32, int MH>
 cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
   auto kernel = gemm_kernel<BS, HAS_ZP, SF32, MH>;
@@ -657,12 +1011,102 @@ cudaError_t gemm_take_fault(unsigned int *out) {
 }
 
 bool gemm_supports(const MatmulArgs &a) {
-  // bf16 activations whose rows TMA can address (16-byte row stride).
-  return !a.a_f32 && (a.K % 8) == 0 && (reinterpret_cast<uintptr_t>(a.A) % 16) == 0;
+  // Activations whose rows TMA can address (16-byte row stride and base):
+  // bf16 (any weight), or fp32 on the tf32 kernel (single weights).
+  if (reinterpret_cast<uintptr_t>(a.A) % 16 != 0) return false;
+  if (a.a_f32) return (a.K % 4) == 0 && !a.paired;
+  return (a.K % 8) == 0;
+}
+
+// fp32 activations: the tf32 kernel, 128 x 128 tiles, one CTA per SM.
+cudaError_t launch_gemm_tf32(const MatmulArgs &a, cudaStream_t stream) {
+  GemmParams p{};
+  const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
+  const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
+  const uint64_t es = a.scale_f32 ? 4 : 2;
+  const uint32_t bpc = a.bs < kBK ? kBK / a.bs : 1;
+  const uint32_t ppc = a.bs < 32 ? 2 : 1;
+  cudaError_t e;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 4};
+    const uint32_t box[2] = {kBK / 2, kBH};  // 32 fp32 = 128 bytes per row
+    e = make_tmap(&p.tma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.A, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const uint64_t dims[3] = {kChunkBytes / 4, K64, N16};
+    const uint64_t strides[2] = {kChunkBytes, K64 * kChunkBytes};
+    const uint32_t box[3] = {kChunkBytes / 4, 1, kTilesN};
+    e = make_tmap(&p.tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.packed_b, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const uint64_t words = kTileN * es / 4;
+    const uint64_t dims[3] = {words, nb, N16};
+    const uint64_t strides[2] = {kTileN * es, nb * kTileN * es};
+    const uint32_t box[3] = {static_cast<uint32_t>(words), bpc, kTilesN};
+    e = make_tmap(&p.tms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.scales, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.zp) {
+    const uint64_t dims[3] = {4, nbz / 2, N16};
+    const uint64_t strides[2] = {16, nbz * 8};
+    const uint32_t box[3] = {4, ppc, kTilesN};
+    e = make_tmap(&p.tmz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, a.zp, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
+  p.sc_bytes = static_cast<int>(kTilesN * bpc * kTileN * es);
+  p.zp_bytes = a.zp ? static_cast<int>(kTilesN * ppc * 16) : 0;
+  p.bias = a.bias;
+  p.Y = a.Y;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K64 = static_cast<int>(K64);
+  p.has_zp = a.zp != nullptr;
+  // K split (cluster of 1..8 CTAs) when the output tiles cannot fill the
+  // GPU: a CTA spends about 0.75 us per 64-wide k stage (the tf32 tensor
+  // rate of one SM), plus the split's fixed cost; one CTA per SM, clusters
+  // packing per GPC.
+  const int64_t tiles = ceil_div(a.M, int64_t(kBH)) * ceil_div(a.N, int64_t(kBN));
+  int ksplit = 1;
+  {
+    const int sms = sm_count();
+    double best = 0.0;
+    for (int c = 1; c <= 8; c *= 2) {
+      const int64_t kps = ceil_div(int64_t(K64), int64_t(c));
+      if (c > 1 && (kps < 4 || (c - 1) * kps >= int64_t(K64))) continue;
+      const int64_t slots = c <= 2 ? sms - (c == 2 ? 8 : 0) : sms - 24;
+      const double fixed = c == 1 ? 2.0 : c == 2 ? 4.0 : c == 4 ? 6.0 : 13.0;
+      const double cost = double(ceil_div(tiles * c, slots)) * (double(kps) * 0.75 + fixed);
+      if (c == 1 || cost < best - 1e-9) {
+        best = cost;
+        ksplit = c;
+      }
+    }
+  }
+  p.ksplit = ksplit;
+  p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
+  const dim3 grid(static_cast<unsigned>(ceil_div(a.N, int64_t(kBN))),
+                  static_cast<unsigned>(ceil_div(a.M, int64_t(kBH))),
+                  static_cast<unsigned>(ksplit));
+  switch (a.bs) {
+    case 16: return launch_tf32_flags<16>(p, grid, a.scale_f32, a.pdl, stream);
+    case 32: return launch_tf32_flags<32>(p, grid, a.scale_f32, a.pdl, stream);
+    case 64: return launch_tf32_flags<64>(p, grid, a.scale_f32, a.pdl, stream);
+    case 128: return launch_tf32_flags<128>(p, grid, a.scale_f32, a.pdl, stream);
+    case 256: return launch_tf32_flags<256>(p, grid, a.scale_f32, a.pdl, stream);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   if (!gemm_supports(a)) return cudaErrorNotSupported;
+  if (a.a_f32) return launch_gemm_tf32(a, stream);
   GemmParams p{};
   const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
   // Output columns per CTA: 128, or 64 for a gated-MLP pair (64 gate and 64

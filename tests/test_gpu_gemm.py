@@ -7,6 +7,11 @@ its error is bounded by 2^-8 * sum|a w| plus fp32 accumulation; with random
 inputs and K >= 256 the rounding errors average out far below the stated
 2e-3 * sum|a w| + 1e-5 bound, which these tests apply. Small-K shapes are
 checked against the rigorous rounding bound instead.
+
+fp32 activations take the tf32 kernel: the dequantised weight is rounded
+to tf32 (2^-11) and the tensor core reads A with a tf32 significand
+(2^-10), so each product is within 1.5e-3 of exact and the stated bound
+holds rigorously for any K.
 """
 import numpy as np
 import pytest
@@ -85,7 +90,7 @@ def test_gemm_matches_gemv_path_at_crossover(dev):
 
 @pytest.mark.parametrize("M", [17, 64, 100])
 def test_fp32_activations_above_16_rows(dev, M):
-    """fp32 activations with M > 16 run the decode kernel over 16-row slices."""
+    """fp32 activations with M > 16 (and 16-byte rows) run the tf32 kernel."""
     prob = make_problem(M, 700, 1000, 32, dtype=torch.float32, zero_points=True, bias=True,
                         seed=M)
     Y = run(prob, dev)
@@ -131,3 +136,52 @@ def test_gemm_256_row_tiles_with_tails(dev, bs, with_zp):
                                      rng.choice(N, 48, replace=False)]))
     R, mag = ref(prob, rows=rows, cols=cols)
     check(Y[rows][:, cols], R, mag, f"gemm256 bs{bs}")
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("with_zp", [False, True])
+@pytest.mark.parametrize("scale_f32", [False, True])
+def test_tf32_gemm_tiles_and_tails(dev, bs, with_zp, scale_f32):
+    """fp32 activations on the tf32 kernel: ragged M and N around the
+    128 x 128 tile, a partial last block, K from 4 to 2560."""
+    i = 0
+    for (M, N, K) in ((128, 128, 256), (129, 257, 520), (300, 1000, 1024), (17, 16, 264),
+                      (200, 130, 2560), (33, 70, 4), (150, 40, 100)):
+        i += 1
+        prob = make_problem(M, N, K, bs, dtype=torch.float32, zero_points=with_zp,
+                            bias=(i % 2 == 0), seed=20 * bs + i)
+        if not scale_f32:
+            prob.scales = prob.scales.to(torch.bfloat16)
+        Y = run(prob, dev, path="gemm")
+        assert Y.dtype == torch.float32
+        R, mag = ref(prob)
+        check(Y, R, mag, f"tf32 M{M} N{N} K{K} bs{bs}")
+
+
+def test_fp32_rows_the_tma_cannot_address(dev):
+    """K = 1001 fp32 rows are not 16-byte strided: the dispatch keeps them on
+    the decode kernel's 16-row slices; forcing the tensor-core path is
+    refused."""
+    prob = make_problem(40, 300, 1001, 64, dtype=torch.float32, zero_points=True, bias=True,
+                        seed=9)
+    R, mag = ref(prob)
+    check(run(prob, dev), R, mag, "fp32 K1001 auto")
+    with pytest.raises(mnb.MnbError) as e:
+        run(prob, dev, path="gemm")
+    assert e.value.status == -8
+
+
+@pytest.mark.parametrize("proj", ["q", "o", "gate", "down"])
+def test_qwen3_0p6b_fp32_prefill_sampled(dev, proj):
+    """Qwen3-0.6B prefill shapes as the artifact stores them (fp32 A and
+    scales, bs 32, zero points), M = 512: seeded 8 rows x 64 columns."""
+    from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_0P6B
+    p = {q.name: q for q in QWEN3_0P6B["projections"]}[proj]
+    prob = make_problem(512, p.N, p.K, 32, dtype=torch.float32, zero_points=True, bias=False,
+                        seed=p.N + p.K)
+    Y = run(prob, dev)
+    rng = np.random.default_rng(p.N)
+    rows = np.sort(rng.choice(512, 8, replace=False))
+    cols = np.sort(rng.choice(p.N, 64, replace=False))
+    R, mag = ref(prob, rows=rows, cols=cols)
+    check(Y[rows][:, cols], R, mag, f"0.6B {proj}")
