@@ -522,6 +522,7 @@ CASES = {
     "gemv_gate": (1, 9728, 2560, 128, "bf16", False, False, "auto"),
     "gemv_lm_head": (1, 151936, 2560, 128, "bf16", False, False, "auto"),
     "gemm_gate": (2048, 9728, 2560, 128, "bf16", True, True, "gemm"),
+    "gemm_gate_f32": (2048, 9728, 2560, 128, "f32", True, True, "gemm"),
 }
 
 

@@ -199,9 +199,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   using S = Smem<MH>;
   constexpr int kStages = S::kStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // 1024-byte alignment for the swizzled operand tiles.
-  unsigned char *smem = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment for the swizzled operand tiles. The offset is added
+  // to the shared array itself (not through an integer cast) so that every
+  // access below stays a shared-memory access rather than a generic one.
+  unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBar);
   uint64_t *empty = full + kStages;
   uint64_t *bfull = empty + kStages;
@@ -630,6 +631,17 @@ __device__ __forceinline__ void umma_tf32(uint32_t tmem_d, uint64_t adesc, uint6
       : "memory");
 }
 
+// B row (within a 16-row tile) of weight row g < 8 in the tf32 tile: rows
+// g = 2p and 2p + 1 (the lanes of one 8-lane store phase) go to rows p and
+// p + 4, whose swizzle phases differ in bit 2, so the phase's two rows write
+// disjoint halves of the 128-byte row: conflict-free 16-byte stores. Weight
+// row g + 8 goes 8 rows further.
+__host__ __device__ constexpr int tf32_row(int g) { return ((g & 1) << 2) | (g >> 1); }
+// Output column (within the CTA's 128) of tf32 accumulator column c.
+__host__ __device__ constexpr int out_col_tf32(int c) {
+  return (c & ~7) + 2 * (c & 3) + ((c >> 2) & 1);
+}
+
 // fp32 -> tf32, round to nearest (ties away from zero), as fp32 bits.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t r;
@@ -643,8 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using S = SmemT;
   constexpr int kStages = S::kStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char *smem = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBar);
   uint64_t *empty = full + kStages;
   uint64_t *bfull = empty + kStages;
@@ -736,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int tile = warp - 2;
     const int g = lane >> 2, t = lane & 3;
-    const int r0 = tile * kTileN + 2 * g;  // B rows 2g, 2g + 1 of weight rows g, g + 8
+    const int r0 = tile * kTileN + tf32_row(g);  // weight row g; g + 8 is r0 + 8
     {
       const int e = tid - 64;
       if (e < kBN) {
@@ -800,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char *half = btile + (k0 >> 5) * S::kHalf;
         const int c = (k0 & 31) >> 2;
         *reinterpret_cast<uint4 *>(half + r0 * 128 + ((c ^ (r0 & 7)) * 16)) = row0;
-        *reinterpret_cast<uint4 *>(half + (r0 + 1) * 128 + ((c ^ ((r0 + 1) & 7)) * 16)) = row1;
+        *reinterpret_cast<uint4 *>(half + (r0 + 8) * 128 + ((c ^ (r0 & 7)) * 16)) = row1;
       }
       fence_async_smem();
       __syncwarp();
@@ -840,7 +851,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float *yrow = static_cast<float *>(p.Y) + static_cast<int64_t>(m) * p.N;
           float o[32];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) o[out_col(q)] = v[q] + sBias[c * 32 + out_col(q)];
+          for (int q = 0; q < 32; ++q)
+            o[out_col_tf32(q)] = v[q] + sBias[c * 32 + out_col_tf32(q)];
           if (n0 + 32 <= p.N && y4) {
 #pragma unroll
             for (int q = 0; q < 32; q += 4)
@@ -877,8 +889,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float *yrow = static_cast<float *>(p.Y) + static_cast<int64_t>(m) * p.N;
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
-            const int n = n_base + c0 + out_col(q);
-            if (n < p.N) yrow[n] = acc[q] + sBias[c0 + out_col(q)];
+            const int n = n_base + c0 + out_col_tf32(q);
+            if (n < p.N) yrow[n] = acc[q] + sBias[c0 + out_col_tf32(q)];
           }
         }
       }
