@@ -83,27 +83,43 @@ struct GemmParams {
   int sc_up, zp_up;  // paired: byte offsets of the up halves in a stage's scales / zero points
 };
 
-// Shared-memory plan (offsets from a 1024-aligned base).
-template <int MH>
-struct Smem {
-  static constexpr int kStages = MH == 1 ? 3 : 2;  // input ring depth
-  static constexpr int kATileBytes = MH * kAHalfBytes;
-  static constexpr int kA = 0;
-  static constexpr int kB = kA + kStages * kATileBytes;
-  static constexpr int kCodes = kB + kBStages * kBTileBytes;
-  static constexpr int kSc = kCodes + kStages * kCodeBytes;
-  static constexpr int kScBytes = 2048;  // 8 tiles x up to 4 blocks x 16 fp32 scales
-  static constexpr int kZp = kSc + kStages * kScBytes;
-  static constexpr int kZpBytes = 256;  // 8 tiles * 2 pairs * 16 bytes
-  static constexpr int kBias = kZp + kStages * kZpBytes;
-  static constexpr int kBar = kBias + kBN * 4;
-  static constexpr int kTmemSlot = kBar + (2 * kStages + 2 * kBStages + 1) * 8;
-  static constexpr int kTotal = kTmemSlot + 16;
-};
+// Shared-memory plan (offsets from a 1024-aligned base). The A tiles and the
+// packed weights of a stage travel in separate rings: the small weight
+// stream (codes, scales, zero points) runs further ahead, so a stage's B tile
+// is dequantised while its A tile is still in flight.
 // Two CTAs share an SM: each may use at most half of its 228 KB, less the
 // 1 KB the runtime reserves per CTA and the 1 KB alignment slack.
-static_assert(Smem<1>::kTotal + 1024 <= (228 * 1024) / 2 - 1024, "two CTAs per SM");
-static_assert(Smem<2>::kTotal + 1024 <= (228 * 1024) / 2 - 1024, "two CTAs per SM");
+constexpr int kSmemLimit2 = (228 * 1024) / 2 - 1024;
+
+template <int MH, int BS, bool SF32>
+struct Smem {
+  static constexpr int kAStages = MH == 1 ? 3 : 2;  // A ring depth
+  static constexpr int kATileBytes = MH * kAHalfBytes;
+  static constexpr int kBpcS = BS < kBK ? kBK / BS : 1;
+  // 8 tiles x the stage's blocks x 16 scales (a multiple of 128 bytes).
+  static constexpr int kScBytes = kTilesN * kBpcS * kTileN * (SF32 ? 4 : 2);
+  static constexpr int kZpBytes = 256;  // 8 tiles x up to 2 pairs x 16 bytes, or a pair's halves
+  // Weight ring depth: 3 where it fits beside the A and B rings, else 2.
+  static constexpr int kWBytes = kCodeBytes + kScBytes + kZpBytes;
+  static constexpr int kFixed =
+      kAStages * kATileBytes + kBStages * kBTileBytes + kBN * 4 + 256 + 1024;
+  static constexpr int kWStages = kFixed + 3 * kWBytes <= kSmemLimit2 ? 3 : 2;
+  static constexpr int kA = 0;
+  static constexpr int kB = kA + kAStages * kATileBytes;
+  static constexpr int kCodes = kB + kBStages * kBTileBytes;
+  static constexpr int kSc = kCodes + kWStages * kCodeBytes;
+  static constexpr int kZp = kSc + kWStages * kScBytes;
+  static constexpr int kBias = kZp + kWStages * kZpBytes;
+  static constexpr int kBar = kBias + kBN * 4;
+  static constexpr int kNumBars = 2 * kAStages + 2 * kWStages + 2 * kBStages + 1;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kTotal = kTmemSlot + 16;
+};
+static_assert(Smem<1, 16, true>::kTotal + 1024 <= kSmemLimit2, "two CTAs per SM");
+static_assert(Smem<2, 16, true>::kTotal + 1024 <= kSmemLimit2, "two CTAs per SM");
+static_assert(Smem<2, 128, false>::kWStages == 3, "three weight stages for the common case");
+// A split-K CTA parks its 128 x 128 fp32 accumulator in the drained A and B rings.
+static_assert(Smem<1, 16, true>::kCodes >= kBH * kBN * 4, "split-K parking space");
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   // K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row atoms of
@@ -196,16 +212,18 @@ __host__ __device__ constexpr int out_col(int c) {
 
 template <int BS, bool HAS_ZP, bool SF32, int MH>
 __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant__ GemmParams p) {
-  using S = Smem<MH>;
-  constexpr int kStages = S::kStages;
+  using S = Smem<MH, BS, SF32>;
+  constexpr int kAStages = S::kAStages, kWStages = S::kWStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles. The offset is added
   // to the shared array itself (not through an integer cast) so that every
   // access below stays a shared-memory access rather than a generic one.
   unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBar);
-  uint64_t *empty = full + kStages;
-  uint64_t *bfull = empty + kStages;
+  uint64_t *afull = reinterpret_cast<uint64_t *>(smem + S::kBar);
+  uint64_t *aempty = afull + kAStages;
+  uint64_t *wfull = aempty + kAStages;
+  uint64_t *wempty = wfull + kWStages;
+  uint64_t *bfull = wempty + kWStages;
   uint64_t *bempty = bfull + kBStages;
   uint64_t *acc_full = bempty + kBStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kTmemSlot);
@@ -220,9 +238,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   const int nk = min(p.K64 - kb0, p.kps);
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(empty + i, 1);
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(afull + i, 1);
+      mbar_init(aempty + i, 1);
+    }
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(wfull + i, 1);
+      mbar_init(wempty + i, kDqWarps);
     }
     for (int i = 0; i < kBStages; ++i) {
       mbar_init(bfull + i, kDqWarps);
@@ -251,16 +273,27 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   bool fault = false;
   if (warp == 0) {
     if (lane == 0) {
+      // A tiles.
       for (int i = 0; i < nk; ++i) {
-        const int s = i % kStages, kb = kb0 + i;
-        if (i >= kStages && !mbar_wait(empty + s, ((i / kStages) - 1) & 1)) {
+        const int s = i % kAStages, kb = kb0 + i;
+        if (i >= kAStages && !mbar_wait(aempty + s, ((i / kAStages) - 1) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           break;
         }
-        uint64_t *bar = full + s;
-        mbar_arrive_expect_tx(bar, S::kATileBytes + kCodeBytes + p.sc_bytes + p.zp_bytes);
+        mbar_arrive_expect_tx(afull + s, S::kATileBytes);
+        tma_load_2d(smem + S::kA + s * S::kATileBytes, &p.tma, kb * kBK, m0, afull + s);
+      }
+    } else if (lane == 1) {
+      // Packed weights: codes, scales and zero points of the stage.
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % kWStages, kb = kb0 + i;
+        if (i >= kWStages && !mbar_wait(wempty + s, ((i / kWStages) - 1) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          break;
+        }
+        uint64_t *bar = wfull + s;
+        mbar_arrive_expect_tx(bar, kCodeBytes + p.sc_bytes + p.zp_bytes);
         const int blk = (kb * kBK) / BS;
-        tma_load_2d(smem + S::kA + s * S::kATileBytes, &p.tma, kb * kBK, m0, bar);
         unsigned char *cd = smem + S::kCodes + s * kCodeBytes;
         unsigned char *sd = smem + S::kSc + s * S::kScBytes;
         unsigned char *zd = smem + S::kZp + s * S::kZpBytes;
@@ -284,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   } else if (warp == 1) {
     if (lane == 0) {
       for (int i = 0; i < nk; ++i) {
-        const int s = i % kStages, b = i % kBStages;
-        if (!mbar_wait(full + s, (i / kStages) & 1) ||
+        const int s = i % kAStages, b = i % kBStages;
+        if (!mbar_wait(afull + s, (i / kAStages) & 1) ||
             !mbar_wait(bfull + b, (i / kBStages) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           fault = true;
@@ -300,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
           for (int h = 0; h < MH; ++h)
             umma_bf16(tmem + h * kBN, smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32),
                       smem_desc_sw128(b_base + kk * 32), i > 0 || kk > 0);
-        umma_commit(empty + s);
+        umma_commit(aempty + s);
         umma_commit(bempty + b);
       }
       if (!fault) umma_commit(acc_full);
@@ -325,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
       }
     }
     for (int i = 0; i < nk; ++i) {
-      const int s = i % kStages, bslot = i % kBStages, kb = kb0 + i;
-      if (!mbar_wait(full + s, (i / kStages) & 1) ||
+      const int s = i % kWStages, bslot = i % kBStages, kb = kb0 + i;
+      if (!mbar_wait(wfull + s, (i / kWStages) & 1) ||
           (i >= kBStages && !mbar_wait(bempty + bslot, ((i / kBStages) - 1) & 1))) {
         record_fault(&g_fault_gemm, kFaultGemmWait);
         fault = true;
@@ -389,7 +422,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
       }
       fence_async_smem();  // make the tile visible to the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(bfull + bslot);
+      if (lane == 0) {
+        mbar_arrive(bfull + bslot);
+        mbar_arrive(wempty + s);  // this warp is done with the stage's weights
+      }
     }
 
     // ---- epilogue: TMEM -> registers -> Y ----------------------------------
@@ -955,7 +991,7 @@ cudaError_t launch_tf32_flags(const GemmParams &p, dim3 grid, bool sf32, bool pd
 template <int BS, bool HAS_ZP, bool SF32, int MH>
 cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
   auto kernel = gemm_kernel<BS, HAS_ZP, SF32, MH>;
-  const int smem = Smem<MH>::kTotal + 1024;
+  const int smem = Smem<MH, BS, SF32>::kTotal + 1024;
   static bool configured = false;
   if (!configured) {
     const cudaError_t e =
