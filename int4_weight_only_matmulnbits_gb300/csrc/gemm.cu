@@ -635,20 +635,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
 // with fp32 accumulation the stated bound 2e-3 * sum|a w| + 1e-5 holds. One
 // CTA per SM (the fp32 tiles need about 180 KB of shared memory).
 struct SmemT {
-  static constexpr int kStages = 3;
+  static constexpr int kAStages = 3;  // A ring
+  static constexpr int kWStages = 4;  // packed-weight ring, further ahead
   static constexpr int kATile = kBH * kBK * 4;  // 32 KB: two 16 KB halves
   static constexpr int kBTile = kBN * kBK * 4;  // 32 KB: two 16 KB halves
   static constexpr int kHalf = 16 * 1024;
   static constexpr int kA = 0;
-  static constexpr int kB = kA + kStages * kATile;
+  static constexpr int kB = kA + kAStages * kATile;
   static constexpr int kCodes = kB + kBStages * kBTile;
-  static constexpr int kSc = kCodes + kStages * kCodeBytes;
+  static constexpr int kSc = kCodes + kWStages * kCodeBytes;
   static constexpr int kScBytes = 2048;
-  static constexpr int kZp = kSc + kStages * kScBytes;
+  static constexpr int kZp = kSc + kWStages * kScBytes;
   static constexpr int kZpBytes = 256;
-  static constexpr int kBias = kZp + kStages * kZpBytes;
+  static constexpr int kBias = kZp + kWStages * kZpBytes;
   static constexpr int kBar = kBias + kBN * 4;
-  static constexpr int kTmemSlot = kBar + (2 * kStages + 2 * kBStages + 1) * 8;
+  static constexpr int kTmemSlot = kBar + (2 * kAStages + 2 * kWStages + 2 * kBStages + 1) * 8;
   static constexpr int kTotal = kTmemSlot + 16;
 };
 static_assert(SmemT::kTotal + 1024 <= 227 * 1024, "one CTA per SM");
@@ -689,12 +690,14 @@ template <int BS, bool HAS_ZP, bool SF32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tf32_kernel(const __grid_constant__ GemmParams p) {
   using S = SmemT;
-  constexpr int kStages = S::kStages;
+  constexpr int kAStages = S::kAStages, kWStages = S::kWStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBar);
-  uint64_t *empty = full + kStages;
-  uint64_t *bfull = empty + kStages;
+  uint64_t *afull = reinterpret_cast<uint64_t *>(smem + S::kBar);
+  uint64_t *aempty = afull + kAStages;
+  uint64_t *wfull = aempty + kAStages;
+  uint64_t *wempty = wfull + kWStages;
+  uint64_t *bfull = wempty + kWStages;
   uint64_t *bempty = bfull + kBStages;
   uint64_t *acc_full = bempty + kBStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kTmemSlot);
@@ -709,9 +712,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nk = min(p.K64 - kb0, p.kps);
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(empty + i, 1);
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(afull + i, 1);
+      mbar_init(aempty + i, 1);
+    }
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(wfull + i, 1);
+      mbar_init(wempty + i, kDqWarps);
     }
     for (int i = 0; i < kBStages; ++i) {
       mbar_init(bfull + i, kDqWarps);
@@ -738,19 +745,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool fault = false;
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % kStages;
-        if (i >= kStages && !mbar_wait(empty + s, ((i / kStages) - 1) & 1)) {
+      for (int i = 0; i < nk; ++i) {  // A tiles
+        const int s = i % kAStages, kb = kb0 + i;
+        if (i >= kAStages && !mbar_wait(aempty + s, ((i / kAStages) - 1) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           break;
         }
-        uint64_t *bar = full + s;
-        mbar_arrive_expect_tx(bar, S::kATile + kCodeBytes + p.sc_bytes + p.zp_bytes);
-        const int kb = kb0 + i;
-        const int blk = (kb * kBK) / BS;
+        mbar_arrive_expect_tx(afull + s, S::kATile);
         unsigned char *ad = smem + S::kA + s * S::kATile;
-        tma_load_2d(ad, &p.tma, kb * kBK, m0, bar);
-        tma_load_2d(ad + S::kHalf, &p.tma, kb * kBK + kBK / 2, m0, bar);
+        tma_load_2d(ad, &p.tma, kb * kBK, m0, afull + s);
+        tma_load_2d(ad + S::kHalf, &p.tma, kb * kBK + kBK / 2, m0, afull + s);
+      }
+    } else if (lane == 1) {
+      for (int i = 0; i < nk; ++i) {  // packed weights
+        const int s = i % kWStages, kb = kb0 + i;
+        if (i >= kWStages && !mbar_wait(wempty + s, ((i / kWStages) - 1) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          break;
+        }
+        uint64_t *bar = wfull + s;
+        mbar_arrive_expect_tx(bar, kCodeBytes + p.sc_bytes + p.zp_bytes);
+        const int blk = (kb * kBK) / BS;
         tma_load_3d(smem + S::kCodes + s * kCodeBytes, &p.tmw, 0, kb, nt0, bar);
         tma_load_3d(smem + S::kSc + s * S::kScBytes, &p.tms, 0, blk, nt0, bar);
         if (HAS_ZP) tma_load_3d(smem + S::kZp + s * S::kZpBytes, &p.tmz, 0, blk >> 1, nt0, bar);
@@ -759,8 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       for (int i = 0; i < nk; ++i) {
-        const int s = i % kStages, b = i % kBStages;
-        if (!mbar_wait(full + s, (i / kStages) & 1) ||
+        const int s = i % kAStages, b = i % kBStages;
+        if (!mbar_wait(afull + s, (i / kAStages) & 1) ||
             !mbar_wait(bfull + b, (i / kBStages) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           fault = true;
@@ -775,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_tf32(tmem, smem_desc_sw128(a_base + off), smem_desc_sw128(b_base + off),
                     i > 0 || kk > 0);
         }
-        umma_commit(empty + s);
+        umma_commit(aempty + s);
         umma_commit(bempty + b);
       }
       if (!fault) umma_commit(acc_full);
@@ -792,8 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int i = 0; i < nk; ++i) {
-      const int s = i % kStages, bslot = i % kBStages;
-      if (!mbar_wait(full + s, (i / kStages) & 1) ||
+      const int s = i % kWStages, bslot = i % kBStages;
+      if (!mbar_wait(wfull + s, (i / kWStages) & 1) ||
           (i >= kBStages && !mbar_wait(bempty + bslot, ((i / kBStages) - 1) & 1))) {
         record_fault(&g_fault_gemm, kFaultGemmWait);
         fault = true;
@@ -851,7 +866,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bfull + bslot);
+      if (lane == 0) {
+        mbar_arrive(bfull + bslot);
+        mbar_arrive(wempty + s);
+      }
     }
 
     if (!fault && !mbar_wait(acc_full, 0)) {
@@ -1162,9 +1180,8 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   const int64_t cols = a.paired ? kBN / 2 : kBN;
   // Tile height (128 or 256 rows) and K split (cluster of 1..8 CTAs, 128-row
   // tiles only) by a cost model fitted to GB300 measurements: a CTA spends
-  // about 0.77 us per 64-wide k stage with 128 rows and 1.12 us with 256
-  // rows (its dequantisation warps are latency-bound, so this hardly depends
-  // on a second CTA sharing the SM), plus a fixed cost that grows with the
+  // about 0.72 us per 64-wide k stage with 128 rows and 0.95 us with 256
+  // rows (two CTAs share the SM's tensor core), plus a fixed cost that grows with the
   // split (the partial tiles' reduction through distributed shared memory);
   // CTAs run in rounds of what can be resident at once, clusters packing per
   // GPC.
@@ -1183,7 +1200,7 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
         if (slots <= 0) continue;
         const double fixed = c == 1 ? 2.0 : c == 2 ? 4.0 : c == 4 ? 6.0 : 13.0;
         const double cost = double(ceil_div(ctas, slots)) *
-                            (double(kps) * (h == 2 ? 1.12 : 0.77) + fixed);
+                            (double(kps) * (h == 2 ? 0.95 : 0.72) + fixed);
         if (!have || cost < best - 1e-9) {
           best = cost;
           mh = h;
