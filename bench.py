@@ -183,11 +183,13 @@ def run_reference(args, rank, world):
 # GPU leg
 # ----------------------------------------------------------------------------
 
-def build_decode_step(dev, seed_base=5000):
+def build_decode_step(dev, seed_base=5000, keep=None):
     """Prepacked weights, activations and outputs of one decode step, all
     resident on dev, as a list of launches: (weights, activation row,
     outputs). Weights are drawn on the device from a seeded generator
-    (2 GB would take minutes on the host)."""
+    (2 GB would take minutes on the host). `keep`: names of launches whose
+    raw inputs (activation row, and per weight its codes and scales) are
+    also returned as host tensors in a fifth element, for parity checks."""
     import torch
 
     import int4_weight_only_matmulnbits_gb300 as mnb
@@ -208,6 +210,7 @@ def build_decode_step(dev, seed_base=5000):
     ao = yo = 0
     algo_bytes = 0
     launches = []
+    kept = {}
     seed = seed_base
     for name, ps in plan:
         K = ps[0].K
@@ -226,6 +229,9 @@ def build_decode_step(dev, seed_base=5000):
                               generator=g)
             S = (torch.rand(p.N, nb, device=dev, generator=g) * 0.008 + 0.002).to(torch.bfloat16)
             ws.append(mnb.mnb_prepack(B, S, None, p.N, K, bs))
+            if keep and name in keep:
+                kept.setdefault(name, {"A": A.cpu(), "weights": []})["weights"].append(
+                    (B.cpu(), S.cpu(), p.N, K))
             del B, S
             algo_bytes += p.N * nb * bs // 2 + p.N * nb * 2
             if not paired or i == 0:
@@ -235,6 +241,8 @@ def build_decode_step(dev, seed_base=5000):
         launches.append((name, ws, A, Ys))
         seed += 1
     torch.cuda.synchronize()
+    if keep is not None:
+        return launches, A_all, Y_all, algo_bytes, kept
     return launches, A_all, Y_all, algo_bytes
 
 
