@@ -61,6 +61,9 @@ def load(path: str | None = None):
         lib.oracle_qdq_matmul.restype = i32
         lib.oracle_rms_normalize.argtypes = [p, i32, p, ctypes.c_double, i64, i64, p]
         lib.oracle_rms_normalize.restype = i32
+        lib.oracle_bnb4_matmul.argtypes = [p, i32, p, p, i32, p, p, i64, i64, i64, i32, p,
+                                           i64, p, i64, p, p]
+        lib.oracle_bnb4_matmul.restype = i32
         if path is None:
             _lib = lib
         return lib
@@ -249,3 +252,44 @@ def lm_head_argmax(Y):
     greedy ArgMax"): the index of the largest logit of each row, the first
     one on ties (numpy's argmax)."""
     return np.argmax(np.asarray(Y), axis=1)
+
+
+def bnb4_matmul(A, B, absmax, code, bias=None, *, N: int, K: int, block_size: int, rows=None,
+                cols=None, lib=None):
+    """The bitsandbytes-style 4-bit matrix (page "Qwen3 CPU Inference Critical
+    Path", MatMulBnb4 row): B is the N x K weight flattened row-major, two
+    codes per byte with the first in the high nibble; absmax holds one scale
+    per block_size consecutive flattened elements; code is the 16-value fp32
+    code book; w[n,k] = code[q] * absmax. Returns (Y, absdot) like
+    matmulnbits."""
+    lib = lib or load()
+    a, a_t = _as_array(A, "A")
+    b, _ = _as_array(B, "B")
+    s, s_t = _as_array(absmax, "absmax")
+    c, c_t = _as_array(code, "code")
+    if c_t != F32 or c.size != 16:
+        raise TypeError("code must be 16 fp32 values")
+    bi = None
+    if bias is not None:
+        bi, bt = _as_array(bias, "bias")
+        if bt != F32:
+            raise TypeError("bias must be fp32")
+    if a.ndim != 2 or a.shape[1] != K:
+        raise ValueError("A must be a 2-D [M, K] array")
+    M = a.shape[0]
+    if b.size != (N * K + 1) // 2:
+        raise ValueError("B has the wrong number of bytes")
+    if s.size != -(-(N * K) // block_size):
+        raise ValueError("absmax has the wrong number of elements")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    cc = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else r.size
+    nc = N if cc is None else cc.size
+    Y = np.zeros((nr, nc), dtype=np.float64)
+    mag = np.zeros((nr, nc), dtype=np.float64)
+    rc = lib.oracle_bnb4_matmul(_ptr(a), a_t, _ptr(b), _ptr(s), s_t, _ptr(c), _ptr(bi), M, N,
+                                K, block_size, _ptr(r), 0 if r is None else r.size, _ptr(cc),
+                                0 if cc is None else cc.size, _ptr(Y), _ptr(mag))
+    if rc != 0:
+        raise ValueError(f"oracle_bnb4_matmul rejected its arguments ({rc})")
+    return Y, mag

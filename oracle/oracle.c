@@ -246,3 +246,58 @@ int oracle_rms_normalize(const void *A, int a_dtype, const float *gamma, double 
   }
   return 0;
 }
+
+/*
+ * bitsandbytes-style 4-bit matrix (page "Qwen3 CPU Inference Critical Path",
+ * com.microsoft operator inventory, row MatMulBnb4: an alternative
+ * bitsandbytes-style 4-bit matrix format, to be adapted into the same
+ * weight-only plan). The pages name the format and nothing more; readings:
+ *
+ *   B      uint8 [(N*K + 1) / 2]: the N x K weight (row n = output n)
+ *          flattened row-major; element i is in byte i/2, in the HIGH
+ *          nibble for even i (the first element of a pair high);
+ *   absmax [ceil(N*K / bs)], fp32 or bf16: one scale per run of bs
+ *          consecutive flattened elements;
+ *   code   fp32 [16]: the 16-value code book (NF4, FP4 or any other);
+ *
+ *   w[n,k] = code[q(n*K + k)] * absmax[(n*K + k) / bs]
+ *   Y[m,n] = sum_k A[m,k] * w[n,k] + bias[n]
+ *
+ * in double, in increasing k.
+ */
+static int bnb4_nibble(const uint8_t *B, int64_t i) {
+  uint8_t byte = B[i / 2];
+  return (i % 2 == 0) ? (byte >> 4) : (byte & 0x0F);
+}
+
+int oracle_bnb4_matmul(const void *A, int a_dtype, const uint8_t *B, const void *absmax,
+                       int absmax_dtype, const float *code, const float *bias,
+                       int64_t M, int64_t N, int64_t K, int bs, const int64_t *rows,
+                       int64_t n_rows, const int64_t *cols, int64_t n_cols, double *Y,
+                       double *absdot) {
+  int rc = check_args(M, N, K, 2, a_dtype, absmax_dtype);  /* any block size >= 1 here */
+  if (rc) return rc;
+  if (bs < 1 || code == NULL) return -3;
+  if (rows == NULL) n_rows = M;
+  if (cols == NULL) n_cols = N;
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t m = rows ? rows[i] : i;
+    if (m < 0 || m >= M) return -2;
+    for (int64_t j = 0; j < n_cols; ++j) {
+      int64_t n = cols ? cols[j] : j;
+      if (n < 0 || n >= N) return -2;
+      double acc = 0.0, mag = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        int64_t flat = n * K + k;
+        double w = (double)code[bnb4_nibble(B, flat)] * widen(absmax, flat / bs, absmax_dtype);
+        double a = widen(A, m * K + k, a_dtype);
+        acc += a * w;
+        mag += fabs(a * w);
+      }
+      if (bias) acc += (double)bias[n];
+      Y[i * n_cols + j] = acc;
+      if (absdot) absdot[i * n_cols + j] = mag;
+    }
+  }
+  return 0;
+}

@@ -44,3 +44,13 @@ def pack_flat(Q: np.ndarray) -> np.ndarray:
     if flat.size % 2:
         flat = np.concatenate([flat, np.zeros(1, dtype=np.uint8)])
     return (flat[0::2] | (flat[1::2] << 4)).astype(np.uint8)
+
+
+def pack_bnb4_flat(Q: np.ndarray) -> np.ndarray:
+    """Logical 4-bit codes (any shape) -> uint8 bytes with two codes per byte,
+    the FIRST of each pair in the HIGH nibble (the bitsandbytes-style order
+    read for MatMulBnb4); an odd count leaves the last low nibble 0."""
+    flat = np.asarray(Q, dtype=np.uint8).reshape(-1)
+    if flat.size % 2:
+        flat = np.concatenate([flat, np.zeros(1, dtype=np.uint8)])
+    return ((flat[0::2] << 4) | flat[1::2]).astype(np.uint8)
