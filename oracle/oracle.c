@@ -294,7 +294,7 @@ int oracle_bnb4_matmul(const void *A, int a_dtype, const uint8_t *B, const void 
         acc += a * w;
         mag += fabs(a * w);
       }
-      if (bias) acc += (double)bias[n];
+      acc += bias ? (double)bias[n] : 0.0;
       Y[i * n_cols + j] = acc;
       if (absdot) absdot[i * n_cols + j] = mag;
     }
