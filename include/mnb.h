@@ -332,6 +332,42 @@ MNB_API mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float 
                                       mnb_stream_t stream);
 
 /*
+ * The bitsandbytes-style 4-bit matrix (page "Qwen3 CPU Inference Critical
+ * Path", com.microsoft operator inventory, row MatMulBnb4: an alternative
+ * bitsandbytes-style 4-bit matrix format, adapted into the same weight-only
+ * plan). The pages name the format only; this library reads it as:
+ *   B       uint8 [(N*K + 1) / 2] DEVICE: the N x K weight (row n = output
+ *           n) flattened row-major, two codes per byte, the first of each
+ *           pair in the HIGH nibble;
+ *   absmax  [N*K / block_size] DEVICE, fp32 or bf16 (absmax_dtype): one
+ *           scale per block_size consecutive flattened elements;
+ *   code    fp32 [16] DEVICE: the code book (NF4, FP4 or any other);
+ *   w[n,k]  = code[q] * absmax[(n*K + k) / block_size]
+ *   Y[m,n]  = sum_k A[m,k] w[n,k] + bias[n]
+ * K must be a multiple of block_size (a block may not straddle two rows of
+ * the plan), and block_size a power of two in [16, 256].
+ *
+ * mnb_prepack_bnb4 re-lays out B and absmax into the packed plan (codes as
+ * mnb_prepack's, absmax as its scales; sizes from mnb_prepacked_sizes with
+ * no zero points). Errors: as mnb_prepack; MNB_ERR_UNSUPPORTED when K is
+ * not a multiple of block_size.
+ *
+ * mnb_matmul_bnb4 runs the decode kernel with the code book (over 8-row
+ * slices beyond 8 rows): each CTA turns the 16 values into a table of
+ * bf16 pairs, so every weight is code[q] rounded to bf16 (within 2^-9) times
+ * the fp32 or bf16 absmax applied in fp32. Errors: as mnb_matmul;
+ * MNB_ERR_NULL for code; MNB_ERR_ALIAS if Y overlaps code.
+ */
+MNB_API mnb_status mnb_prepack_bnb4(const uint8_t *B, const void *absmax, int64_t N,
+                                    int64_t K, int block_size, mnb_dtype absmax_dtype,
+                                    void *packed_b, void *packed_scales, mnb_stream_t stream);
+MNB_API mnb_status mnb_matmul_bnb4(const void *A, const void *packed_b,
+                                   const void *packed_scales, const float *code,
+                                   const float *bias, int64_t M, int64_t N, int64_t K,
+                                   int block_size, void *Y, mnb_dtype a_dtype,
+                                   mnb_dtype absmax_dtype, mnb_stream_t stream);
+
+/*
  * Decode chain: a sequence of MatMulNBits projections with declared data
  * dependencies, run as ONE persistent cooperative kernel launch.
  *

@@ -26,7 +26,7 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_matmul_path", "mnb_matmul_from_host",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
            "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc",
-           "mnb_matmul_rmsnorm")
+           "mnb_matmul_rmsnorm", "mnb_prepack_bnb4", "mnb_matmul_bnb4")
 
 _lock = threading.Lock()
 _lib = None
@@ -125,6 +125,10 @@ def load(build_if_missing: bool = False):
         lib.mnb_matmul_rmsnorm.argtypes = [p, i32, p, ctypes.c_float, p, p, p, p, i64, i64,
                                            i64, i32, p, p, i32, i32, p]
         lib.mnb_matmul_rmsnorm.restype = i32
+        lib.mnb_prepack_bnb4.argtypes = [p, p, i64, i64, i32, i32, p, p, p]
+        lib.mnb_prepack_bnb4.restype = i32
+        lib.mnb_matmul_bnb4.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32, i32, p]
+        lib.mnb_matmul_bnb4.restype = i32
         _lib = lib
         return lib
 
@@ -465,3 +469,39 @@ def mnb_matmul_rmsnorm(A: torch.Tensor, w: PackedWeight, bias: torch.Tensor | No
         _ptr(Y), _ptr(idx), _dtype_code(A.dtype), _dtype_code(w.scale_dtype), _stream(stream)),
         "mnb_matmul_rmsnorm")
     return Y, idx
+
+
+def mnb_prepack_bnb4(B: torch.Tensor, absmax: torch.Tensor, N: int, K: int, block_size: int,
+                     *, stream=None) -> PackedWeight:
+    """Re-lay out a bitsandbytes-style 4-bit matrix (flattened N x K codes,
+    first of a pair in the high nibble; absmax per block_size flattened
+    elements) into the packed plan; K must be a multiple of block_size."""
+    if B.dtype != torch.uint8 or not B.is_cuda or not absmax.is_cuda:
+        raise ValueError("B must be a CUDA uint8 tensor and absmax a CUDA tensor")
+    b, s, _ = mnb_prepacked_sizes(N, K, block_size, absmax.dtype, False)
+    pb = torch.empty(b, dtype=torch.uint8, device=B.device)
+    ps = torch.empty(s // absmax.element_size(), dtype=absmax.dtype, device=B.device)
+    _check(load().mnb_prepack_bnb4(_ptr(B), _ptr(absmax.contiguous()), N, K, block_size,
+                                   _dtype_code(absmax.dtype), _ptr(pb), _ptr(ps),
+                                   _stream(stream)), "mnb_prepack_bnb4")
+    return PackedWeight(pb, ps, None, N, K, block_size, absmax.dtype)
+
+
+def mnb_matmul_bnb4(A: torch.Tensor, w: PackedWeight, code: torch.Tensor,
+                    bias: torch.Tensor | None = None, *, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Y = A @ (code[q] * absmax)^T + bias for a packed bitsandbytes-style
+    weight; code: the 16 fp32 code-book values (CUDA)."""
+    if A.dim() != 2 or A.shape[1] != w.K or not A.is_cuda or not A.is_contiguous():
+        raise ValueError(f"A must be a contiguous CUDA [M, {w.K}] tensor")
+    if code.dtype != torch.float32 or code.numel() != 16 or not code.is_cuda:
+        raise ValueError("code must be 16 fp32 values on the GPU")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty(M, w.N, dtype=A.dtype, device=A.device)
+    _check(load().mnb_matmul_bnb4(_ptr(A), _ptr(w.packed_b), _ptr(w.packed_scales),
+                                  _ptr(code.contiguous()), _ptr(bias), M, w.N, w.K,
+                                  w.block_size, _ptr(out), _dtype_code(A.dtype),
+                                  _dtype_code(w.scale_dtype), _stream(stream)),
+           "mnb_matmul_bnb4")
+    return out

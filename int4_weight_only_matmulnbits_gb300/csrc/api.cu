@@ -633,6 +633,84 @@ mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
   return MNB_OK;
 }
 
+mnb_status mnb_prepack_bnb4(const uint8_t *B, const void *absmax, int64_t N, int64_t K,
+                            int block_size, mnb_dtype absmax_dtype, void *packed_b,
+                            void *packed_scales, mnb_stream_t stream) {
+  if (!B || !absmax || !packed_b || !packed_scales) return MNB_ERR_NULL;
+  mnb_status st = check_shape(N, K, block_size, absmax_dtype);
+  if (st != MNB_OK) return st;
+  if (K % block_size != 0) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "mnb_prepack_bnb4: K=%lld is not a multiple of block_size=%d (blocks "
+                  "would straddle rows)",
+                  (long long)K, block_size);
+    return MNB_ERR_UNSUPPORTED;
+  }
+  if (!aligned(packed_b, 16) || !aligned(packed_scales, 16) ||
+      !aligned(absmax, dtype_size(absmax_dtype)))
+    return MNB_ERR_ALIGN;
+  const int64_t nb = K / block_size;
+  const Sizes out = packed_sizes(N, K, block_size, absmax_dtype, false);
+  const void *const ins[3] = {B, absmax, nullptr};
+  const size_t in_n[3] = {size_t((N * K + 1) / 2), size_t(N) * nb * dtype_size(absmax_dtype),
+                          0};
+  void *const outs[3] = {packed_b, packed_scales, nullptr};
+  const size_t out_n[3] = {out.b, out.s, 0};
+  st = check_outputs_disjoint(outs, out_n, ins, in_n);
+  if (st != MNB_OK) return st;
+  st = check_device();
+  if (st != MNB_OK) return st;
+  PrepackArgs a{B, absmax, nullptr, N, K, block_size, absmax_dtype == MNB_F32, packed_b,
+                packed_scales, nullptr};
+  a.bnb4 = true;
+  const cudaError_t e = launch_prepack(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_prepack_bnb4");
+  return MNB_OK;
+}
+
+mnb_status mnb_matmul_bnb4(const void *A, const void *packed_b, const void *packed_scales,
+                           const float *code, const float *bias, int64_t M, int64_t N,
+                           int64_t K, int block_size, void *Y, mnb_dtype a_dtype,
+                           mnb_dtype absmax_dtype, mnb_stream_t stream) {
+  if (!code) return MNB_ERR_NULL;
+  if (!aligned(code, 4)) return MNB_ERR_ALIGN;
+  mnb_status st = validate_matmul(A, packed_b, packed_scales, nullptr, bias, M, N, K,
+                                  block_size, Y, a_dtype, absmax_dtype, MNB_PATH_AUTO);
+  if (st != MNB_OK) return st;
+  if (overlap(Y, size_t(M) * N * dtype_size(a_dtype), code, 64)) return MNB_ERR_ALIAS;
+  const size_t es = dtype_size(a_dtype);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The decode kernel in code-book mode, over 8-row slices.
+  constexpr int64_t kRows = kGemvMaxM / 2;
+  for (int64_t m0 = 0; m0 < M; m0 += kRows) {
+    GroupArgs g{};
+    g.A = static_cast<const char *>(A) + size_t(m0) * K * es;
+    g.count = 1;
+    g.packed_b[0] = packed_b;
+    g.scales[0] = packed_scales;
+    g.bias[0] = bias;
+    g.Y[0] = static_cast<char *>(Y) + size_t(m0) * N * es;
+    g.N[0] = N;
+    g.M = std::min<int64_t>(kRows, M - m0);
+    g.K = K;
+    g.bs = block_size;
+    g.a_f32 = a_dtype == MNB_F32;
+    g.scale_f32 = absmax_dtype == MNB_F32;
+    g.has_zp = false;
+    g.pdl = g_pdl.load() != 0;
+    g.code = code;
+    const cudaError_t e = launch_gemv_group(g, s);
+    if (e == cudaErrorNotSupported) {
+      std::snprintf(g_last_error, sizeof g_last_error,
+                    "no code-book kernel for N=%lld K=%lld bs=%d", (long long)N, (long long)K,
+                    block_size);
+      return MNB_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_bnb4");
+  }
+  return MNB_OK;
+}
+
 mnb_status mnb_chain_build(const mnb_chain_op *ops, int32_t n_ops, int64_t M,
                            int block_size, mnb_dtype a_dtype, mnb_dtype scale_dtype,
                            void *plan, size_t plan_bytes, mnb_chain_info *info,

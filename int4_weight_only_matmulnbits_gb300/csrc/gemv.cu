@@ -96,11 +96,27 @@ struct GemvParams {
   // LM-head GEMV, and greedy ArgMax"): keys [M], or null. Y[0] may then be
   // null (logits not stored).
   unsigned long long *amax;
+  // Code-book weights (the bitsandbytes-style format): the 16 fp32 values,
+  // or null for the affine codes. Each CTA turns them into a 256-entry table
+  // of bf16 pairs (code[lo], code[hi]) indexed by two codes.
+  const float *code;
   int st_sc, st_zp;  // offsets of scales and zero points in a stage (128-aligned)
   int nbs, nps;      // blocks and zero-point word pairs per stage and tile
   int off_alo, off_s, off_red, off_part, off_bar, off_ring;
   int off_nrm;  // r[m] and the ArgMax keys (norm or amax)
+  int off_lut;  // the code-book pair table (code)
 };
+
+// Four bf16x2 registers of eight codes through the pair table: register i
+// takes the codes at bits 4i and 16 + 4i, as codes_to_bf16x2 does.
+__device__ __forceinline__ void codes_to_lut(uint32_t w, const uint32_t *pair,
+                                             uint32_t (&r)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t x = w >> (4 * i);
+    r[i] = pair[(x & 0xFu) | ((x >> 12) & 0xF0u)];
+  }
+}
 
 // ArgMax key of output (v, n): larger keys for larger v (an order-preserving
 // map of the fp32 bits) and, among equal v, for smaller n.
@@ -197,7 +213,7 @@ __device__ __forceinline__ void store_gate_up(const GemvParams &p, int m, int n,
         static_cast<uint16_t>(bf16_bits(v));
 }
 
-template <int MT, int BS, bool HAS_ZP, bool SF32>
+template <int MT, int BS, bool HAS_ZP, bool SF32, bool CODE>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     gemv_kernel(const __grid_constant__ GemvParams p) {
   using G = BlockGeom<BS>;
@@ -209,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   float *sRed = reinterpret_cast<float *>(smem + p.off_red);
   float *sPart = reinterpret_cast<float *>(smem + p.off_part);
   float *sNrm = reinterpret_cast<float *>(smem + p.off_nrm);
+  uint32_t *sPair = reinterpret_cast<uint32_t *>(smem + p.off_lut);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
   uint64_t *empty = full + kMaxStages;
   uint64_t *abar = empty + kMaxStages;  // activation copy
@@ -336,6 +353,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     bool fault = false;
     if (p.amax && tid < kGemvMaxM)
       reinterpret_cast<unsigned long long *>(sNrm + kGemvMaxM)[tid] = 0ull;
+    if (CODE && tid < 256)
+      sPair[tid] = bf16_bits(__ldg(p.code + (tid & 15))) |
+                   (bf16_bits(__ldg(p.code + (tid >> 4))) << 16);
     if (p.norm) {
       // r[m] from the whole row (this CTA may stage only part of K): per-warp
       // partial sums of squares, then a fixed-order sum over the warps.
@@ -509,7 +529,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         // Blocks past the last real one arrive zero-filled: scale 0.
         auto correct = [&](int b, float (&d)[MT][4]) {
           const int bi = b - b0s;
-          float s0, s1, z0 = 136.f, z1 = 136.f;
+          // Affine codes arrive as 128 + q: remove (128 + z) S. Code-book
+          // values are the weights themselves: nothing to remove.
+          float s0, s1, z0 = CODE ? 0.f : 136.f, z1 = z0;
           if (SF32) {
             const float *sc = reinterpret_cast<const float *>(st + sofs) + bi * kTileN + g;
             s0 = sc[0];
@@ -540,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         // step of a block starts its sums from zero.
         auto kstep = [&](uint32_t w, int ci, int jj, bool first, float (&d)[MT][4]) {
           uint32_t wf[4];
-          codes_to_bf16x2(w, wf);
+          if (CODE) codes_to_lut(w, sPair, wf);
+          else codes_to_bf16x2(w, wf);
           const int ko = ci * kChunkK + 16 * jj;
           if (mok0) bfrag0 = *reinterpret_cast<const uint2 *>(ap0 + ko);
           if (first) mma_bf16_16816_zero(d[0], wf, bfrag0.x, bfrag0.y);
@@ -795,6 +818,8 @@ bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   if (cluster > 1) off += align16(size_t(tpc) * kTileN * a.M * 4);
   L.off_nrm = static_cast<int>(off);
   off += align16(kGemvMaxM * 4 + kGemvMaxM * 8);  // r[m], then the ArgMax keys
+  L.off_lut = static_cast<int>(off);
+  off += 256 * 4;  // code-book pair table
   L.off_bar = static_cast<int>(off);
   off += (2 * kMaxStages + 1) * 8;
   off = align128(off);
@@ -825,10 +850,10 @@ bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   return true;
 }
 
-template <int MT, int BS, bool HAS_ZP, bool SF32>
+template <int MT, int BS, bool HAS_ZP, bool SF32, bool CODE = false>
 cudaError_t launch_one(const GemvParams &p, const Choice &ch, int grid, bool pdl,
                        cudaStream_t stream) {
-  auto kernel = gemv_kernel<MT, BS, HAS_ZP, SF32>;
+  auto kernel = gemv_kernel<MT, BS, HAS_ZP, SF32, CODE>;
   static bool configured = false;
   if (!configured) {
     const cudaError_t e = cudaFuncSetAttribute(
@@ -863,6 +888,13 @@ cudaError_t launch_one(const GemvParams &p, const Choice &ch, int grid, bool pdl
 template <int MT, int BS>
 cudaError_t launch_flags(const GemvParams &p, const Choice &ch, int grid, bool has_zp,
                          bool sf32, bool pdl, cudaStream_t stream) {
+  if (p.code) {  // code-book weights carry no zero points; up to 8 rows per launch
+    if constexpr (MT == 1)
+      return sf32 ? launch_one<MT, BS, false, true, true>(p, ch, grid, pdl, stream)
+                  : launch_one<MT, BS, false, false, true>(p, ch, grid, pdl, stream);
+    else
+      return cudaErrorNotSupported;
+  }
   if (has_zp)
     return sf32 ? launch_one<MT, BS, true, true>(p, ch, grid, pdl, stream)
                 : launch_one<MT, BS, true, false>(p, ch, grid, pdl, stream);
@@ -982,6 +1014,7 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   p.a_f32 = a.a_f32;
   const int vec_elems = a.a_f32 ? 4 : 8;
   p.a_vec = (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) && (a.K % vec_elems == 0);
+  p.code = a.code;
   p.norm = a.norm ? 1 : 0;
   p.gamma = a.gamma;
   p.eps = a.eps;

@@ -20,6 +20,9 @@ struct PrepackArgs {
   bool scale_f32;
   void *packed_b, *packed_scales, *packed_zp;
   int qdq_axis = -1;  // -1: MatMulNBits storage; 0 / 1: QDQ UINT4 [K,N] / [N,K]
+  // The bitsandbytes-style storage (flattened N x K codes, first of a pair
+  // high; absmax [N * K / bs] read as [N, nb] scales, K a multiple of bs).
+  bool bnb4 = false;
 };
 
 struct UnprepackArgs {
@@ -76,6 +79,10 @@ struct GroupArgs {
   // Greedy ArgMax keys [M] over weight 0's outputs (zeroed by the caller;
   // launch_argmax_finalize turns them into indices). Y[0] may be null.
   unsigned long long *amax = nullptr;
+  // Code-book weights (the bitsandbytes-style format): w = code[q] * s with
+  // code the 16 fp32 values here (rounded to bf16 for the products), no
+  // zero points. Null: the affine MatMulNBits codes.
+  const float *code = nullptr;
 };
 cudaError_t launch_argmax_init(unsigned long long *amax, int M, cudaStream_t stream);
 cudaError_t launch_argmax_finalize(unsigned long long *amax, int M, bool pdl,

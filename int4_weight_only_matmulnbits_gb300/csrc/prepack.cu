@@ -46,6 +46,21 @@ struct QdqCodes {
   }
 };
 
+// Code source for the bitsandbytes-style 4-bit matrix (page "Qwen3 CPU
+// Inference Critical Path", MatMulBnb4 row; the storage is this library's
+// reading): the N x K weight flattened row-major, two codes per byte, the
+// first of a pair in the high nibble.
+struct Bnb4Codes {
+  const uint8_t *B;
+  int64_t N, K;
+  __device__ __forceinline__ uint32_t operator()(int64_t n, int64_t k) const {
+    if (n >= N || k >= K) return 0;
+    const int64_t i = n * K + k;
+    const uint8_t byte = B[i >> 1];
+    return (i & 1) ? (byte & 0x0F) : (byte >> 4);
+  }
+};
+
 template <typename Src>
 __global__ void pack_codes_kernel(Src src, uint32_t *__restrict__ out, int64_t K64,
                                   int64_t words) {
@@ -201,7 +216,10 @@ cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream) {
   const int64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
   const int64_t words = N16 * K64 * (kChunkBytes / 4);
   const bool qdq = a.qdq_axis >= 0;
-  if (qdq)
+  if (a.bnb4)
+    pack_codes_kernel<<<grid_for(words), 256, 0, stream>>>(
+        Bnb4Codes{a.B, a.N, a.K}, static_cast<uint32_t *>(a.packed_b), K64, words);
+  else if (qdq)
     pack_codes_kernel<<<grid_for(words), 256, 0, stream>>>(
         QdqCodes{a.B, a.N, a.K, a.qdq_axis}, static_cast<uint32_t *>(a.packed_b), K64, words);
   else

@@ -250,3 +250,19 @@ def test_matmul_rmsnorm_rejects_invalid_arguments_on_host(lib):
     assert call(am=v((1 << 22) + 8)) == -6     # argmax over Y
     assert call(gamma=v(1 << 22)) == -6        # Y over gamma
     assert call(nrm=0, gamma=v(1 << 22)) in (-7, -9)  # gamma unused without normalize
+
+
+def test_bnb4_rejects_invalid_arguments_on_host(lib):
+    v = ctypes.c_void_p
+    assert lib.mnb_prepack_bnb4(None, v(1 << 16), 16, 64, 32, 0, v(1 << 20), v(1 << 21),
+                                None) == -1
+    assert lib.mnb_prepack_bnb4(v(4096), v(1 << 16), 16, 40, 16, 0, v(1 << 20), v(1 << 21),
+                                None) == -8  # K not a multiple of the block size
+    assert lib.mnb_prepack_bnb4(v(4096), v(1 << 16), 16, 64, 48, 0, v(1 << 20), v(1 << 21),
+                                None) == -3
+    assert lib.mnb_prepack_bnb4(v(4096), v(1 << 16), 16, 64, 32, 0, v((1 << 20) + 8),
+                                v(1 << 21), None) == -5
+    assert lib.mnb_matmul_bnb4(v(16), v(256), v(256), None, None, 1, 16, 64, 32, v(1 << 20),
+                               0, 0, None) == -1
+    assert lib.mnb_matmul_bnb4(v(16), v(256), v(256), v(2), None, 1, 16, 64, 32, v(1 << 20),
+                               0, 0, None) == -5

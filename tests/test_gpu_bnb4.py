@@ -1,0 +1,97 @@
+"""GPU parity of the bitsandbytes-style 4-bit adapter (mnb_prepack_bnb4,
+mnb_matmul_bnb4) against the oracle's statement (oracle.bnb4_matmul), through
+the C ABI.
+
+The code book is arbitrary (16 sorted values that are not bf16 numbers); the
+kernel rounds each code-book value to bf16 once (within 2^-9), so the
+worst-case weight error is 2^-9 |w|, inside the stated 2e-3 factor, which
+these tests apply. The re-layout itself is checked bitwise: unpacking the
+plan gives the MatMulNBits storage of the same logical codes and the absmax
+as per-row scales.
+"""
+import numpy as np
+import pytest
+import torch
+
+import int4_weight_only_matmulnbits_gb300 as mnb
+import oracle
+from tests.packing import pack_bnb4_flat, pack_codes
+from tests.tolerance import check
+
+pytestmark = pytest.mark.gpu
+
+CODE = (np.linspace(-1.0, 1.0, 16) + np.sin(np.arange(16)) * 0.013).astype(np.float32)
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mnb.build_library()
+    mnb.load()
+    return torch.device("cuda:0")
+
+
+def problem(M, N, K, bs, a_dtype, s_dtype, bias, seed):
+    rng = np.random.default_rng(seed)
+    Q = rng.integers(0, 16, size=(N, K))
+    absmax = torch.tensor(rng.uniform(0.01, 0.05, size=(N * K) // bs).astype(np.float32))
+    absmax = absmax.to(s_dtype)
+    A = torch.randn(M, K, generator=torch.Generator().manual_seed(seed)).to(a_dtype)
+    b = torch.tensor(rng.normal(0, 0.02, size=N).astype(np.float32)) if bias else None
+    return Q, absmax, A, b
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("a_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("s_dtype", [torch.float32, torch.bfloat16])
+def test_bnb4_matches_oracle(dev, bs, a_dtype, s_dtype):
+    """Ragged N, K from one block to many, M across the 8-row slices."""
+    i = 0
+    for (N, K) in ((7, bs), (129, 4 * bs), (1000, 2560 // bs * bs or bs)):
+        for M in (1, 5, 8, 17):
+            i += 1
+            Q, absmax, A, b = problem(M, N, K, bs, a_dtype, s_dtype, i % 2 == 0, 40 * bs + i)
+            w = mnb.mnb_prepack_bnb4(torch.tensor(pack_bnb4_flat(Q)).to(dev), absmax.to(dev),
+                                     N, K, bs)
+            Y = mnb.mnb_matmul_bnb4(A.to(dev), w, torch.tensor(CODE).to(dev),
+                                    None if b is None else b.to(dev))
+            torch.cuda.synchronize()
+            R, mag = oracle.bnb4_matmul(A, pack_bnb4_flat(Q), absmax, CODE, b, N=N, K=K,
+                                        block_size=bs)
+            check(Y, R, mag, f"bnb4 M{M} N{N} K{K} bs{bs}")
+
+
+@pytest.mark.parametrize("bs", [16, 64, 256])
+def test_bnb4_relayout_is_the_matmulnbits_plan_of_the_same_codes(dev, bs):
+    N, K = 37, 3 * bs
+    Q, absmax, _, _ = problem(1, N, K, bs, torch.float32, torch.float32, False, bs)
+    w = mnb.mnb_prepack_bnb4(torch.tensor(pack_bnb4_flat(Q)).to(dev), absmax.to(dev), N, K,
+                             bs)
+    B, S, Z = mnb.mnb_unprepack(w)
+    torch.cuda.synchronize()
+    assert Z is None
+    assert np.array_equal(B.cpu().numpy().reshape(-1), pack_codes(Q, bs).reshape(-1))
+    assert torch.equal(S.cpu(), absmax.reshape(N, K // bs))
+
+
+def test_qwen3_4b_lm_head_shape(dev):
+    """The LM head at full size (151936 x 2560, bs 64, bf16 A and absmax),
+    M = 1: 512 seeded columns."""
+    N, K, bs = 151936, 2560, 64
+    Q, absmax, A, _ = problem(1, N, K, bs, torch.bfloat16, torch.bfloat16, False, 9)
+    w = mnb.mnb_prepack_bnb4(torch.tensor(pack_bnb4_flat(Q)).to(dev), absmax.to(dev), N, K,
+                             bs)
+    Y = mnb.mnb_matmul_bnb4(A.to(dev), w, torch.tensor(CODE).to(dev))
+    torch.cuda.synchronize()
+    cols = np.sort(np.random.default_rng(1).choice(N, 512, replace=False))
+    R, mag = oracle.bnb4_matmul(A, pack_bnb4_flat(Q), absmax, CODE, None, N=N, K=K,
+                                block_size=bs, cols=cols)
+    check(Y[:, cols], R, mag, "bnb4 lm_head")
+
+
+def test_blocks_straddling_rows_are_refused(dev):
+    B = torch.zeros((16 * 40 + 1) // 2, dtype=torch.uint8, device=dev)
+    absmax = torch.ones(16 * 40 // 16, device=dev)
+    with pytest.raises(mnb.MnbError) as e:
+        mnb.mnb_prepack_bnb4(B, absmax, 16, 40, 16)
+    assert e.value.status == -8
