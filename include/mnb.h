@@ -62,7 +62,10 @@ typedef enum { MNB_F32 = 0, MNB_BF16 = 1 } mnb_dtype;
 typedef enum {
   MNB_PATH_AUTO = 0, /* small-M kernel for M <= 16, tensor-core GEMM above */
   MNB_PATH_GEMV = 1, /* split-K decode kernel (M <= 16)                    */
-  MNB_PATH_GEMM = 2  /* TMA + tcgen05/TMEM prefill kernel (any M)          */
+  MNB_PATH_GEMM = 2, /* TMA + tcgen05/TMEM prefill kernel (any M)          */
+  MNB_PATH_GEMM_STREAMK = 3 /* the same kernel's stream-K schedule: bf16
+                               activations, a single weight and a workspace
+                               (mnb_matmul_ws), else MNB_ERR_UNSUPPORTED     */
 } mnb_path;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -201,6 +204,48 @@ MNB_API mnb_status mnb_matmul_path(const void *A, const void *packed_b,
                                    int64_t K, int block_size, void *Y,
                                    mnb_dtype a_dtype, mnb_dtype scale_dtype,
                                    mnb_path path, mnb_stream_t stream);
+
+/*
+ * Bytes of workspace that let mnb_matmul_ws run its stream-K schedule on the
+ * current device (0 when no usable device is current): a 4096-byte page of
+ * counters, then two 256 x 128 fp32 partial tiles (256 KiB) for each CTA of
+ * the grid, two CTAs per SM.
+ */
+MNB_API size_t mnb_matmul_workspace_size(void);
+
+/*
+ * mnb_matmul with the path chosen as in mnb_matmul_path and a caller-owned
+ * device workspace. With M > 16 and bf16 activations on a single weight, the
+ * tensor-core path may then split the product's (output tile, 64-wide k
+ * stage) units evenly over two CTAs per SM instead of giving each CTA a
+ * whole tile, where its cost model expects that to be faster: shapes whose
+ * 256 x 128 tiles leave SMs idle (few output tiles, or just more than the
+ * resident CTAs can take at once). A tile that several CTAs share is
+ * completed by whichever of them finishes last, adding the fp32 partial sums
+ * in the order of their k stages; no CTA waits for another. Results are
+ * bitwise reproducible for a given device and shape, and within the same
+ * bound as mnb_matmul. The pages
+ * describe no such schedule (their kernels run on CPU cores); the operation
+ * computed is unchanged.
+ *  workspace: NULL (then exactly mnb_matmul_path), or device memory of
+ *    workspace_bytes bytes, 256-byte aligned, overlapping no input or output.
+ *    Its first 4096 bytes (the counters) must be zero before the first call
+ *    that uses it; every call leaves them zero again, unless
+ *    mnb_fault_status reports a fault, after which the caller zeroes them
+ *    before the next call. One workspace serves calls that are ordered one
+ *    after another (one stream, or a CUDA graph); concurrent calls need
+ *    their own. A workspace smaller than mnb_matmul_workspace_size() limits
+ *    the grid (one CTA per 256 KiB); one of 4096 bytes or less is not used.
+ * Errors: as mnb_matmul_path; MNB_ERR_ALIGN (workspace alignment),
+ * MNB_ERR_ALIAS (workspace overlaps an input or Y).
+ */
+MNB_API mnb_status mnb_matmul_ws(const void *A, const void *packed_b,
+                                 const void *scales, const void *zero_points,
+                                 const float *bias, int64_t M, int64_t N,
+                                 int64_t K, int block_size, void *Y,
+                                 mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                 mnb_path path, void *workspace,
+                                 size_t workspace_bytes, mnb_stream_t stream);
 
 /*
  * Fused-N projections: Y_i = A * dequant(B_i)^T + bias_i for i < count

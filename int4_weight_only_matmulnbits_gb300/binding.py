@@ -17,8 +17,9 @@ import torch
 from . import _build
 
 MNB_OK = 0
+MNB_ERR_DEVICE = -9
 MNB_F32, MNB_BF16 = 0, 1
-MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2}
+MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_streamk": 3}
 
 # Every entry point include/mnb.h declares.
 EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
@@ -26,7 +27,8 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_matmul_path", "mnb_matmul_from_host",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
            "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc",
-           "mnb_matmul_rmsnorm", "mnb_prepack_bnb4", "mnb_matmul_bnb4")
+           "mnb_matmul_rmsnorm", "mnb_prepack_bnb4", "mnb_matmul_bnb4",
+           "mnb_matmul_workspace_size", "mnb_matmul_ws")
 
 _lock = threading.Lock()
 _lib = None
@@ -104,6 +106,11 @@ def load(build_if_missing: bool = False):
         lib.mnb_matmul_path.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32,
                                         i32, i32, p]
         lib.mnb_matmul_path.restype = i32
+        lib.mnb_matmul_workspace_size.argtypes = []
+        lib.mnb_matmul_workspace_size.restype = sz
+        lib.mnb_matmul_ws.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32, i32, i32, p,
+                                      sz, p]
+        lib.mnb_matmul_ws.restype = i32
         lib.mnb_matmul_from_host.argtypes = [p, p, p, p, p, p, i64, i64, i64, i32,
                                              p, p, i32, i32, p]
         lib.mnb_matmul_from_host.restype = i32
@@ -258,10 +265,41 @@ def mnb_unprepack(w: PackedWeight, *, stream=None):
     return B, S, Z
 
 
+def mnb_matmul_workspace(device=None) -> torch.Tensor:
+    """A zero-filled workspace for mnb_matmul's stream-K schedule on `device`
+    (mnb_matmul_workspace_size() bytes). Calls that use one must be ordered
+    one after another (one stream, or a CUDA graph)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    with torch.cuda.device(dev):
+        n = load().mnb_matmul_workspace_size()
+    if n == 0:
+        raise MnbError(MNB_ERR_DEVICE, "mnb_matmul_workspace", "no usable CUDA device")
+    return torch.zeros(n, dtype=torch.uint8, device=dev)
+
+
+# One workspace per (device, stream): calls on one stream run one after another.
+_workspaces: dict = {}
+
+
+def _default_workspace(A: torch.Tensor, stream) -> torch.Tensor:
+    s = torch.cuda.current_stream(A.device) if stream is None else stream
+    key = (A.device.index, s.cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = _workspaces[key] = mnb_matmul_workspace(A.device)
+    return ws
+
+
 def mnb_matmul(A: torch.Tensor, w: PackedWeight, bias: torch.Tensor | None = None, *,
-               out: torch.Tensor | None = None, path: str = "auto",
+               out: torch.Tensor | None = None, path: str = "auto", workspace="auto",
                stream=None) -> torch.Tensor:
-    """Y[M, N] = A[M, K] @ dequant(w)^T + bias, on the GPU."""
+    """Y[M, N] = A[M, K] @ dequant(w)^T + bias, on the GPU.
+
+    workspace: "auto" (above 16 rows: a zero-filled workspace kept per device
+    and stream, which lets the tensor-core kernel use its stream-K schedule
+    where that is faster), None (no workspace: whole-tile CTAs only), or a
+    tensor from mnb_matmul_workspace()."""
     if A.dim() != 2 or A.shape[1] != w.K:
         raise ValueError(f"A must be [M, {w.K}]")
     if not A.is_cuda or not A.is_contiguous():
@@ -271,11 +309,18 @@ def mnb_matmul(A: torch.Tensor, w: PackedWeight, bias: torch.Tensor | None = Non
         out = torch.empty(M, w.N, dtype=A.dtype, device=A.device)
     if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
         raise ValueError("bias must be a CUDA float32 tensor")
-    _check(load().mnb_matmul_path(_ptr(A), _ptr(w.packed_b), _ptr(w.packed_scales),
-                                  _ptr(w.packed_zp), _ptr(bias), M, w.N, w.K,
-                                  w.block_size, _ptr(out), _dtype_code(A.dtype),
-                                  _dtype_code(w.scale_dtype), MNB_PATH[path],
-                                  _stream(stream)), "mnb_matmul")
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be "auto", None or a tensor')
+        workspace = _default_workspace(A, stream) if M > 16 and path != "gemv" else None
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().mnb_matmul_ws(_ptr(A), _ptr(w.packed_b), _ptr(w.packed_scales),
+                                _ptr(w.packed_zp), _ptr(bias), M, w.N, w.K,
+                                w.block_size, _ptr(out), _dtype_code(A.dtype),
+                                _dtype_code(w.scale_dtype), MNB_PATH[path],
+                                _ptr(workspace), ws_bytes, _stream(stream)), "mnb_matmul")
     return out
 
 

@@ -99,17 +99,19 @@ mnb_status check_outputs_disjoint(void *const outs[3], const size_t out_n[3],
   return MNB_OK;
 }
 
-mnb_status validate_matmul(const void *A, const void *packed_b,
-                           const void *scales, const void *zero_points,
-                           const float *bias, int64_t M, int64_t N, int64_t K,
-                           int block_size, const void *Y, int a_dtype,
-                           int scale_dtype, int path) {
+// Argument checks of a product (no device query).
+mnb_status validate_matmul_args(const void *A, const void *packed_b,
+                                const void *scales, const void *zero_points,
+                                const float *bias, int64_t M, int64_t N, int64_t K,
+                                int block_size, const void *Y, int a_dtype,
+                                int scale_dtype, int path) {
   if (!A || !packed_b || !scales || !Y) return MNB_ERR_NULL;
   if (M < 1 || M > kMaxDim) return MNB_ERR_SHAPE;
   mnb_status st = check_shape(N, K, block_size, scale_dtype);
   if (st != MNB_OK) return st;
   if (!valid_dtype(a_dtype)) return MNB_ERR_DTYPE;
-  if (path != MNB_PATH_AUTO && path != MNB_PATH_GEMV && path != MNB_PATH_GEMM)
+  if (path != MNB_PATH_AUTO && path != MNB_PATH_GEMV && path != MNB_PATH_GEMM &&
+      path != MNB_PATH_GEMM_STREAMK)
     return MNB_ERR_UNSUPPORTED;
   if (path == MNB_PATH_GEMV && M > kGemvMaxM) return MNB_ERR_UNSUPPORTED;
   const size_t es = dtype_size(a_dtype);
@@ -124,20 +126,33 @@ mnb_status validate_matmul(const void *A, const void *packed_b,
                           bias ? size_t(N) * 4 : 0};
   for (int j = 0; j < 5; ++j)
     if (overlap(Y, y_bytes, ins[j], in_n[j])) return MNB_ERR_ALIAS;
-  return check_device();
+  return MNB_OK;
+}
+
+mnb_status validate_matmul(const void *A, const void *packed_b,
+                           const void *scales, const void *zero_points,
+                           const float *bias, int64_t M, int64_t N, int64_t K,
+                           int block_size, const void *Y, int a_dtype,
+                           int scale_dtype, int path) {
+  const mnb_status st = validate_matmul_args(A, packed_b, scales, zero_points, bias, M, N,
+                                             K, block_size, Y, a_dtype, scale_dtype, path);
+  return st != MNB_OK ? st : check_device();
 }
 
 mnb_status run_matmul(const void *A, const void *packed_b, const void *scales,
                       const void *zero_points, const float *bias, int64_t M,
                       int64_t N, int64_t K, int block_size, void *Y,
                       int a_dtype, int scale_dtype, int path,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, void *ws = nullptr, size_t ws_bytes = 0) {
   MatmulArgs a{A, packed_b, scales, zero_points, bias, Y, M, N, K, block_size,
                a_dtype == MNB_F32, scale_dtype == MNB_F32, g_pdl.load() != 0};
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.sk_only = path == MNB_PATH_GEMM_STREAMK;
   cudaError_t e;
   if (path == MNB_PATH_GEMV || (path == MNB_PATH_AUTO && M <= kGemvMaxM)) {
     e = launch_gemv(a, stream);
-  } else if (path == MNB_PATH_GEMM || gemm_supports(a)) {
+  } else if (path == MNB_PATH_GEMM || path == MNB_PATH_GEMM_STREAMK || gemm_supports(a)) {
     e = launch_gemm(a, stream);
   } else {
     // Activations the tensor-core kernel cannot stage (fp32, or rows that
@@ -385,6 +400,36 @@ mnb_status mnb_matmul_path(const void *A, const void *packed_b,
   return run_matmul(A, packed_b, scales, zero_points, bias, M, N, K,
                     block_size, Y, a_dtype, scale_dtype, path,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t mnb_matmul_workspace_size(void) {
+  if (check_device() != MNB_OK) return 0;
+  return gemm_workspace_bytes();
+}
+
+mnb_status mnb_matmul_ws(const void *A, const void *packed_b, const void *scales,
+                         const void *zero_points, const float *bias, int64_t M,
+                         int64_t N, int64_t K, int block_size, void *Y,
+                         mnb_dtype a_dtype, mnb_dtype scale_dtype, mnb_path path,
+                         void *workspace, size_t workspace_bytes, mnb_stream_t stream) {
+  mnb_status st = validate_matmul_args(A, packed_b, scales, zero_points, bias, M, N, K,
+                                       block_size, Y, a_dtype, scale_dtype, path);
+  if (st != MNB_OK) return st;
+  if (workspace) {
+    if (!aligned(workspace, 256)) return MNB_ERR_ALIGN;
+    const size_t es = dtype_size(a_dtype);
+    const Sizes in = packed_sizes(N, K, block_size, scale_dtype, zero_points != nullptr);
+    const void *others[6] = {A, packed_b, scales, zero_points, bias, Y};
+    const size_t on[6] = {size_t(M) * K * es, in.b, in.s, in.z, bias ? size_t(N) * 4 : 0,
+                          size_t(M) * N * es};
+    for (int j = 0; j < 6; ++j)
+      if (overlap(workspace, workspace_bytes, others[j], on[j])) return MNB_ERR_ALIAS;
+  }
+  st = check_device();
+  if (st != MNB_OK) return st;
+  return run_matmul(A, packed_b, scales, zero_points, bias, M, N, K, block_size, Y,
+                    a_dtype, scale_dtype, path, reinterpret_cast<cudaStream_t>(stream),
+                    workspace, workspace ? workspace_bytes : 0);
 }
 
 mnb_status mnb_matmul(const void *A, const void *packed_b, const void *scales,

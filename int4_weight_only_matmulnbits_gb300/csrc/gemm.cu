@@ -72,6 +72,14 @@ struct GemmParams {
   CUtensorMap tms;  // scales: {16 scales as words, nb, N16}, box {.., bpc, 8}
   CUtensorMap tmz;  // zero points: {4 words, nbz/2, N16}, box {4, ppc, 8}
   CUtensorMap tmw2, tms2, tmz2;  // a pair's up weight (boxes of 4 tiles, as the gate's)
+  // Stream-K schedule (gemm_sk_kernel): units = tiles * K64 (tile, k stage)
+  // pairs split evenly over sk_ctas CTAs; tiles_n output tiles along N; ws
+  // holds two 256 x 128 fp32 partial tiles per CTA (its first and its last
+  // piece), count one arrival counter per CTA (for the split tile it heads).
+  int64_t units;
+  int sk_ctas, tiles_n;
+  float *ws;
+  unsigned int *count;
   const float *bias, *bias2;
   void *Y;
   int M, N, K64;
@@ -111,7 +119,8 @@ struct Smem {
   static constexpr int kZp = kSc + kWStages * kScBytes;
   static constexpr int kBias = kZp + kWStages * kZpBytes;
   static constexpr int kBar = kBias + kBN * 4;
-  static constexpr int kNumBars = 2 * kAStages + 2 * kWStages + 2 * kBStages + 1;
+  // ... + acc_full, and acc_empty (the stream-K kernel's drained accumulator)
+  static constexpr int kNumBars = 2 * kAStages + 2 * kWStages + 2 * kBStages + 2;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kTotal = kTmemSlot + 16;
 };
@@ -623,6 +632,429 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   }
 }
 
+// ---- stream-K schedule for 256-row tiles -----------------------------------
+//
+// A product with few output tiles (or a tile count just above a multiple of
+// the CTA slots) leaves SMs idle in the kernel above: a CTA alone on its SM
+// runs a k stage little faster than two CTAs sharing it. Here the product's
+// T x K64 (tile, k stage) units are split evenly over two CTAs per SM: CTA c
+// takes units [c U / C, (c + 1) U / C) in tile-major order. Its range falls
+// into segments, one per tile it touches:
+//  * a whole tile is stored as the kernel above stores it;
+//  * a tile split over several CTAs has a head (the CTA holding k stage 0,
+//    whose segment is the last of its range) and contributors (CTAs whose
+//    ranges start inside the tile: their first segments). Each piece parks
+//    its fp32 partial tile in the workspace and counts itself in on the
+//    tile's counter (acq_rel); the piece that arrives last adds all partial
+//    tiles in k order (the head's first), adds the bias, stores the tile and
+//    clears the counter. A head that finds every contribution already in
+//    (the usual case: it reaches its last segment late) adds them to its
+//    accumulators directly and parks nothing.
+// The sums run in one fixed order whichever piece completes the tile, so
+// results are bitwise reproducible. No CTA ever waits for another. Between
+// segments the MMA thread waits until the epilogue has drained the TMEM
+// accumulators.
+
+__device__ __forceinline__ uint32_t flag_load_acquire(const unsigned int *f) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel(unsigned int *f, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(f), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void flag_store_relaxed(unsigned int *f, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+struct SkSeg {
+  int t, kb0, kb1;  // tile, k stages [kb0, kb1)
+};
+__device__ __forceinline__ int64_t sk_lo(const GemmParams &p, int c) {
+  return int64_t(c) * p.units / p.sk_ctas;
+}
+// The segment of the range [u, hi) that starts at unit u.
+__device__ __forceinline__ SkSeg sk_seg(const GemmParams &p, int64_t u, int64_t hi) {
+  SkSeg g;
+  g.t = static_cast<int>(u / p.K64);
+  g.kb0 = static_cast<int>(u - int64_t(g.t) * p.K64);
+  const int64_t e = hi - int64_t(g.t) * p.K64;
+  g.kb1 = e < p.K64 ? static_cast<int>(e) : p.K64;
+  return g;
+}
+__device__ __forceinline__ int64_t sk_next(const GemmParams &p, const SkSeg &g) {
+  return int64_t(g.t) * p.K64 + g.kb1;
+}
+
+// 32 output values of row m (output columns n0 .. n0 + 31) as bf16.
+__device__ __forceinline__ void store_row32(const GemmParams &p, int m, int n0, const float (&o)[32]) {
+  uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
+  if (n0 + 32 <= p.N && p.y_vec) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = bf16_bits(o[i + 2 * e]) | (bf16_bits(o[i + 2 * e + 1]) << 16);
+      *reinterpret_cast<uint4 *>(yrow + n0 + i) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    for (int i = 0; i < 32; ++i)
+      if (n0 + i < p.N) yrow[n0 + i] = static_cast<uint16_t>(bf16_bits(o[i]));
+  }
+}
+
+template <int BS, bool HAS_ZP, bool SF32>
+__global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int MH = 2;
+  constexpr int kTileRows = kBH * MH;
+  using S = Smem<MH, BS, SF32>;
+  constexpr int kAStages = S::kAStages, kWStages = S::kWStages;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t *afull = reinterpret_cast<uint64_t *>(smem + S::kBar);
+  uint64_t *aempty = afull + kAStages;
+  uint64_t *wfull = aempty + kAStages;
+  uint64_t *wempty = wfull + kWStages;
+  uint64_t *bfull = wempty + kWStages;
+  uint64_t *bempty = bfull + kBStages;
+  uint64_t *acc_full = bempty + kBStages;
+  uint64_t *acc_empty = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kTmemSlot);
+  uint32_t *sh_fault = tmem_slot + 1;  // a wait ran out (epilogue warps)
+  uint32_t *sh_mode = tmem_slot + 2;   // a head parks its piece (1) or completes the tile (0)
+  uint32_t *sh_last = tmem_slot + 3;   // this CTA's piece was the tile's last
+  float *sBias = reinterpret_cast<float *>(smem + S::kBias);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  const int64_t lo = sk_lo(p, c), hi = sk_lo(p, c + 1);
+
+  if (tid == 0) {
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(afull + i, 1);
+      mbar_init(aempty + i, 1);
+    }
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(wfull + i, 1);
+      mbar_init(wempty + i, kDqWarps);
+    }
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(bfull + i, kDqWarps);
+      mbar_init(bempty + i, 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 1);
+    *sh_fault = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kBN * MH)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  bool fault = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      // A tiles of every stage of every segment.
+      int i = 0;
+      for (int64_t u = lo; u < hi && !fault;) {
+        const SkSeg g = sk_seg(p, u, hi);
+        const int m0 = (g.t / p.tiles_n) * kTileRows;
+        for (int kb = g.kb0; kb < g.kb1; ++kb, ++i) {
+          const int s = i % kAStages;
+          if (i >= kAStages && !mbar_wait(aempty + s, ((i / kAStages) - 1) & 1)) {
+            record_fault(&g_fault_gemm, kFaultGemmWait);
+            fault = true;
+            break;
+          }
+          mbar_arrive_expect_tx(afull + s, S::kATileBytes);
+          tma_load_2d(smem + S::kA + s * S::kATileBytes, &p.tma, kb * kBK, m0, afull + s);
+        }
+        u = sk_next(p, g);
+      }
+    } else if (lane == 1) {
+      // Packed weights of every stage of every segment.
+      int i = 0;
+      for (int64_t u = lo; u < hi && !fault;) {
+        const SkSeg g = sk_seg(p, u, hi);
+        const int nt0 = (g.t % p.tiles_n) * kTilesN;
+        for (int kb = g.kb0; kb < g.kb1; ++kb, ++i) {
+          const int s = i % kWStages;
+          if (i >= kWStages && !mbar_wait(wempty + s, ((i / kWStages) - 1) & 1)) {
+            record_fault(&g_fault_gemm, kFaultGemmWait);
+            fault = true;
+            break;
+          }
+          uint64_t *bar = wfull + s;
+          mbar_arrive_expect_tx(bar, kCodeBytes + p.sc_bytes + p.zp_bytes);
+          const int blk = (kb * kBK) / BS;
+          tma_load_3d(smem + S::kCodes + s * kCodeBytes, &p.tmw, 0, kb, nt0, bar);
+          tma_load_3d(smem + S::kSc + s * S::kScBytes, &p.tms, 0, blk, nt0, bar);
+          if (HAS_ZP) tma_load_3d(smem + S::kZp + s * S::kZpBytes, &p.tmz, 0, blk >> 1, nt0, bar);
+        }
+        u = sk_next(p, g);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int i = 0, j = 0;
+      for (int64_t u = lo; u < hi && !fault; ++j) {
+        const SkSeg g = sk_seg(p, u, hi);
+        // The epilogue has read the previous segment's accumulators.
+        if (j > 0 && !mbar_wait(acc_empty, (j - 1) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          fault = true;
+          break;
+        }
+        for (int kb = g.kb0; kb < g.kb1; ++kb, ++i) {
+          const int s = i % kAStages, b = i % kBStages;
+          if (!mbar_wait(afull + s, (i / kAStages) & 1) ||
+              !mbar_wait(bfull + b, (i / kBStages) & 1)) {
+            record_fault(&g_fault_gemm, kFaultGemmWait);
+            fault = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_addr(smem + S::kA + s * S::kATileBytes);
+          const uint32_t b_base = smem_addr(smem + S::kB + b * kBTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+#pragma unroll
+            for (int h = 0; h < MH; ++h)
+              umma_bf16(tmem + h * kBN, smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32),
+                        smem_desc_sw128(b_base + kk * 32), kb > g.kb0 || kk > 0);
+          umma_commit(aempty + s);
+          umma_commit(bempty + b);
+        }
+        if (fault) break;
+        umma_commit(acc_full);
+        u = sk_next(p, g);
+      }
+    }
+  } else {
+    // ---- dequantisation warps (2..9) and each segment's epilogue ----------
+    // Every warp walks the same segments and passes the same named barriers
+    // whatever happens; after a fault it only skips the work.
+    const int tile = warp - 2;
+    const int quarter = warp & 3;          // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;      // which half of the columns
+    const int dg = lane >> 2, dt = lane & 3;
+    // Weight rows g and g + 8 of the tile go to B rows 2g and 2g + 1.
+    const int r0 = tile * kTileN + 2 * dg;
+    constexpr int kBpc = BS < kBK ? kBK / BS : 1;
+    int i = 0, j = 0;
+    for (int64_t u = lo; u < hi; ++j) {
+      const SkSeg g = sk_seg(p, u, hi);
+      u = sk_next(p, g);
+      for (int kb = g.kb0; kb < g.kb1; ++kb, ++i) {
+        if (fault) continue;
+        const int s = i % kWStages, bslot = i % kBStages;
+        if (!mbar_wait(wfull + s, (i / kWStages) & 1) ||
+            (i >= kBStages && !mbar_wait(bempty + bslot, ((i / kBStages) - 1) & 1))) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          fault = true;
+          continue;
+        }
+        // As in gemm_kernel (single weight), every pointer taken from the
+        // shared array in this scope so that the accesses stay shared ones.
+        const unsigned char *codes = smem + S::kCodes + s * kCodeBytes;
+        const unsigned char *sc = smem + S::kSc + s * S::kScBytes;
+        const uint2 *zp = reinterpret_cast<const uint2 *>(smem + S::kZp + s * S::kZpBytes);
+        unsigned char *btile = smem + S::kB + bslot * kBTileBytes;
+        const int blk0 = (kb * kBK) / BS;
+        uint32_t sb0[kBpc], sb1[kBpc], zc0[kBpc], zc1[kBpc];
+        float sf0[kBpc], sf1[kBpc];
+#pragma unroll
+        for (int bi = 0; bi < kBpc; ++bi) {
+          if (SF32) {
+            const float *s4 = reinterpret_cast<const float *>(sc) + (tile * kBpc + bi) * kTileN;
+            sf0[bi] = s4[dg];
+            sf1[bi] = s4[dg + 8];
+            sb0[bi] = sb1[bi] = 0;
+          } else {
+            const uint16_t *s2 =
+                reinterpret_cast<const uint16_t *>(sc) + (tile * kBpc + bi) * kTileN;
+            sb0[bi] = s2[dg] * 0x10001u;
+            sb1[bi] = s2[dg + 8] * 0x10001u;
+            sf0[bi] = sf1[bi] = 0.f;
+          }
+          zc0[bi] = zc1[bi] = 0x43084308u;  // bf16 136 = 128 + 8
+          if (HAS_ZP) {
+            const int b = blk0 + bi;
+            const int pairs = BS < 32 ? 2 : 1;
+            const uint2 zw = zp[(tile * pairs + (BS < 32 ? bi >> 1 : 0)) * 2 + (b & 1)];
+            zc0[bi] = (0x4300u | ((zw.x >> (4 * dg)) & 15)) * 0x10001u;
+            zc1[bi] = (0x4300u | ((zw.y >> (4 * dg)) & 15)) * 0x10001u;
+          }
+        }
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + tile * kChunkBytes + lane * 16);
+        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int bi = BS < kBK ? (16 * q) / BS : 0;
+          uint32_t r[4];
+          codes_to_bf16x2(wv[q], r);
+          const uint32_t v00 = dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi]);  // row g
+          const uint32_t v02 = dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi]);
+          const uint32_t v10 = dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi]);  // row g + 8
+          const uint32_t v12 = dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi]);
+          const int k0 = 16 * q + 4 * dt;
+          const int inner = (k0 & 7) * 2;
+          *reinterpret_cast<uint2 *>(btile + r0 * 128 + (((k0 >> 3) ^ (r0 & 7)) * 16) + inner) =
+              make_uint2(v00, v02);
+          *reinterpret_cast<uint2 *>(btile + (r0 + 1) * 128 +
+                                     (((k0 >> 3) ^ ((r0 + 1) & 7)) * 16) + inner) =
+              make_uint2(v10, v12);
+        }
+        fence_async_smem();  // make the tile visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bfull + bslot);
+          mbar_arrive(wempty + s);
+        }
+      }
+
+      // ---- epilogue of the segment -----------------------------------------
+      const int m0 = (g.t / p.tiles_n) * kTileRows;
+      const int n_base = (g.t % p.tiles_n) * kBN;
+      const bool head = g.kb0 == 0, whole = head && g.kb1 == p.K64;
+      // A split tile: its head CTA (the one holding k stage 0) and the CTAs
+      // after it whose ranges start inside the tile, in the order of their
+      // k stages.
+      int ch = c, ncontrib = 0;
+      if (!whole) {
+        const int64_t t0 = int64_t(g.t) * p.K64, tend = t0 + p.K64;
+        while (sk_lo(p, ch) > t0) --ch;
+        while (ch + 1 + ncontrib < p.sk_ctas && sk_lo(p, ch + 1 + ncontrib) < tend) ++ncontrib;
+      }
+      {
+        const int e = tid - 64;
+        if (e < kBN) {
+          const int n = n_base + e;
+          sBias[e] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.f;
+        }
+      }
+      // A head whose contributions have all arrived completes the tile from
+      // its accumulators; any other piece of a split tile is parked.
+      if (head && !whole && warp == 2) {
+        if (lane == 0)
+          *sh_mode = (!fault && flag_load_acquire(p.count + c) == uint32_t(ncontrib)) ? 0u : 1u;
+        __syncwarp();
+      }
+      if (!fault && !mbar_wait(acc_full, j & 1)) {
+        record_fault(&g_fault_gemm, kFaultGemmWait);
+        fault = true;
+      }
+      if (fault) *sh_fault = 1;
+      named_barrier_sync(kBarEpi, 32 * kDqWarps);  // bias staged, mode decided
+      fault = fault || *sh_fault != 0;
+      const bool park = !whole && (!head || *sh_mode != 0u);
+      float *own = p.ws + (2 * int64_t(c) + (head ? 1 : 0)) * (kTileRows * kBN);
+      if (!fault) {
+        if (!whole && !park) fence_acq_rel_gpu();  // the contributions the acquire saw
+        tc_fence_after();
+#pragma unroll 1
+        for (int h = 0; h < MH; ++h) {
+          const int row = h * kBH + quarter * 32 + lane;  // row of the tile
+          const int m = m0 + row;
+#pragma unroll 1
+          for (int cc = half * (kBN / 64); cc < (half + 1) * (kBN / 64); ++cc) {
+            float v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + h * kBN + cc * 32, v);
+            if (park) {
+              // Column-major [accumulator column][row]: each store
+              // instruction writes 32 consecutive rows.
+#pragma unroll
+              for (int x = 0; x < 32; ++x) __stcg(own + (cc * 32 + x) * kTileRows + row, v[x]);
+            } else {
+              for (int q = 1; q <= ncontrib; ++q) {
+                const float *part = p.ws + 2 * int64_t(c + q) * (kTileRows * kBN);
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                  v[x] += __ldcg(part + (cc * 32 + x) * kTileRows + row);
+              }
+              if (m < p.M) {
+                float o[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) o[out_col(x)] = v[x] + sBias[cc * 32 + out_col(x)];
+                store_row32(p, m, n_base + cc * 32, o);
+              }
+            }
+          }
+        }
+        if (!whole && !park && tid == 64) flag_store_relaxed(p.count + c, 0u);
+      }
+      if (park) {
+        // Count this piece in; the last of the tile's pieces completes it,
+        // adding the parked partial tiles in the order of their k stages
+        // (the head's first), as a head completing from its accumulators
+        // does: the result does not depend on which piece came last.
+        __threadfence();
+        named_barrier_sync(kBarEpi, 32 * kDqWarps);  // the partial tile is written
+        if (tid == 64)
+          *sh_last = (!fault && atom_add_acq_rel(p.count + ch, 1u) == uint32_t(ncontrib)) ? 1u : 0u;
+        __syncwarp();
+        named_barrier_sync(kBarEpi, 32 * kDqWarps);
+        if (*sh_last != 0u && !fault) {
+          fence_acq_rel_gpu();
+#pragma unroll 1
+          for (int h = 0; h < MH; ++h) {
+            const int row = h * kBH + quarter * 32 + lane;
+            const int m = m0 + row;
+#pragma unroll 1
+            for (int cc = half * (kBN / 64); cc < (half + 1) * (kBN / 64); ++cc) {
+              float v[32];
+              const float *hp = p.ws + (2 * int64_t(ch) + 1) * (kTileRows * kBN);
+#pragma unroll
+              for (int x = 0; x < 32; ++x) v[x] = __ldcg(hp + (cc * 32 + x) * kTileRows + row);
+              for (int q = 1; q <= ncontrib; ++q) {
+                const float *part = p.ws + 2 * int64_t(ch + q) * (kTileRows * kBN);
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                  v[x] += __ldcg(part + (cc * 32 + x) * kTileRows + row);
+              }
+              if (m < p.M) {
+                float o[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) o[out_col(x)] = v[x] + sBias[cc * 32 + out_col(x)];
+                store_row32(p, m, n_base + cc * 32, o);
+              }
+            }
+          }
+          if (tid == 64) flag_store_relaxed(p.count + ch, 0u);
+        }
+      }
+      // The accumulators are drained: the MMA thread may start the next segment.
+      tc_fence_before();
+      named_barrier_sync(kBarEpi, 32 * kDqWarps);
+      if (tid == 64 && !fault) mbar_arrive(acc_empty);
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kBN * MH)
+                 : "memory");
+  }
+}
+
 // ---- fp32 activations: tf32 tensor-core products ---------------------------
 //
 // The same pipeline for fp32 activations, one 128 x 128 output tile per CTA:
@@ -1058,6 +1490,51 @@ cudaError_t launch_mh(const GemmParams &p, dim3 grid, int mh, bool sf32, bool pd
                  : launch_flags<BS, 1>(p, grid, sf32, pdl, stream);
 }
 
+// Stream-K workspace: a page of per-CTA arrival counters, then two
+// 256 x 128 fp32 partial tiles per CTA.
+constexpr size_t kSkCountBytes = 4096;
+constexpr size_t kSkPartBytes = size_t(2 * kBH) * kBN * 4;
+constexpr size_t kSkCtaBytes = 2 * kSkPartBytes;
+constexpr int64_t kSkMaxCtas = kSkCountBytes / 4;
+constexpr int64_t kSkMinStages = 4;  // fewer k stages per CTA do not pay for the fix-up
+
+template <int BS, bool HAS_ZP, bool SF32>
+cudaError_t sk_run(const GemmParams &p, cudaStream_t stream) {
+  auto kernel = gemm_sk_kernel<BS, HAS_ZP, SF32>;
+  const int smem = Smem<2, BS, SF32>::kTotal + 1024;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.sk_ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <int BS>
+cudaError_t sk_flags(const GemmParams &p, bool sf32, cudaStream_t stream) {
+  if (p.has_zp)
+    return sf32 ? sk_run<BS, true, true>(p, stream) : sk_run<BS, true, false>(p, stream);
+  return sf32 ? sk_run<BS, false, true>(p, stream) : sk_run<BS, false, false>(p, stream);
+}
+
+cudaError_t sk_bs(const GemmParams &p, int bs, bool sf32, cudaStream_t stream) {
+  switch (bs) {
+    case 16: return sk_flags<16>(p, sf32, stream);
+    case 32: return sk_flags<32>(p, sf32, stream);
+    case 64: return sk_flags<64>(p, sf32, stream);
+    case 128: return sk_flags<128>(p, sf32, stream);
+    case 256: return sk_flags<256>(p, sf32, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
 // CTAs resident at once for a split-K cluster size: two per SM; clusters
 // pack per GPC, which on GB300 (152 SMs) leaves 8 CTA slots unused with
 // clusters of 4 and 16 with clusters of 8 (occupancy query for this kernel's
@@ -1074,6 +1551,10 @@ cudaError_t gemm_take_fault(unsigned int *out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_fault_gemm, sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fault_gemm, &zero, sizeof(unsigned int));
   return e;
+}
+
+size_t gemm_workspace_bytes() {
+  return kSkCountBytes + size_t(2) * size_t(sm_count()) * kSkCtaBytes;
 }
 
 bool gemm_supports(const MatmulArgs &a) {
@@ -1172,6 +1653,7 @@ cudaError_t launch_gemm_tf32(const MatmulArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   if (!gemm_supports(a)) return cudaErrorNotSupported;
+  if (a.sk_only && (a.a_f32 || a.paired || !a.ws)) return cudaErrorNotSupported;
   if (a.a_f32) return launch_gemm_tf32(a, stream);
   GemmParams p{};
   const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
@@ -1186,9 +1668,9 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   // CTAs run in rounds of what can be resident at once, clusters packing per
   // GPC.
   int mh = 1, ksplit = 1;
+  const int sms = sm_count();
+  double best = 0.0;
   {
-    const int sms = sm_count();
-    double best = 0.0;
     bool have = false;
     for (int h = 1; h <= 2; ++h)
       for (int c = 1; c <= (h == 1 ? (a.paired ? 4 : 8) : 1); c *= 2) {
@@ -1209,6 +1691,39 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
         }
       }
   }
+  // Stream-K over 256-row tiles (single weights, with a workspace): every
+  // CTA takes an equal share of the (tile, k stage) units, at the 256-row
+  // stage cost, plus what GB300 measurements of the split tiles show (Qwen3
+  // prefill shapes, M = 512 to 4096): about 28 us fixed (parking partial
+  // tiles through L2, the arrival counters, the accumulator drain between
+  // segments), about 2.5 us for each further piece of a tile and about 1 us
+  // for each further tile a CTA's range touches. It wins where whole tiles
+  // leave half the CTA slots idle for long (down and o projections with
+  // M >= 2048, 4096) and loses where tiles are few or short.
+  bool sk = false;
+  int64_t sk_ctas = 0, units = 0;
+  const int64_t tiles_n = ceil_div(a.N, int64_t(kBN));
+  if (a.ws && !a.paired && a.ws_bytes > kSkCountBytes) {
+    {
+      units = ceil_div(a.M, int64_t(2 * kBH)) * tiles_n * int64_t(K64);
+      const int64_t room = static_cast<int64_t>((a.ws_bytes - kSkCountBytes) / kSkCtaBytes);
+      const int64_t ctas = std::min(std::min(2 * int64_t(sms), room),
+                                    std::min(units / kSkMinStages, kSkMaxCtas));
+      if (ctas >= 1) {
+        const int64_t L = ceil_div(units, ctas);
+        const int64_t segs = ceil_div(L - 1, int64_t(K64)) + 1;
+        const int64_t parts = ceil_div(int64_t(K64), L);
+        const double cost = double(L) * 0.95 + 28.0 + double(segs - 1) + 2.5 * double(parts - 1);
+        if (a.sk_only || cost < best - 1e-9) {
+          sk = true;
+          sk_ctas = ctas;
+          mh = 2;
+          ksplit = 1;
+        }
+      }
+    }
+  }
+  if (a.sk_only && !sk) return cudaErrorNotSupported;
   const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
   const uint64_t es = a.scale_f32 ? 4 : 2;
   const uint32_t bpc = a.bs < kBK ? kBK / a.bs : 1;
@@ -1277,6 +1792,14 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
   p.ksplit = ksplit;
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
+  if (sk) {
+    p.units = units;
+    p.sk_ctas = static_cast<int>(sk_ctas);
+    p.tiles_n = static_cast<int>(tiles_n);
+    p.count = static_cast<unsigned int *>(a.ws);
+    p.ws = reinterpret_cast<float *>(static_cast<unsigned char *>(a.ws) + kSkCountBytes);
+    return sk_bs(p, a.bs, a.scale_f32, stream);
+  }
   const dim3 grid(static_cast<unsigned>(ceil_div(a.N, cols)),
                   static_cast<unsigned>(ceil_div(a.M, int64_t(kBH) * mh)),
                   static_cast<unsigned>(ksplit));

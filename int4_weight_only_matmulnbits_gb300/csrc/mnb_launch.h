@@ -49,7 +49,17 @@ struct MatmulArgs {
   bool paired = false;
   const void *packed_b2 = nullptr, *scales2 = nullptr, *zp2 = nullptr;
   const float *bias2 = nullptr;
+  // Caller-owned workspace for the tensor-core kernel's stream-K schedule
+  // (null: not used); see gemm_workspace_bytes().
+  void *ws = nullptr;
+  size_t ws_bytes = 0;
+  bool sk_only = false;  // the stream-K schedule or cudaErrorNotSupported
 };
+
+// Workspace bytes that let launch_gemm use its stream-K schedule on the
+// current device: a flag page plus one 256 x 128 fp32 partial tile for each
+// CTA the cooperative grid can hold.
+size_t gemm_workspace_bytes();
 
 cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream);
 cudaError_t launch_unprepack(const UnprepackArgs &a, cudaStream_t stream);

@@ -266,3 +266,31 @@ def test_bnb4_rejects_invalid_arguments_on_host(lib):
                                0, 0, None) == -1
     assert lib.mnb_matmul_bnb4(v(16), v(256), v(256), v(2), None, 1, 16, 64, 32, v(1 << 20),
                                0, 0, None) == -5
+
+
+def _call_matmul_ws(lib, ws, ws_bytes, **kw):
+    args = dict(A=16, packed_b=256, scales=256, zp=None, bias=None, M=64, N=16, K=64,
+                bs=32, Y=1 << 20, a_t=1, s_t=1, path=3)
+    args.update(kw)
+    v = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.mnb_matmul_ws(v(args["A"]), v(args["packed_b"]), v(args["scales"]),
+                             v(args["zp"]), v(args["bias"]), args["M"], args["N"], args["K"],
+                             args["bs"], v(args["Y"]), args["a_t"], args["s_t"], args["path"],
+                             v(ws), ws_bytes, None)
+
+
+def test_matmul_ws_checks_its_workspace_on_host(lib):
+    """Workspace alignment (256 bytes) and overlap with every input and the
+    output are refused before any device work; argument errors come first."""
+    far = 1 << 30
+    assert _call_matmul_ws(lib, far + 128, 1 << 20) == -5
+    assert _call_matmul_ws(lib, 256, 1 << 16) == -6          # covers B and the scales
+    assert _call_matmul_ws(lib, (1 << 20) - 256, 512) == -6  # covers the start of Y
+    assert _call_matmul_ws(lib, far, 1 << 20, A=None) == -1
+    assert _call_matmul_ws(lib, far, 1 << 20, path=4) == -8
+    # A valid request reaches the device query, which fails without a GPU
+    # (MNB_ERR_CUDA, or MNB_ERR_DEVICE for another architecture).
+    import torch
+    if not torch.cuda.is_available():
+        assert _call_matmul_ws(lib, far, 1 << 20) in (-7, -9)
+        assert lib.mnb_matmul_workspace_size() == 0
