@@ -43,9 +43,9 @@ WORKLOAD = "Qwen3-4B decode step projections, M=1, bf16 A, bs 128, no zp"
 # capture of the 145 launches (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the decode-kernel sources it was measured on.
 STEP_TRAFFIC = {
-    "bytes_per_launch": 14399608,
+    "bytes_per_launch": 14399470,
     "sources": ("gemv.cu", "mnb_common.cuh", "mnb_launch.h"),
-    "sha256": "cc35c82e686cea0af85006942a24649834ccba5e407a03b27bc635f7587c10de",
+    "sha256": "6906d3673ce5c5f5e00ee6f8d043985132ab9c92def4a78a0aaa3daaacfe45af",
 }
 
 
