@@ -72,6 +72,7 @@ struct GemmParams {
   CUtensorMap tms;  // scales: {16 scales as words, nb, N16}, box {.., bpc, 8}
   CUtensorMap tmz;  // zero points: {4 words, nbz/2, N16}, box {4, ppc, 8}
   CUtensorMap tmw2, tms2, tmz2;  // a pair's up weight (boxes of 4 tiles, as the gate's)
+  CUtensorMap tmy;  // Y: {N, M} bf16, box {64, 128*MH}, 128-byte swizzle (when y_tma)
   // Stream-K schedule (gemm_sk_kernel): units = tiles * K64 (tile, k stage)
   // pairs split evenly over sk_ctas CTAs; tiles_n output tiles along N; ws
   // holds two 256 x 128 fp32 partial tiles per CTA (its first and its last
@@ -83,6 +84,7 @@ struct GemmParams {
   const float *bias, *bias2;
   void *Y;
   int M, N, K64;
+  int y_tma;  // the epilogue stages the tile in shared memory and stores it with TMA
   int has_zp;
   int y_vec;  // Y rows are 16-byte aligned: 16-byte stores
   int sc_bytes, zp_bytes;  // per stage
@@ -171,6 +173,21 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2-D tiled TMA store from this CTA's shared memory (bulk group).
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_addr(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed bulk store has read its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -494,6 +511,49 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
           }
         }
       }
+    } else if (!fault && p.y_tma) {
+      // Stage the bf16 tile in the drained A ring (two 64-column boxes, each
+      // rows x 128 bytes with the 128-byte swizzle: 16-byte chunk c of row r
+      // at chunk c ^ (r % 8)), then one thread stores both boxes with TMA;
+      // rows past M and columns past N are clipped by the tensor map.
+      tc_fence_after();
+      const int quarter = warp & 3;
+      const int half = (warp - 2) >> 2;
+      unsigned char *stage = smem + S::kA;
+      constexpr int kBoxBytes = kBH * MH * 128;
+#pragma unroll 1
+      for (int h = 0; h < MH; ++h) {
+        const int row = h * kBH + quarter * 32 + lane;
+#pragma unroll 1
+        for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
+          float v[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + h * kBN + c * 32, v);
+          float o[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[out_col(i)] = v[i] + sBias[c * 32 + out_col(i)];
+          unsigned char *box = stage + (c >> 1) * kBoxBytes + row * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = bf16_bits(o[8 * q + 2 * e]) | (bf16_bits(o[8 * q + 2 * e + 1]) << 16);
+            const int chunk = ((c & 1) * 4 + q) ^ (row & 7);
+            *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      fence_async_smem();  // the staged tile, to the TMA engine
+      named_barrier_sync(kBarEpi, 32 * kDqWarps);
+      if (tid == 64) {
+        const int n_base = nt0 * kTileN;
+#pragma unroll
+        for (int b = 0; b < kBN / 64; ++b)
+          if (n_base + 64 * b < p.N) tma_store_2d(&p.tmy, stage + b * kBoxBytes, n_base + 64 * b, m0);
+        bulk_commit();
+        bulk_wait_read_all();  // the source stays valid until the CTA exits
+      }
+      __syncwarp();
     } else if (!fault) {
       tc_fence_after();
       const int quarter = warp & 3;          // TMEM lanes this warp may read
@@ -1792,6 +1852,18 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
   p.ksplit = ksplit;
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
+  // TMA stores of the output tile: single weight, no K split, rows of Y a
+  // multiple of 16 bytes from a 16-byte aligned base.
+  if (!sk && !a.paired && ksplit == 1 && (a.N % 8) == 0 &&
+      (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(kBH * mh)};
+    e = make_tmap(&p.tmy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Y, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    p.y_tma = 1;
+  }
   if (sk) {
     p.units = units;
     p.sk_ctas = static_cast<int>(sk_ctas);

@@ -119,13 +119,17 @@ def test_gemm_bitwise_reproducible(dev):
     assert torch.equal(run(prob, dev, "gemm"), run(prob, dev, "gemm"))
 
 
+@pytest.mark.parametrize("N", [12300, 12352])
 @pytest.mark.parametrize("bs,with_zp", [(32, True), (64, False), (256, True)])
-def test_gemm_256_row_tiles_with_tails(dev, bs, with_zp):
+def test_gemm_256_row_tiles_with_tails(dev, bs, with_zp, N):
     """Enough output tiles for the 256-row tile variant (two A halves per B
-    tile): ragged M (777 = 3*256 + 9) and N (12300 = 96*128 + 12), a partial
-    last block; seeded rows (incl. the first and the last) x columns (incl.
-    the ragged N tail) checked element by element."""
-    M, N, K = 777, 12300, 520
+    tile): ragged M (777 = 3*256 + 9) and N, a partial last block; seeded
+    rows (incl. the first and the last) x columns (incl. the ragged N tail)
+    checked element by element. N = 12300 (rows of Y not a multiple of 16
+    bytes) takes the direct stores; N = 12352 = 96.5 * 128 the TMA stores
+    of the staged tile, whose last tile has one 64-column box inside N and
+    one wholly past it."""
+    M, K = 777, 520
     prob = make_problem(M, N, K, bs, dtype=torch.bfloat16, zero_points=with_zp, bias=True,
                         seed=bs + 5)
     Y = run(prob, dev, path="gemm")
