@@ -705,9 +705,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
 //    whose segment is the last of its range) and contributors (CTAs whose
 //    ranges start inside the tile: their first segments). Each piece parks
 //    its fp32 partial tile in the workspace and counts itself in on the
-//    tile's counter (acq_rel); the piece that arrives last adds all partial
-//    tiles in k order (the head's first), adds the bias, stores the tile and
-//    clears the counter. A head that finds every contribution already in
+//    tile's counter (the word of its head CTA; acq_rel); the piece that
+//    arrives last adds all partial tiles in k order (the head's first),
+//    adds the bias, stores the tile and clears the counter. A head that finds every contribution already in
 //    (the usual case: it reaches its last segment late) adds them to its
 //    accumulators directly and parks nothing.
 // The sums run in one fixed order whichever piece completes the tile, so
@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
 // segments the MMA thread waits until the epilogue has drained the TMEM
 // accumulators.
 
-__device__ __forceinline__ uint32_t flag_load_acquire(const unsigned int *f) {
+__device__ __forceinline__ uint32_t count_load_acquire(const unsigned int *f) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
   return v;
@@ -725,7 +725,7 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(unsigned int *f, uint32_t v
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(f), "r"(v) : "memory");
   return old;
 }
-__device__ __forceinline__ void flag_store_relaxed(unsigned int *f, uint32_t v) {
+__device__ __forceinline__ void count_store_relaxed(unsigned int *f, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() {
@@ -1011,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_const
       // its accumulators; any other piece of a split tile is parked.
       if (head && !whole && warp == 2) {
         if (lane == 0)
-          *sh_mode = (!fault && flag_load_acquire(p.count + c) == uint32_t(ncontrib)) ? 0u : 1u;
+          *sh_mode = (!fault && count_load_acquire(p.count + c) == uint32_t(ncontrib)) ? 0u : 1u;
         __syncwarp();
       }
       if (!fault && !mbar_wait(acc_full, j & 1)) {
@@ -1055,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_const
             }
           }
         }
-        if (!whole && !park && tid == 64) flag_store_relaxed(p.count + c, 0u);
+        if (!whole && !park && tid == 64) count_store_relaxed(p.count + c, 0u);
       }
       if (park) {
         // Count this piece in; the last of the tile's pieces completes it,
@@ -1094,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_const
               }
             }
           }
-          if (tid == 64) flag_store_relaxed(p.count + ch, 0u);
+          if (tid == 64) count_store_relaxed(p.count + ch, 0u);
         }
       }
       // The accumulators are drained: the MMA thread may start the next segment.
