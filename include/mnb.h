@@ -248,6 +248,38 @@ MNB_API mnb_status mnb_matmul_ws(const void *A, const void *packed_b,
                                  size_t workspace_bytes, mnb_stream_t stream);
 
 /*
+ * What mnb_matmul_ws would launch for a product: the kernel and, on the
+ * tensor-core path, its tile height, K split, schedule and epilogue. Pure
+ * host arithmetic (the same cost models the launch uses), for a GPU with
+ * sm_count SMs (0: the current device's). Activations and Y are taken to be
+ * 16-byte aligned, a workspace of workspace_bytes present when it is not 0.
+ * No counterpart in the pages; it reports, it computes nothing.
+ *  out: filled on MNB_OK.
+ * Errors: MNB_ERR_NULL (out), the argument errors of mnb_matmul_path,
+ * MNB_ERR_UNSUPPORTED (a forced path that cannot serve the product),
+ * MNB_ERR_DEVICE / MNB_ERR_CUDA (sm_count 0 without a usable device).
+ */
+typedef struct {
+  int32_t path;      /* MNB_PATH_GEMV (the decode kernel) or MNB_PATH_GEMM  */
+  int32_t m_slices;  /* decode kernel over 16-row slices of A (activations
+                        the tensor-core kernel cannot stage): how many; else 0 */
+  int32_t tile_rows; /* tensor-core kernel: output rows per tile (128, 256)  */
+  int32_t k_split;   /* tensor-core kernel: CTAs of a cluster sharing a
+                        tile's k range (1, 2, 4, 8)                          */
+  int32_t stream_k;  /* 1: the stream-K schedule                             */
+  int32_t tf32;      /* 1: the tf32 kernel (fp32 activations)                */
+  int32_t tma_store; /* 1: the output tile goes out through TMA stores      */
+  int32_t reserved;  /* 0                                                    */
+  int64_t ctas;      /* CTAs of the tensor-core launch                       */
+} mnb_matmul_plan_info;
+
+MNB_API mnb_status mnb_matmul_plan(int64_t M, int64_t N, int64_t K,
+                                   int block_size, mnb_dtype a_dtype,
+                                   mnb_dtype scale_dtype, int has_zero_points,
+                                   mnb_path path, size_t workspace_bytes,
+                                   int sm_count, mnb_matmul_plan_info *out);
+
+/*
  * Fused-N projections: Y_i = A * dequant(B_i)^T + bias_i for i < count
  * (1 <= count <= 4), for weights that read the same activations, such as
  * the q/k/v or the gate/up projections of a decoder layer (page "Qwen3 CPU

@@ -9,7 +9,7 @@ from .binding import (EXPORTS, ChainOp, MnbChain, MnbError, PackedWeight, load,
                       mnb_chain_run_noalloc, mnb_matmul_rmsnorm,
                       mnb_prepack_bnb4, mnb_matmul_bnb4,
                       mnb_fault_status, mnb_matmul, mnb_matmul_from_host,
-                      mnb_matmul_workspace,
+                      mnb_matmul_workspace, mnb_matmul_plan,
                       mnb_matmul_gate_up, mnb_matmul_grouped, mnb_prepack,
                       mnb_prepack_qdq,
                       mnb_prepacked_sizes, mnb_set_programmatic_launch,
@@ -17,6 +17,6 @@ from .binding import (EXPORTS, ChainOp, MnbChain, MnbError, PackedWeight, load,
 from ._build import build_library
 
 __all__ = ["EXPORTS", "ChainOp", "MnbChain", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc", "mnb_matmul_rmsnorm", "mnb_prepack_bnb4", "mnb_matmul_bnb4", "MnbError", "PackedWeight", "build_library", "load",
-           "library_path", "mnb_fault_status", "mnb_matmul", "mnb_matmul_workspace", "mnb_matmul_gate_up", "mnb_matmul_grouped", "mnb_matmul_from_host", "mnb_prepack", "mnb_prepack_qdq",
+           "library_path", "mnb_fault_status", "mnb_matmul", "mnb_matmul_workspace", "mnb_matmul_plan", "mnb_matmul_gate_up", "mnb_matmul_grouped", "mnb_matmul_from_host", "mnb_prepack", "mnb_prepack_qdq",
            "mnb_prepacked_sizes", "mnb_set_programmatic_launch", "mnb_unprepack",
            "mnb_version", "status_string"]

@@ -28,10 +28,19 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
            "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc",
            "mnb_matmul_rmsnorm", "mnb_prepack_bnb4", "mnb_matmul_bnb4",
-           "mnb_matmul_workspace_size", "mnb_matmul_ws")
+           "mnb_matmul_workspace_size", "mnb_matmul_ws", "mnb_matmul_plan")
 
 _lock = threading.Lock()
 _lib = None
+
+
+class PlanInfoC(ctypes.Structure):
+    """mnb_matmul_plan_info (include/mnb.h)."""
+    _fields_ = [("path", ctypes.c_int32), ("m_slices", ctypes.c_int32),
+                ("tile_rows", ctypes.c_int32), ("k_split", ctypes.c_int32),
+                ("stream_k", ctypes.c_int32), ("tf32", ctypes.c_int32),
+                ("tma_store", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("ctas", ctypes.c_int64)]
 
 
 class ChainOpC(ctypes.Structure):
@@ -111,6 +120,9 @@ def load(build_if_missing: bool = False):
         lib.mnb_matmul_ws.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32, i32, i32, p,
                                       sz, p]
         lib.mnb_matmul_ws.restype = i32
+        lib.mnb_matmul_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, sz, i32,
+                                        ctypes.POINTER(PlanInfoC)]
+        lib.mnb_matmul_plan.restype = i32
         lib.mnb_matmul_from_host.argtypes = [p, p, p, p, p, p, i64, i64, i64, i32,
                                              p, p, i32, i32, p]
         lib.mnb_matmul_from_host.restype = i32
@@ -263,6 +275,25 @@ def mnb_unprepack(w: PackedWeight, *, stream=None):
                                 _ptr(B), _ptr(S), _ptr(Z), _stream(stream)),
            "mnb_unprepack")
     return B, S, Z
+
+
+def mnb_matmul_plan(M: int, N: int, K: int, block_size: int, *,
+                    a_dtype: torch.dtype = torch.bfloat16,
+                    scale_dtype: torch.dtype | None = None, zero_points: bool = False,
+                    path: str = "auto", workspace_bytes: int = 0,
+                    sm_count: int = 0) -> dict:
+    """What mnb_matmul(..., workspace) would launch (host arithmetic only):
+    {"path": "gemv" | "gemm", "m_slices", "tile_rows", "k_split", "stream_k",
+    "tf32", "tma_store", "ctas"}. sm_count 0 asks the current device."""
+    info = PlanInfoC()
+    sd = a_dtype if scale_dtype is None else scale_dtype
+    _check(load().mnb_matmul_plan(M, N, K, block_size, _dtype_code(a_dtype), _dtype_code(sd),
+                                  int(bool(zero_points)), MNB_PATH[path], workspace_bytes,
+                                  sm_count, ctypes.byref(info)), "mnb_matmul_plan")
+    return {"path": "gemv" if info.path == MNB_PATH["gemv"] else "gemm",
+            "m_slices": info.m_slices, "tile_rows": info.tile_rows,
+            "k_split": info.k_split, "stream_k": bool(info.stream_k), "tf32": bool(info.tf32),
+            "tma_store": bool(info.tma_store), "ctas": info.ctas}
 
 
 def mnb_matmul_workspace(device=None) -> torch.Tensor:

@@ -402,6 +402,58 @@ mnb_status mnb_matmul_path(const void *A, const void *packed_b,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
+static_assert(sizeof(mnb_matmul_plan_info) == 40, "mnb_matmul_plan_info layout");
+
+mnb_status mnb_matmul_plan(int64_t M, int64_t N, int64_t K, int block_size,
+                           mnb_dtype a_dtype, mnb_dtype scale_dtype, int has_zero_points,
+                           mnb_path path, size_t workspace_bytes, int sm_count_in,
+                           mnb_matmul_plan_info *out) {
+  if (!out) return MNB_ERR_NULL;
+  if (M < 1 || M > kMaxDim) return MNB_ERR_SHAPE;
+  mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  if (!valid_dtype(a_dtype)) return MNB_ERR_DTYPE;
+  if (path != MNB_PATH_AUTO && path != MNB_PATH_GEMV && path != MNB_PATH_GEMM &&
+      path != MNB_PATH_GEMM_STREAMK)
+    return MNB_ERR_UNSUPPORTED;
+  if (path == MNB_PATH_GEMV && M > kGemvMaxM) return MNB_ERR_UNSUPPORTED;
+  int sms = sm_count_in;
+  if (sms <= 0) {
+    st = check_device();
+    if (st != MNB_OK) return st;
+    sms = sm_count();
+  }
+  // The arguments run_matmul builds; null A and Y count as aligned, and the
+  // planner only tests the zero points and the workspace for presence.
+  alignas(256) static unsigned char present[1];
+  MatmulArgs a{nullptr, nullptr, nullptr, has_zero_points ? present : nullptr,
+               nullptr, nullptr, M, N, K, block_size, a_dtype == MNB_F32,
+               scale_dtype == MNB_F32, false};
+  a.ws = workspace_bytes ? present : nullptr;
+  a.ws_bytes = workspace_bytes;
+  a.sk_only = path == MNB_PATH_GEMM_STREAMK;
+  mnb_matmul_plan_info r{};
+  if (path == MNB_PATH_GEMV || (path == MNB_PATH_AUTO && M <= kGemvMaxM)) {
+    r.path = MNB_PATH_GEMV;
+  } else if (path == MNB_PATH_GEMM || path == MNB_PATH_GEMM_STREAMK || gemm_supports(a)) {
+    if (!gemm_supports(a) || (a.sk_only && (a.a_f32 || !a.ws))) return MNB_ERR_UNSUPPORTED;
+    const GemmPlanInfo g = gemm_plan_info(a, sms);
+    if (a.sk_only && !g.stream_k) return MNB_ERR_UNSUPPORTED;
+    r.path = MNB_PATH_GEMM;
+    r.tile_rows = g.tile_rows;
+    r.k_split = g.k_split;
+    r.stream_k = g.stream_k;
+    r.tf32 = g.tf32;
+    r.tma_store = g.tma_store;
+    r.ctas = g.ctas;
+  } else {
+    r.path = MNB_PATH_GEMV;
+    r.m_slices = static_cast<int32_t>((M + kGemvMaxM - 1) / kGemvMaxM);
+  }
+  *out = r;
+  return MNB_OK;
+}
+
 size_t mnb_matmul_workspace_size(void) {
   if (check_device() != MNB_OK) return 0;
   return gemm_workspace_bytes();

@@ -1550,6 +1550,12 @@ cudaError_t launch_mh(const GemmParams &p, dim3 grid, int mh, bool sf32, bool pd
                  : launch_flags<BS, 1>(p, grid, sf32, pdl, stream);
 }
 
+struct GemmPlan {
+  int mh = 1, ksplit = 1;  // tile height in halves of 128 rows; cluster K split
+  bool sk = false;         // stream-K schedule
+  int64_t sk_ctas = 0, units = 0;
+};
+
 // Stream-K workspace: a page of per-CTA arrival counters, then two
 // 256 x 128 fp32 partial tiles per CTA.
 constexpr size_t kSkCountBytes = 4096;
@@ -1599,8 +1605,8 @@ cudaError_t sk_bs(const GemmParams &p, int bs, bool sf32, cudaStream_t stream) {
 // pack per GPC, which on GB300 (152 SMs) leaves 8 CTA slots unused with
 // clusters of 4 and 16 with clusters of 8 (occupancy query for this kernel's
 // shared memory and 320 threads: 152, 74 and 36 clusters of 2, 4 and 8).
-int64_t resident_ctas(int c) {
-  const int64_t two = 2 * int64_t(sm_count());
+int64_t resident_ctas(int c, int sms) {
+  const int64_t two = 2 * int64_t(sms);
   return c <= 2 ? two : c == 4 ? two - two / 38 : two - two / 19;
 }
 
@@ -1623,6 +1629,33 @@ bool gemm_supports(const MatmulArgs &a) {
   if (reinterpret_cast<uintptr_t>(a.A) % 16 != 0) return false;
   if (a.a_f32) return (a.K % 4) == 0 && !a.paired;
   return (a.K % 8) == 0;
+}
+
+// K split of the tf32 kernel (fp32 activations) on a GPU with `sms` SMs.
+int plan_gemm_tf32(const MatmulArgs &a, int sms) {
+  // K split (cluster of 1..8 CTAs) when the output tiles cannot fill the
+  // GPU: a CTA spends about 0.75 us per 64-wide k stage (the tf32 tensor
+  // rate of one SM), plus the split's fixed cost; one CTA per SM, clusters
+  // packing per GPC.
+  const uint64_t K64 = ceil_div(a.K, kChunkK);
+  const int64_t tiles = ceil_div(a.M, int64_t(kBH)) * ceil_div(a.N, int64_t(kBN));
+  int ksplit = 1;
+  {
+    double best = 0.0;
+    for (int c = 1; c <= 8; c *= 2) {
+      const int64_t kps = ceil_div(int64_t(K64), int64_t(c));
+      if (c > 1 && (kps < 4 || (c - 1) * kps >= int64_t(K64))) continue;
+      const int64_t slots = c <= 2 ? sms - (c == 2 ? 8 : 0) : sms - 24;
+      if (slots <= 0) continue;
+      const double fixed = c == 1 ? 2.0 : c == 2 ? 4.0 : c == 4 ? 6.0 : 13.0;
+      const double cost = double(ceil_div(tiles * c, slots)) * (double(kps) * 0.75 + fixed);
+      if (c == 1 || cost < best - 1e-9) {
+        best = cost;
+        ksplit = c;
+      }
+    }
+  }
+  return ksplit;
 }
 
 // fp32 activations: the tf32 kernel, 128 x 128 tiles, one CTA per SM.
@@ -1675,27 +1708,7 @@ cudaError_t launch_gemm_tf32(const MatmulArgs &a, cudaStream_t stream) {
   p.N = static_cast<int>(a.N);
   p.K64 = static_cast<int>(K64);
   p.has_zp = a.zp != nullptr;
-  // K split (cluster of 1..8 CTAs) when the output tiles cannot fill the
-  // GPU: a CTA spends about 0.75 us per 64-wide k stage (the tf32 tensor
-  // rate of one SM), plus the split's fixed cost; one CTA per SM, clusters
-  // packing per GPC.
-  const int64_t tiles = ceil_div(a.M, int64_t(kBH)) * ceil_div(a.N, int64_t(kBN));
-  int ksplit = 1;
-  {
-    const int sms = sm_count();
-    double best = 0.0;
-    for (int c = 1; c <= 8; c *= 2) {
-      const int64_t kps = ceil_div(int64_t(K64), int64_t(c));
-      if (c > 1 && (kps < 4 || (c - 1) * kps >= int64_t(K64))) continue;
-      const int64_t slots = c <= 2 ? sms - (c == 2 ? 8 : 0) : sms - 24;
-      const double fixed = c == 1 ? 2.0 : c == 2 ? 4.0 : c == 4 ? 6.0 : 13.0;
-      const double cost = double(ceil_div(tiles * c, slots)) * (double(kps) * 0.75 + fixed);
-      if (c == 1 || cost < best - 1e-9) {
-        best = cost;
-        ksplit = c;
-      }
-    }
-  }
+  const int ksplit = plan_gemm_tf32(a, sm_count());
   p.ksplit = ksplit;
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
   const dim3 grid(static_cast<unsigned>(ceil_div(a.N, int64_t(kBN))),
@@ -1711,14 +1724,11 @@ cudaError_t launch_gemm_tf32(const MatmulArgs &a, cudaStream_t stream) {
   }
 }
 
-cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
-  if (!gemm_supports(a)) return cudaErrorNotSupported;
-  if (a.sk_only && (a.a_f32 || a.paired || !a.ws)) return cudaErrorNotSupported;
-  if (a.a_f32) return launch_gemm_tf32(a, stream);
-  GemmParams p{};
-  const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
-  // Output columns per CTA: 128, or 64 for a gated-MLP pair (64 gate and 64
-  // up rows fill the B tile).
+// Tile height, K split and schedule of the bf16 kernel for a product on a
+// GPU with `sms` SMs: pure host arithmetic, shared by the launch and by
+// mnb_matmul_plan.
+GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
+  const uint64_t K64 = ceil_div(a.K, kChunkK);
   const int64_t cols = a.paired ? kBN / 2 : kBN;
   // Tile height (128 or 256 rows) and K split (cluster of 1..8 CTAs, 128-row
   // tiles only) by a cost model fitted to GB300 measurements: a CTA spends
@@ -1727,8 +1737,8 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   // split (the partial tiles' reduction through distributed shared memory);
   // CTAs run in rounds of what can be resident at once, clusters packing per
   // GPC.
-  int mh = 1, ksplit = 1;
-  const int sms = sm_count();
+  GemmPlan r;
+  int &mh = r.mh, &ksplit = r.ksplit;
   double best = 0.0;
   {
     bool have = false;
@@ -1738,7 +1748,7 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
         if (c > 1 && (kps < 4 || (c - 1) * kps >= int64_t(K64))) continue;
         const int64_t ctas = ceil_div(a.M, int64_t(kBH) * h) * ceil_div(a.N, cols) * c;
         if (h == 2 && ctas < sms) continue;  // a lone 256-row CTA per SM is slower
-        const int64_t slots = resident_ctas(c);
+        const int64_t slots = resident_ctas(c, sms);
         if (slots <= 0) continue;
         const double fixed = c == 1 ? 2.0 : c == 2 ? 4.0 : c == 4 ? 6.0 : 13.0;
         const double cost = double(ceil_div(ctas, slots)) *
@@ -1760,29 +1770,43 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   // for each further tile a CTA's range touches. It wins where whole tiles
   // leave half the CTA slots idle for long (down and o projections with
   // M >= 2048, 4096) and loses where tiles are few or short.
-  bool sk = false;
-  int64_t sk_ctas = 0, units = 0;
-  const int64_t tiles_n = ceil_div(a.N, int64_t(kBN));
   if (a.ws && !a.paired && a.ws_bytes > kSkCountBytes) {
-    {
-      units = ceil_div(a.M, int64_t(2 * kBH)) * tiles_n * int64_t(K64);
-      const int64_t room = static_cast<int64_t>((a.ws_bytes - kSkCountBytes) / kSkCtaBytes);
-      const int64_t ctas = std::min(std::min(2 * int64_t(sms), room),
-                                    std::min(units / kSkMinStages, kSkMaxCtas));
-      if (ctas >= 1) {
-        const int64_t L = ceil_div(units, ctas);
-        const int64_t segs = ceil_div(L - 1, int64_t(K64)) + 1;
-        const int64_t parts = ceil_div(int64_t(K64), L);
-        const double cost = double(L) * 0.95 + 28.0 + double(segs - 1) + 2.5 * double(parts - 1);
-        if (a.sk_only || cost < best - 1e-9) {
-          sk = true;
-          sk_ctas = ctas;
-          mh = 2;
-          ksplit = 1;
-        }
+    const int64_t tiles_n = ceil_div(a.N, int64_t(kBN));
+    const int64_t units = ceil_div(a.M, int64_t(2 * kBH)) * tiles_n * int64_t(K64);
+    const int64_t room = static_cast<int64_t>((a.ws_bytes - kSkCountBytes) / kSkCtaBytes);
+    const int64_t ctas = std::min(std::min(2 * int64_t(sms), room),
+                                  std::min(units / kSkMinStages, kSkMaxCtas));
+    if (ctas >= 1) {
+      const int64_t L = ceil_div(units, ctas);
+      const int64_t segs = ceil_div(L - 1, int64_t(K64)) + 1;
+      const int64_t parts = ceil_div(int64_t(K64), L);
+      const double cost = double(L) * 0.95 + 28.0 + double(segs - 1) + 2.5 * double(parts - 1);
+      if (a.sk_only || cost < best - 1e-9) {
+        r.sk = true;
+        r.sk_ctas = ctas;
+        r.units = units;
+        mh = 2;
+        ksplit = 1;
       }
     }
   }
+  return r;
+}
+
+cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
+  if (!gemm_supports(a)) return cudaErrorNotSupported;
+  if (a.sk_only && (a.a_f32 || a.paired || !a.ws)) return cudaErrorNotSupported;
+  if (a.a_f32) return launch_gemm_tf32(a, stream);
+  GemmParams p{};
+  const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
+  // Output columns per CTA: 128, or 64 for a gated-MLP pair (64 gate and 64
+  // up rows fill the B tile).
+  const int64_t cols = a.paired ? kBN / 2 : kBN;
+  const GemmPlan plan = plan_gemm(a, sm_count());
+  const int mh = plan.mh, ksplit = plan.ksplit;
+  const bool sk = plan.sk;
+  const int64_t sk_ctas = plan.sk_ctas, units = plan.units;
+  const int64_t tiles_n = ceil_div(a.N, int64_t(kBN));
   if (a.sk_only && !sk) return cudaErrorNotSupported;
   const uint64_t nb = ceil_div(a.K, a.bs), nbz = ceil_div(nb, 2) * 2;
   const uint64_t es = a.scale_f32 ? 4 : 2;
@@ -1883,6 +1907,28 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
     case 256: return launch_mh<256>(p, grid, mh, a.scale_f32, a.pdl, stream);
     default: return cudaErrorNotSupported;
   }
+}
+
+GemmPlanInfo gemm_plan_info(const MatmulArgs &a, int sms) {
+  GemmPlanInfo o;
+  if (a.a_f32) {
+    o.tf32 = true;
+    o.tile_rows = kBH;
+    o.k_split = plan_gemm_tf32(a, sms);
+    o.ctas = ceil_div(a.M, int64_t(kBH)) * ceil_div(a.N, int64_t(kBN)) * o.k_split;
+    return o;
+  }
+  const GemmPlan pl = plan_gemm(a, sms);
+  o.tile_rows = kBH * pl.mh;
+  o.k_split = pl.ksplit;
+  o.stream_k = pl.sk;
+  o.ctas = pl.sk ? pl.sk_ctas
+                 : ceil_div(a.M, int64_t(kBH) * pl.mh) *
+                       ceil_div(a.N, int64_t(a.paired ? kBN / 2 : kBN)) * pl.ksplit;
+  // As launch_gemm decides it.
+  o.tma_store = !pl.sk && !a.paired && pl.ksplit == 1 && (a.N % 8) == 0 &&
+                (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
+  return o;
 }
 
 }  // namespace mnb

@@ -56,6 +56,16 @@ struct MatmulArgs {
   bool sk_only = false;  // the stream-K schedule or cudaErrorNotSupported
 };
 
+// What launch_gemm would launch for a product on a GPU with `sms` SMs (host
+// arithmetic only; `a.A`, `a.Y` and `a.ws` are only tested for alignment or
+// presence).
+struct GemmPlanInfo {
+  bool tf32 = false, stream_k = false, tma_store = false;
+  int tile_rows = 0, k_split = 1;
+  int64_t ctas = 0;
+};
+GemmPlanInfo gemm_plan_info(const MatmulArgs &a, int sms);
+
 // Workspace bytes that let launch_gemm use its stream-K schedule on the
 // current device: a flag page plus one 256 x 128 fp32 partial tile for each
 // CTA the cooperative grid can hold.
