@@ -76,12 +76,14 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_path: str | None = None):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        out_dir = os.path.join(ROOT, "gpurun_out")
-        self.out = (os.path.join(out_dir, f"clocks_gpu{gpu_index}.csv")
-                    if os.path.isdir(out_dir) else f"/tmp/mnb_clocks_{os.getpid()}.csv")
+        # The raw samples go to the caller's file (--clock-log) or a private
+        # temporary file; only their summary enters the JSON line.
+        self.out = log_path or os.path.join(tempfile.mkdtemp(prefix="mnb_clocks_"),
+                                            f"clocks_gpu{gpu_index}.csv")
 
     def start(self):
         try:
@@ -396,7 +398,7 @@ def run_gpu(args, rank, world, dist):
         graph.replay()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, args.clock_log)
     if dist:
         dist.barrier()
     sampler.start()
@@ -612,6 +614,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="file for the raw nvidia-smi clock samples of the timed region "
+                         "(default: a private temporary file)")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--case", default=None, choices=sorted(CASES) + ["step", "sweep"],
                     help="run one kernel shape (or one eager decode step per --steps, or "

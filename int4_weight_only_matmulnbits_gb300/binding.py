@@ -17,6 +17,14 @@ import torch
 from . import _build
 
 MNB_OK = 0
+MNB_ERR_NULL = -1
+MNB_ERR_SHAPE = -2
+MNB_ERR_BLOCKSIZE = -3
+MNB_ERR_DTYPE = -4
+MNB_ERR_ALIGN = -5
+MNB_ERR_ALIAS = -6
+MNB_ERR_CUDA = -7
+MNB_ERR_UNSUPPORTED = -8
 MNB_ERR_DEVICE = -9
 MNB_F32, MNB_BF16 = 0, 1
 MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_streamk": 3}

@@ -740,12 +740,11 @@ cudaError_t configure_one(int smem, int *occ) {
 
 template <int BS, bool HAS_ZP, bool SF32>
 cudaError_t launch_chain_one(const ChainParams &p, const ChainGeom &g, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = configure_one<BS, HAS_ZP, SF32>(g.smem, nullptr);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  if (const cudaError_t e =
+          ensure_smem_limit(chain_kernel<BS, HAS_ZP, SF32>, kBudget1, configured);
+      e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid, 1, 1);
   cfg.blockDim = dim3(kThreadsChain, 1, 1);

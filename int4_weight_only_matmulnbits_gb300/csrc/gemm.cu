@@ -1457,13 +1457,9 @@ template <int BS, bool HAS_ZP, bool SF32>
 cudaError_t launch_tf32_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
   auto kernel = gemm_tf32_kernel<BS, HAS_ZP, SF32>;
   const int smem = SmemT::kTotal + 1024;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  if (const cudaError_t e = ensure_smem_limit(kernel, smem, configured); e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1502,13 +1498,9 @@ template <int BS, bool HAS_ZP, bool SF32, int MH>
 cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
   auto kernel = gemm_kernel<BS, HAS_ZP, SF32, MH>;
   const int smem = Smem<MH, BS, SF32>::kTotal + 1024;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  if (const cudaError_t e = ensure_smem_limit(kernel, smem, configured); e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1568,13 +1560,9 @@ template <int BS, bool HAS_ZP, bool SF32>
 cudaError_t sk_run(const GemmParams &p, cudaStream_t stream) {
   auto kernel = gemm_sk_kernel<BS, HAS_ZP, SF32>;
   const int smem = Smem<2, BS, SF32>::kTotal + 1024;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  if (const cudaError_t e = ensure_smem_limit(kernel, smem, configured); e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.sk_ctas), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -854,13 +854,9 @@ template <int MT, int BS, bool HAS_ZP, bool SF32, bool CODE = false>
 cudaError_t launch_one(const GemvParams &p, const Choice &ch, int grid, bool pdl,
                        cudaStream_t stream) {
   auto kernel = gemv_kernel<MT, BS, HAS_ZP, SF32, CODE>;
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  if (const cudaError_t e = ensure_smem_limit(kernel, kSmemMax, configured); e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -7,9 +7,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <vector>
 
 namespace mnb {
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device: `done` (one per kernel instantiation) holds a bit
+// for each device ordinal below 64 already configured; higher ordinals are
+// configured on every call. Two host threads may both set it the first
+// time, which is harmless (the call is idempotent).
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kernel, int bytes, std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 struct PrepackArgs {
   const uint8_t *B;
