@@ -430,9 +430,10 @@ MNB_API mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float 
  * not a multiple of block_size.
  *
  * mnb_matmul_bnb4 runs the decode kernel with the code book (over 8-row
- * slices beyond 8 rows): each CTA turns the 16 values into a table of
- * bf16 pairs, so every weight is code[q] rounded to bf16 (within 2^-9) times
- * the fp32 or bf16 absmax applied in fp32. Errors: as mnb_matmul;
+ * slices beyond 8 rows): each CTA turns the 16 values into a table of bf16
+ * pairs, each value c held as hi = bf16(c) and lo = bf16(c - hi) and both
+ * multiplied by the activations, so every weight is within 2^-16 |c| of
+ * code[q], times the fp32 or bf16 absmax applied in fp32. Errors: as mnb_matmul;
  * MNB_ERR_NULL for code; MNB_ERR_ALIAS if Y overlaps code.
  */
 MNB_API mnb_status mnb_prepack_bnb4(const uint8_t *B, const void *absmax, int64_t N,

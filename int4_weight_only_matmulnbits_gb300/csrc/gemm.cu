@@ -15,17 +15,18 @@
 //    tile ((128*MH) x 64 bf16, 128-byte swizzle), the 128 x 64 packed codes
 //    of the stage and their scales and zero points into the input ring,
 //    completing on full[s].
-//  * warps 2-9, one 16-row weight tile each: dequantise the stage's codes to
-//    bf16 (q - z) * s (the difference is exact; one rounding in the product)
-//    into a two-deep ring of B tiles in the K-major, 128-byte-swizzled layout
-//    tcgen05.mma reads, fence the writes to the async proxy and arrive on
-//    bfull[b]. Weight rows g and g+8 of a 16-row tile go to B rows 2g and
-//    2g+1, which keeps every warp's stores free of bank conflicts; the
-//    epilogue maps the columns back.
+//  * warps 2-9, one 16-row weight tile each: dequantise the stage's codes,
+//    w = (q - z) * s, into two bf16 B tiles, hi = w rounded and lo = the
+//    remainder (hi + lo == w for bf16 scales, within 2^-16 |w| for fp32
+//    scales), in the K-major, 128-byte-swizzled layout tcgen05.mma reads;
+//    fence the writes to the async proxy and arrive on bfull[b]. Weight rows
+//    g and g+8 of a 16-row tile go to B rows 2g and 2g+1, which keeps every
+//    warp's stores free of bank conflicts; the epilogue maps the columns
+//    back.
 //  * warp 1: allocates the TMEM accumulators (128 lanes x 128*MH fp32
-//    columns); one thread issues 4*MH tcgen05.mma (M=128, N=128, K=16) per
-//    stage, the MH halves of A sharing the B tile, and commits each stage to
-//    empty[s] and bempty[b], the last one to acc_full.
+//    columns); one thread issues 8*MH tcgen05.mma (M=128, N=128, K=16) per
+//    stage, the MH halves of A sharing the hi and the lo tile, and commits
+//    each stage to empty[s] and bempty[b], the last one to acc_full.
 //  * warps 2-9 then read the accumulators with tcgen05.ld (each warp its
 //    TMEM lane quarter and half of the columns), add the bias (staged in
 //    shared memory), round to bf16 and store Y.
@@ -57,12 +58,14 @@ namespace {
 constexpr int kBH = 128;  // rows of one A half (the MMA's M)
 constexpr int kBN = 128;
 constexpr int kBK = 64;  // one chunk of the packed layout
-constexpr int kBStages = 2;  // dequantised B tiles
+constexpr int kBStagesTf32 = 2;  // dequantised B tiles of the tf32 kernel
 constexpr int kDqWarps = 8;
 constexpr int kThreads = 32 * (2 + kDqWarps);
 constexpr int kTilesN = kBN / kTileN;
 constexpr int kAHalfBytes = kBH * kBK * 2;  // 16 KB
-constexpr int kBTileBytes = kBN * kBK * 2;  // 16 KB
+constexpr int kBTileBytes = kBN * kBK * 2;  // 16 KB: one bf16 B tile
+// A B slot of the bf16 kernels holds two tiles, hi and lo (see dequant_pair).
+constexpr int kBSlotBytes = 2 * kBTileBytes;
 constexpr int kCodeBytes = kTilesN * kChunkBytes;  // 4 KB
 constexpr int kBarEpi = 1;  // named barrier of the dequantisation/epilogue warps
 
@@ -104,6 +107,10 @@ constexpr int kSmemLimit2 = (228 * 1024) / 2 - 1024;
 template <int MH, int BS, bool SF32>
 struct Smem {
   static constexpr int kAStages = MH == 1 ? 3 : 2;  // A ring depth
+  // Dequantised B slots (hi and lo tiles, 32 KB each): one. The dequantisation
+  // of stage i + 1 then waits for the MMAs of stage i; the SM's other CTA
+  // keeps the tensor core busy meanwhile.
+  static constexpr int kBStages = 1;
   static constexpr int kATileBytes = MH * kAHalfBytes;
   static constexpr int kBpcS = BS < kBK ? kBK / BS : 1;
   // 8 tiles x the stage's blocks x 16 scales (a multiple of 128 bytes).
@@ -112,11 +119,11 @@ struct Smem {
   // Weight ring depth: 3 where it fits beside the A and B rings, else 2.
   static constexpr int kWBytes = kCodeBytes + kScBytes + kZpBytes;
   static constexpr int kFixed =
-      kAStages * kATileBytes + kBStages * kBTileBytes + kBN * 4 + 256 + 1024;
+      kAStages * kATileBytes + kBStages * kBSlotBytes + kBN * 4 + 256 + 1024;
   static constexpr int kWStages = kFixed + 3 * kWBytes <= kSmemLimit2 ? 3 : 2;
   static constexpr int kA = 0;
   static constexpr int kB = kA + kAStages * kATileBytes;
-  static constexpr int kCodes = kB + kBStages * kBTileBytes;
+  static constexpr int kCodes = kB + kBStages * kBSlotBytes;
   static constexpr int kSc = kCodes + kWStages * kCodeBytes;
   static constexpr int kZp = kSc + kWStages * kScBytes;
   static constexpr int kBias = kZp + kWStages * kZpBytes;
@@ -220,15 +227,42 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
-// (q - z) * s for a bf16 pair holding 128 + q: exact difference, one rounding.
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// w = (q - z) * s for a bf16 pair holding 128 + q, returned as two bf16
+// pairs whose sum is w: hi = w rounded to bf16, lo = (w - hi) rounded to
+// bf16. The tensor core multiplies the activations by both (two MMAs into
+// one accumulator), so no weight carries the 2^-8 relative error of a single
+// bf16 rounding:
+//  * bf16 scales: q - z is an integer of at most 4 bits and s has an 8-bit
+//    significand, so w is exact in 12 bits; hi takes the leading 8 and the
+//    fused multiply-add returns the remainder w - hi exactly (at most 5
+//    significant bits). hi + lo == w.
+//  * fp32 scales: w is formed in fp32 (relative error 2^-24), w - hi is exact
+//    in fp32, and rounding it to bf16 leaves at most 2^-8 |w - hi| <=
+//    2^-16 |w|.
 template <bool SF32>
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t v, uint32_t zc, uint32_t sb,
-                                                 float sf) {
+__device__ __forceinline__ void dequant_pair(uint32_t v, uint32_t zc, uint32_t sb, float sf,
+                                             uint32_t &hi, uint32_t &lo) {
   const uint32_t dq = bf16x2_sub(v, zc);  // q - z, exact
-  if (!SF32) return bf16x2_mul(dq, sb);
-  const float lo = bf16_bits_to_f32(dq & 0xFFFFu) * sf;
-  const float hi = bf16_bits_to_f32(dq >> 16) * sf;
-  return bf16_bits(lo) | (bf16_bits(hi) << 16);
+  if (!SF32) {
+    hi = bf16x2_mul(dq, sb);
+    lo = bf16x2_fma(dq, sb, hi ^ 0x80008000u);  // w - hi, exact
+    return;
+  }
+  const float w0 = bf16_bits_to_f32(dq & 0xFFFFu) * sf;
+  const float w1 = bf16_bits_to_f32(dq >> 16) * sf;
+  hi = f32x2_to_bf16x2(w0, w1);
+  lo = f32x2_to_bf16x2(w0 - bf16_bits_to_f32(hi & 0xFFFFu), w1 - bf16_bits_to_f32(hi >> 16));
 }
 
 // Output column (within the CTA's 128) of B row / accumulator column c.
@@ -239,7 +273,7 @@ __host__ __device__ constexpr int out_col(int c) {
 template <int BS, bool HAS_ZP, bool SF32, int MH>
 __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant__ GemmParams p) {
   using S = Smem<MH, BS, SF32>;
-  constexpr int kAStages = S::kAStages, kWStages = S::kWStages;
+  constexpr int kAStages = S::kAStages, kWStages = S::kWStages, kBStages = S::kBStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles. The offset is added
   // to the shared array itself (not through an integer cast) so that every
@@ -352,13 +386,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         }
         tc_fence_after();
         const uint32_t a_base = smem_addr(smem + S::kA + s * S::kATileBytes);
-        const uint32_t b_base = smem_addr(smem + S::kB + b * kBTileBytes);
+        const uint32_t b_base = smem_addr(smem + S::kB + b * kBSlotBytes);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
 #pragma unroll
-          for (int h = 0; h < MH; ++h)
-            umma_bf16(tmem + h * kBN, smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32),
-                      smem_desc_sw128(b_base + kk * 32), i > 0 || kk > 0);
+          for (int h = 0; h < MH; ++h) {
+            const uint64_t ad = smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32);
+            umma_bf16(tmem + h * kBN, ad, smem_desc_sw128(b_base + kk * 32), i > 0 || kk > 0);
+            umma_bf16(tmem + h * kBN, ad, smem_desc_sw128(b_base + kBTileBytes + kk * 32), true);
+          }
         umma_commit(aempty + s);
         umma_commit(bempty + b);
       }
@@ -394,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
       const unsigned char *codes = smem + S::kCodes + s * kCodeBytes;
       const unsigned char *sc = smem + S::kSc + s * S::kScBytes;
       const uint2 *zp = reinterpret_cast<const uint2 *>(smem + S::kZp + s * S::kZpBytes);
-      unsigned char *btile = smem + S::kB + bslot * kBTileBytes;
+      unsigned char *btile = smem + S::kB + bslot * kBSlotBytes;
       const int blk0 = (kb * kBK) / BS;
       // Scales and zero points of weight rows g, g + 8 for the stage's
       // blocks (zero-filled past the last block).
@@ -433,18 +469,21 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         const int bi = BS < kBK ? (16 * j) / BS : 0;  // block of this k step
         uint32_t r[4];
         codes_to_bf16x2(wv[j], r);
-        const uint32_t v00 = dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi]);  // row g
-        const uint32_t v02 = dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi]);
-        const uint32_t v10 = dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi]);  // row g + 8
-        const uint32_t v12 = dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi]);
-        // K-major 128-byte swizzle: 16-byte chunk (k / 8) XOR (row % 8).
+        uint32_t h00, l00, h02, l02, h10, l10, h12, l12;
+        dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi], h00, l00);  // row g
+        dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi], h02, l02);
+        dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi], h10, l10);  // row g + 8
+        dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi], h12, l12);
+        // K-major 128-byte swizzle: 16-byte chunk (k / 8) XOR (row % 8); the
+        // lo tile sits kBTileBytes after the hi tile.
         const int k0 = 16 * j + 4 * t;
         const int inner = (k0 & 7) * 2;
-        *reinterpret_cast<uint2 *>(btile + r0 * 128 + (((k0 >> 3) ^ (r0 & 7)) * 16) + inner) =
-            make_uint2(v00, v02);
-        *reinterpret_cast<uint2 *>(btile + (r0 + 1) * 128 +
-                                   (((k0 >> 3) ^ ((r0 + 1) & 7)) * 16) + inner) =
-            make_uint2(v10, v12);
+        const int o0 = r0 * 128 + (((k0 >> 3) ^ (r0 & 7)) * 16) + inner;
+        const int o1 = (r0 + 1) * 128 + (((k0 >> 3) ^ ((r0 + 1) & 7)) * 16) + inner;
+        *reinterpret_cast<uint2 *>(btile + o0) = make_uint2(h00, h02);
+        *reinterpret_cast<uint2 *>(btile + o1) = make_uint2(h10, h12);
+        *reinterpret_cast<uint2 *>(btile + kBTileBytes + o0) = make_uint2(l00, l02);
+        *reinterpret_cast<uint2 *>(btile + kBTileBytes + o1) = make_uint2(l10, l12);
       }
       fence_async_smem();  // make the tile visible to the tensor core
       __syncwarp();
@@ -774,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_const
   constexpr int MH = 2;
   constexpr int kTileRows = kBH * MH;
   using S = Smem<MH, BS, SF32>;
-  constexpr int kAStages = S::kAStages, kWStages = S::kWStages;
+  constexpr int kAStages = S::kAStages, kWStages = S::kWStages, kBStages = S::kBStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t *afull = reinterpret_cast<uint64_t *>(smem + S::kBar);
@@ -889,13 +928,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_const
           }
           tc_fence_after();
           const uint32_t a_base = smem_addr(smem + S::kA + s * S::kATileBytes);
-          const uint32_t b_base = smem_addr(smem + S::kB + b * kBTileBytes);
+          const uint32_t b_base = smem_addr(smem + S::kB + b * kBSlotBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
 #pragma unroll
-            for (int h = 0; h < MH; ++h)
-              umma_bf16(tmem + h * kBN, smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32),
-                        smem_desc_sw128(b_base + kk * 32), kb > g.kb0 || kk > 0);
+            for (int h = 0; h < MH; ++h) {
+              const uint64_t ad = smem_desc_sw128(a_base + h * kAHalfBytes + kk * 32);
+              umma_bf16(tmem + h * kBN, ad, smem_desc_sw128(b_base + kk * 32),
+                        kb > g.kb0 || kk > 0);
+              umma_bf16(tmem + h * kBN, ad, smem_desc_sw128(b_base + kBTileBytes + kk * 32),
+                        true);
+            }
           umma_commit(aempty + s);
           umma_commit(bempty + b);
         }
@@ -933,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_const
         const unsigned char *codes = smem + S::kCodes + s * kCodeBytes;
         const unsigned char *sc = smem + S::kSc + s * S::kScBytes;
         const uint2 *zp = reinterpret_cast<const uint2 *>(smem + S::kZp + s * S::kZpBytes);
-        unsigned char *btile = smem + S::kB + bslot * kBTileBytes;
+        unsigned char *btile = smem + S::kB + bslot * kBSlotBytes;
         const int blk0 = (kb * kBK) / BS;
         uint32_t sb0[kBpc], sb1[kBpc], zc0[kBpc], zc1[kBpc];
         float sf0[kBpc], sf1[kBpc];
@@ -967,17 +1010,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_sk_kernel(const __grid_const
           const int bi = BS < kBK ? (16 * q) / BS : 0;
           uint32_t r[4];
           codes_to_bf16x2(wv[q], r);
-          const uint32_t v00 = dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi]);  // row g
-          const uint32_t v02 = dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi]);
-          const uint32_t v10 = dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi]);  // row g + 8
-          const uint32_t v12 = dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi]);
+          uint32_t h00, l00, h02, l02, h10, l10, h12, l12;
+          dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi], h00, l00);  // row g
+          dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi], h02, l02);
+          dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi], h10, l10);  // row g + 8
+          dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi], h12, l12);
           const int k0 = 16 * q + 4 * dt;
           const int inner = (k0 & 7) * 2;
-          *reinterpret_cast<uint2 *>(btile + r0 * 128 + (((k0 >> 3) ^ (r0 & 7)) * 16) + inner) =
-              make_uint2(v00, v02);
-          *reinterpret_cast<uint2 *>(btile + (r0 + 1) * 128 +
-                                     (((k0 >> 3) ^ ((r0 + 1) & 7)) * 16) + inner) =
-              make_uint2(v10, v12);
+          const int o0 = r0 * 128 + (((k0 >> 3) ^ (r0 & 7)) * 16) + inner;
+          const int o1 = (r0 + 1) * 128 + (((k0 >> 3) ^ ((r0 + 1) & 7)) * 16) + inner;
+          *reinterpret_cast<uint2 *>(btile + o0) = make_uint2(h00, h02);
+          *reinterpret_cast<uint2 *>(btile + o1) = make_uint2(h10, h12);
+          *reinterpret_cast<uint2 *>(btile + kBTileBytes + o0) = make_uint2(l00, l02);
+          *reinterpret_cast<uint2 *>(btile + kBTileBytes + o1) = make_uint2(l10, l12);
         }
         fence_async_smem();  // make the tile visible to the tensor core
         __syncwarp();
@@ -1134,14 +1179,14 @@ struct SmemT {
   static constexpr int kHalf = 16 * 1024;
   static constexpr int kA = 0;
   static constexpr int kB = kA + kAStages * kATile;
-  static constexpr int kCodes = kB + kBStages * kBTile;
+  static constexpr int kCodes = kB + kBStagesTf32 * kBTile;
   static constexpr int kSc = kCodes + kWStages * kCodeBytes;
   static constexpr int kScBytes = 2048;
   static constexpr int kZp = kSc + kWStages * kScBytes;
   static constexpr int kZpBytes = 256;
   static constexpr int kBias = kZp + kWStages * kZpBytes;
   static constexpr int kBar = kBias + kBN * 4;
-  static constexpr int kTmemSlot = kBar + (2 * kAStages + 2 * kWStages + 2 * kBStages + 1) * 8;
+  static constexpr int kTmemSlot = kBar + (2 * kAStages + 2 * kWStages + 2 * kBStagesTf32 + 1) * 8;
   static constexpr int kTotal = kTmemSlot + 16;
 };
 static_assert(SmemT::kTotal + 1024 <= 227 * 1024, "one CTA per SM");
@@ -1190,8 +1235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *wfull = aempty + kAStages;
   uint64_t *wempty = wfull + kWStages;
   uint64_t *bfull = wempty + kWStages;
-  uint64_t *bempty = bfull + kBStages;
-  uint64_t *acc_full = bempty + kBStages;
+  uint64_t *bempty = bfull + kBStagesTf32;
+  uint64_t *acc_full = bempty + kBStagesTf32;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kTmemSlot);
   float *sBias = reinterpret_cast<float *>(smem + S::kBias);
 
@@ -1212,7 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(wfull + i, 1);
       mbar_init(wempty + i, kDqWarps);
     }
-    for (int i = 0; i < kBStages; ++i) {
+    for (int i = 0; i < kBStagesTf32; ++i) {
       mbar_init(bfull + i, kDqWarps);
       mbar_init(bempty + i, 1);
     }
@@ -1266,9 +1311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       for (int i = 0; i < nk; ++i) {
-        const int s = i % kAStages, b = i % kBStages;
+        const int s = i % kAStages, b = i % kBStagesTf32;
         if (!mbar_wait(afull + s, (i / kAStages) & 1) ||
-            !mbar_wait(bfull + b, (i / kBStages) & 1)) {
+            !mbar_wait(bfull + b, (i / kBStagesTf32) & 1)) {
           record_fault(&g_fault_gemm, kFaultGemmWait);
           fault = true;
           break;
@@ -1299,9 +1344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int i = 0; i < nk; ++i) {
-      const int s = i % kWStages, bslot = i % kBStages;
+      const int s = i % kWStages, bslot = i % kBStagesTf32;
       if (!mbar_wait(wfull + s, (i / kWStages) & 1) ||
-          (i >= kBStages && !mbar_wait(bempty + bslot, ((i / kBStages) - 1) & 1))) {
+          (i >= kBStagesTf32 && !mbar_wait(bempty + bslot, ((i / kBStagesTf32) - 1) & 1))) {
         record_fault(&g_fault_gemm, kFaultGemmWait);
         fault = true;
         break;

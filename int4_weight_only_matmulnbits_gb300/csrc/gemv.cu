@@ -98,7 +98,8 @@ struct GemvParams {
   unsigned long long *amax;
   // Code-book weights (the bitsandbytes-style format): the 16 fp32 values,
   // or null for the affine codes. Each CTA turns them into a 256-entry table
-  // of bf16 pairs (code[lo], code[hi]) indexed by two codes.
+  // indexed by two codes: the bf16 pair (code[lo], code[hi]) rounded, and the
+  // pair of their remainders, so that each value is hi + lo.
   const float *code;
   int st_sc, st_zp;  // offsets of scales and zero points in a stage (128-aligned)
   int nbs, nps;      // blocks and zero-point word pairs per stage and tile
@@ -108,13 +109,16 @@ struct GemvParams {
 };
 
 // Four bf16x2 registers of eight codes through the pair table: register i
-// takes the codes at bits 4i and 16 + 4i, as codes_to_bf16x2 does.
-__device__ __forceinline__ void codes_to_lut(uint32_t w, const uint32_t *pair,
-                                             uint32_t (&r)[4]) {
+// takes the codes at bits 4i and 16 + 4i, as codes_to_bf16x2 does; r holds
+// the rounded code-book values, rl their remainders.
+__device__ __forceinline__ void codes_to_lut(uint32_t w, const uint2 *pair, uint32_t (&r)[4],
+                                             uint32_t (&rl)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t x = w >> (4 * i);
-    r[i] = pair[(x & 0xFu) | ((x >> 12) & 0xF0u)];
+    const uint2 e = pair[(x & 0xFu) | ((x >> 12) & 0xF0u)];
+    r[i] = e.x;
+    rl[i] = e.y;
   }
 }
 
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   float *sRed = reinterpret_cast<float *>(smem + p.off_red);
   float *sPart = reinterpret_cast<float *>(smem + p.off_part);
   float *sNrm = reinterpret_cast<float *>(smem + p.off_nrm);
-  uint32_t *sPair = reinterpret_cast<uint32_t *>(smem + p.off_lut);
+  uint2 *sPair = reinterpret_cast<uint2 *>(smem + p.off_lut);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
   uint64_t *empty = full + kMaxStages;
   uint64_t *abar = empty + kMaxStages;  // activation copy
@@ -353,9 +357,16 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     bool fault = false;
     if (p.amax && tid < kGemvMaxM)
       reinterpret_cast<unsigned long long *>(sNrm + kGemvMaxM)[tid] = 0ull;
-    if (CODE && tid < 256)
-      sPair[tid] = bf16_bits(__ldg(p.code + (tid & 15))) |
-                   (bf16_bits(__ldg(p.code + (tid >> 4))) << 16);
+    if (CODE && tid < 256) {
+      // Each code-book value c as bf16 hi = round(c) and lo = round(c - hi)
+      // (c - hi is exact in fp32): hi + lo is within 2^-16 |c| of c, where
+      // hi alone could be 2^-8 |c| off.
+      const float c0 = __ldg(p.code + (tid & 15)), c1 = __ldg(p.code + (tid >> 4));
+      const uint32_t h0 = bf16_bits(c0), h1 = bf16_bits(c1);
+      const uint32_t l0 = bf16_bits(c0 - bf16_bits_to_f32(h0));
+      const uint32_t l1 = bf16_bits(c1 - bf16_bits_to_f32(h1));
+      sPair[tid] = make_uint2(h0 | (h1 << 16), l0 | (l1 << 16));
+    }
     if (p.norm) {
       // r[m] from the whole row (this CTA may stage only part of K): per-warp
       // partial sums of squares, then a fixed-order sum over the warps.
@@ -560,14 +571,18 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         // One 16-wide k step of chunk ci (relative to cst): convert the
         // lane's codes, multiply with the activation fragments; the first
         // step of a block starts its sums from zero.
+        // Code-book values are hi + lo: a second MMA with the remainders
+        // (their product with the activations' fp32 remainder is below
+        // 2^-16 of the term and left out).
         auto kstep = [&](uint32_t w, int ci, int jj, bool first, float (&d)[MT][4]) {
-          uint32_t wf[4];
-          if (CODE) codes_to_lut(w, sPair, wf);
+          uint32_t wf[4], wl[4];
+          if (CODE) codes_to_lut(w, sPair, wf, wl);
           else codes_to_bf16x2(w, wf);
           const int ko = ci * kChunkK + 16 * jj;
           if (mok0) bfrag0 = *reinterpret_cast<const uint2 *>(ap0 + ko);
           if (first) mma_bf16_16816_zero(d[0], wf, bfrag0.x, bfrag0.y);
           else mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
+          if (CODE) mma_bf16_16816(d[0], wl, bfrag0.x, bfrag0.y);
           if (two) {
             if (mok0) bfrag0 = *reinterpret_cast<const uint2 *>(ap0 + lo_off + ko);
             mma_bf16_16816(d[0], wf, bfrag0.x, bfrag0.y);
@@ -576,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             if (mok1) bfrag1 = *reinterpret_cast<const uint2 *>(ap1 + ko);
             if (first) mma_bf16_16816_zero(d[MT - 1], wf, bfrag1.x, bfrag1.y);
             else mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
+            if (CODE) mma_bf16_16816(d[MT - 1], wl, bfrag1.x, bfrag1.y);
             if (two) {
               if (mok1) bfrag1 = *reinterpret_cast<const uint2 *>(ap1 + lo_off + ko);
               mma_bf16_16816(d[MT - 1], wf, bfrag1.x, bfrag1.y);
@@ -819,7 +835,7 @@ bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   L.off_nrm = static_cast<int>(off);
   off += align16(kGemvMaxM * 4 + kGemvMaxM * 8);  // r[m], then the ArgMax keys
   L.off_lut = static_cast<int>(off);
-  off += 256 * 4;  // code-book pair table
+  off += a.code ? 256 * 8 : 0;  // code-book pair table (rounded values and remainders)
   L.off_bar = static_cast<int>(off);
   off += (2 * kMaxStages + 1) * 8;
   off = align128(off);

@@ -4,10 +4,12 @@ path MNB_PATH_GEMM_STREAMK) against the oracle, through the C ABI.
 The schedule splits the product's (256 x 128 output tile, 64-wide k stage)
 units evenly over two CTAs per SM; a tile that several CTAs share is
 completed by whichever of them finishes last, adding the fp32 partial tiles
-in the order of their k stages. Each product is the one the
-whole-tile kernel computes (bf16-rounded dequantised weights, fp32
-accumulation), summed in a different but fixed order, so the same bound
-applies (tests/tolerance.py) and repeated runs are bitwise equal.
+in the order of their k stages. Each product is the one the whole-tile
+kernel computes (each dequantised weight as an exact bf16 hi + lo pair,
+fp32 accumulation), summed in a different but fixed order, so the same
+stated bound applies (tests/tolerance.py), also on inputs built so that a
+single rounding of every weight would err the same way
+(tests/adversarial.py), and repeated runs are bitwise equal.
 
 The shapes cover: one tile split over many CTAs (one output tile, 64 k
 stages), CTAs whose ranges cross tiles (many tiles of few stages), ragged M,
@@ -24,6 +26,7 @@ import int4_weight_only_matmulnbits_gb300 as mnb
 import oracle
 from int4_weight_only_matmulnbits_gb300 import binding
 from int4_weight_only_matmulnbits_gb300.workloads import make_problem
+from tests.adversarial import aligned_rounding_problem
 from tests.tolerance import check
 
 pytestmark = pytest.mark.gpu
@@ -79,6 +82,19 @@ def test_streamk_tiles_and_tails(dev, bs, with_zp, scale_f32):
         check(Y, R, mag, f"streamk M{M} N{N} K{K} bs{bs} zp{with_zp} sf32{scale_f32}")
         assert flags_clear(ws)
     assert mnb.mnb_fault_status() == 0
+
+
+@pytest.mark.parametrize("scale_dtype", [torch.bfloat16, torch.float32], ids=["sbf16", "sf32"])
+def test_streamk_adversarial_rounding_within_stated_bound(dev, scale_dtype):
+    ws = mnb.mnb_matmul_workspace(dev)
+    prob = aligned_rounding_problem(300, 700, 64, 8, scale_dtype=scale_dtype,
+                                    zero_points=True, seed=3)
+    w = prepack(prob, dev)
+    Y = mnb.mnb_matmul(prob.A.to(dev), w, None, path="gemm_streamk", workspace=ws)
+    torch.cuda.synchronize()
+    R, mag = ref(prob)
+    check(Y, R, mag, "streamk adversarial")
+    assert flags_clear(ws)
 
 
 def test_streamk_and_whole_tiles_agree_and_repeat_bitwise(dev):
