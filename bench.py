@@ -8,15 +8,21 @@ U[0.002, 0.01]): q 2560->4096, k/v 2560->1024, o 4096->2560, gate/up
 own seeded codes and scales, all resident in HBM before timing.
 
 The step follows the model's data flow: q, k and v read one activation row
-and run as one fused-N launch (mnb_matmul_grouped); gate and up run as one
-gated-MLP launch that stores SiLU(gate) * up (mnb_matmul_gate_up); o, down
-and lm_head each read their own row. That is 4 launches per layer and 145
-per step, replayed as one CUDA graph. The step's bytes exceed the 129 MB L2
-many times over, so no flush is needed.
+and run as one fused-N call (mnb_matmul_grouped); gate and up run as one
+gated-MLP call that stores SiLU(gate) * up (mnb_matmul_gate_up); o, down
+and lm_head each read their own row. That is 4 calls per layer and 145 per
+step, recorded once by the library as one CUDA graph (mnb_graph_build) and
+run with one mnb_graph_run per step; `e2e` runs it with
+mnb_graph_run_from_host, which copies the step's activation rows in from
+pinned host memory and its outputs back every step. The step's bytes exceed
+the 129 MB L2 many times over, so no flush is needed.
 
-Also measured, outside the timed region of the headline number: the prefill
-GEMM at M = 2048 over the seven Qwen3-4B projection shapes (TFLOP/s), when
-the tensor-core path is available.
+Also measured after the headline's timed region, each with its roofline,
+an oracle baseline and a clock record: the prefill GEMM at M = 2048 and
+M = 512 over the seven Qwen3-4B projection shapes (TFLOP/s), the Qwen3-0.6B
+decode step (fp32 activations, bs 32, zero points), the single
+1024 x 3072 GEMV (cold and hot L2) and a condensed GEMV / tensor-core
+crossover; and the same step as one persistent chain launch.
 
 `--impl reference` times the CPU oracle on a bounded sample of the same
 workload instead (there is no runnable reference implementation of this
@@ -90,7 +96,7 @@ class ClockSampler:
             self.f = open(self.out, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -127,31 +133,43 @@ class ClockSampler:
 # CPU oracle leg
 # ----------------------------------------------------------------------------
 
-def oracle_sample(budget_s: float, seed_base: int = 3000):
-    """Times the oracle (single thread) over the decode step's projections in
+def oracle_sample(budget_s: float, seed_base: int = 3000, spec=None):
+    """Times the oracle (single thread) over a decode step's projections in
     order until about budget_s seconds of CPU work; returns (bytes, seconds,
-    description)."""
+    description). spec: the step (default: the Qwen3-4B step)."""
     import torch
 
     import oracle
-    from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_4B, make_problem
+    from int4_weight_only_matmulnbits_gb300 import workloads
+    spec = spec or STEP_4B
+    model = getattr(workloads, spec["model"])
+    adt = torch.float32 if spec["a_dtype"] == "f32" else torch.bfloat16
     oracle.load()
-    projs = [(l, p) for l in range(QWEN3_4B["layers"]) for p in QWEN3_4B["projections"]]
+    projs = [(l, p) for l in range(model["layers"]) for p in model["projections"]]
     done_bytes, spent, names = 0, 0.0, []
     for i, (layer, p) in enumerate(projs):
-        prob = make_problem(1, p.N, p.K, 128, dtype=torch.bfloat16, seed=seed_base + i,
-                            scale_range=(0.002, 0.01))
+        prob = workloads.make_problem(1, p.N, p.K, spec["bs"], dtype=adt, zero_points=spec["zp"],
+                                      seed=seed_base + i, scale_range=spec["scale_range"])
+        if spec["scale_dtype"] == "f32":
+            prob.scales = prob.scales.float()
         t0 = time.perf_counter()
-        oracle.matmulnbits(prob.A, prob.B, prob.scales, None, None, N=p.N, K=p.K,
-                           block_size=128)
+        oracle.matmulnbits(prob.A, prob.B, prob.scales, prob.zero_points, None, N=p.N, K=p.K,
+                           block_size=spec["bs"])
         spent += time.perf_counter() - t0
         done_bytes += prob.algorithmic_bytes()
         names.append(f"L{layer}.{p.name}")
         if spent >= budget_s:
             break
-    desc = (f"first {len(names)} projections of the decode step ({names[0]}..{names[-1]}, "
-            f"{done_bytes / 1e6:.1f} MB algorithmic), oracle single-threaded")
+    desc = (f"first {len(names)} projections of the {spec['model']} decode step "
+            f"({names[0]}..{names[-1]}, {done_bytes / 1e6:.1f} MB algorithmic), "
+            f"oracle single-threaded")
     return done_bytes, spent, desc
+
+
+def cpu_leg(budget_s, spec=None, seed_base=3000):
+    nbytes, secs, desc = oracle_sample(budget_s, seed_base, spec)
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "cpu": cpu_model(),
+            "kind": "oracle", "sample": desc}
 
 
 def run_reference(args, rank, world):
@@ -185,30 +203,43 @@ def run_reference(args, rank, world):
 # GPU leg
 # ----------------------------------------------------------------------------
 
-def build_decode_step(dev, seed_base=5000, keep=None):
+STEP_4B = dict(model="QWEN3_4B", a_dtype="bf16", bs=128, zp=False, scale_dtype="bf16",
+               scale_range=(0.002, 0.01))
+STEP_0P6B = dict(model="QWEN3_0P6B", a_dtype="f32", bs=32, zp=True, scale_dtype="f32",
+                 scale_range=(0.005, 0.02))
+
+
+def build_decode_step(dev, seed_base=5000, keep=None, spec=STEP_4B):
     """Prepacked weights, activations and outputs of one decode step, all
-    resident on dev, as a list of launches: (weights, activation row,
-    outputs). Weights are drawn on the device from a seeded generator
-    (2 GB would take minutes on the host). `keep`: names of launches whose
-    raw inputs (activation row, and per weight its codes and scales) are
-    also returned as host tensors in a fifth element, for parity checks."""
+    resident on dev, as a list of launches: (name, weights, activation row,
+    outputs). Per layer: q/k/v on one row (one fused-N launch), o, the gated
+    gate/up pair, down; then lm_head. Weights are drawn on the device from a
+    seeded generator (2 GB would take minutes on the host). `keep`: names of
+    launches whose raw inputs (activation row, and per weight its codes and
+    scales) are also returned as host tensors in a fifth element, for parity
+    checks (steps without zero points)."""
     import torch
 
     import int4_weight_only_matmulnbits_gb300 as mnb
-    from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_4B
-    P = {p.name: p for p in QWEN3_4B["projections"]}
+    from int4_weight_only_matmulnbits_gb300 import workloads
+    model = getattr(workloads, spec["model"])
+    adt = torch.float32 if spec["a_dtype"] == "f32" else torch.bfloat16
+    sdt = torch.float32 if spec["scale_dtype"] == "f32" else torch.bfloat16
+    bs, zp = spec["bs"], spec["zp"]
+    lo, hi = spec["scale_range"]
+    P = {p.name: p for p in model["projections"]}
     groups = [("qkv", [P["q"], P["k"], P["v"]]), ("o", [P["o"]]),
               ("gate_up", [P["gate"], P["up"]]), ("down", [P["down"]])]
-    plan = [(f"L{l}.{name}", ps) for l in range(QWEN3_4B["layers"]) for name, ps in groups]
-    plan.append(("lm_head", [QWEN3_4B["lm_head"]]))
-    bs = 128
+    plan = [(f"L{l}.{name}", ps) for l in range(model["layers"]) for name, ps in groups]
+    plan.append(("lm_head", [model["lm_head"]]))
     g = torch.Generator(device=dev)
     a_total = sum(ps[0].K for _, ps in plan)
     # The gated-MLP launch writes one output for its two weights.
     y_total = sum(ps[0].N if name.endswith("gate_up") else sum(p.N for p in ps)
                   for name, ps in plan)
-    A_all = torch.empty(a_total, dtype=torch.bfloat16, device=dev)
-    Y_all = torch.empty(y_total, dtype=torch.bfloat16, device=dev)
+    A_all = torch.empty(a_total, dtype=adt, device=dev)
+    Y_all = torch.empty(y_total, dtype=adt, device=dev)
+    es = A_all.element_size()
     ao = yo = 0
     algo_bytes = 0
     launches = []
@@ -219,9 +250,9 @@ def build_decode_step(dev, seed_base=5000, keep=None):
         nb = -(-K // bs)
         A = A_all[ao:ao + K].view(1, K)
         g.manual_seed(seed)
-        A.copy_(torch.randn(1, K, device=dev, generator=g).to(torch.bfloat16))
+        A.copy_(torch.randn(1, K, device=dev, generator=g).to(adt))
         ao += K
-        algo_bytes += K * 2
+        algo_bytes += K * es
         ws, Ys = [], []
         paired = name.endswith("gate_up")
         for i, p in enumerate(ps):
@@ -229,23 +260,45 @@ def build_decode_step(dev, seed_base=5000, keep=None):
             g.manual_seed(seed)
             B = torch.randint(0, 256, (p.N, nb, bs // 2), dtype=torch.uint8, device=dev,
                               generator=g)
-            S = (torch.rand(p.N, nb, device=dev, generator=g) * 0.008 + 0.002).to(torch.bfloat16)
-            ws.append(mnb.mnb_prepack(B, S, None, p.N, K, bs))
+            S = (torch.rand(p.N, nb, device=dev, generator=g) * (hi - lo) + lo).to(sdt)
+            Z = (torch.randint(0, 256, (p.N, (nb + 1) // 2), dtype=torch.uint8, device=dev,
+                               generator=g) if zp else None)
+            ws.append(mnb.mnb_prepack(B, S, Z, p.N, K, bs))
             if keep and name in keep:
                 kept.setdefault(name, {"A": A.cpu(), "weights": []})["weights"].append(
                     (B.cpu(), S.cpu(), p.N, K))
-            del B, S
-            algo_bytes += p.N * nb * bs // 2 + p.N * nb * 2
+            del B, S, Z
+            algo_bytes += p.N * nb * bs // 2 + p.N * nb * S_bytes(sdt)
+            algo_bytes += p.N * ((nb + 1) // 2) if zp else 0
             if not paired or i == 0:
                 Ys.append(Y_all[yo:yo + p.N].view(1, p.N))
                 yo += p.N
-                algo_bytes += p.N * 2
+                algo_bytes += p.N * es
         launches.append((name, ws, A, Ys))
         seed += 1
     torch.cuda.synchronize()
     if keep is not None:
         return launches, A_all, Y_all, algo_bytes, kept
     return launches, A_all, Y_all, algo_bytes
+
+
+def S_bytes(dt):
+    import torch
+    return 4 if dt == torch.float32 else 2
+
+
+def step_ops(mnb, launches):
+    """The launches of a decode step as op descriptors for mnb_graph_build:
+    q, k and v share their activation row (one fused-N call), gate and up
+    form a gated pair; array order is launch order."""
+    ops = []
+    for name, ws, A, Ys in launches:
+        if name.endswith("gate_up"):
+            ops.append(mnb.ChainOp(A, ws[0], Ys[0], up=ws[1]))
+        else:
+            for w, Y in zip(ws, Ys):
+                ops.append(mnb.ChainOp(A, w, Y))
+    return ops
 
 
 def build_decode_chain(mnb, launches):
@@ -301,6 +354,42 @@ def time_region(fn, steps, stream):
     return start.elapsed_time(end) / 1e3
 
 
+def time_steps(fn, steps, stream):
+    """Device time of each of `steps` calls of fn (CUDA events around each, on
+    `stream`); returns (total seconds, per-call seconds)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]) / 1e3, per
+
+
+def pct(xs, q):
+    xs = sorted(xs)
+    if not xs:
+        return None
+    k = (len(xs) - 1) * q / 100.0
+    i = int(k)
+    return xs[i] if i + 1 >= len(xs) else xs[i] + (xs[i + 1] - xs[i]) * (k - i)
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def lm_head_fusions(mnb, lm_launch, dev, steps=50):
     """The step's lm_head launch alone and with the fused final RMSNorm and
     greedy ArgMax (mnb_matmul_rmsnorm), us per call on the same stream;
@@ -324,15 +413,15 @@ def lm_head_fusions(mnb, lm_launch, dev, steps=50):
     return out
 
 
-def prefill_measure(dev, steps=5, warmup=3):
-    """TFLOP/s of the tensor-core path at M=2048 over the seven Qwen3-4B
+def prefill_measure(dev, steps=5, warmup=3, M=2048):
+    """TFLOP/s of the tensor-core path at M rows over the seven Qwen3-4B
     projection shapes (bf16 A, bs 128, zero points, bias), each timed alone;
     None when the path is not available."""
     import torch
 
     import int4_weight_only_matmulnbits_gb300 as mnb
     from int4_weight_only_matmulnbits_gb300.workloads import QWEN3_4B
-    M, bs = 2048, 128
+    bs = 128
     g = torch.Generator(device=dev)
     total_flops, total_s, per = 0, 0.0, {}
     stream = torch.cuda.current_stream()
@@ -364,6 +453,112 @@ def prefill_measure(dev, steps=5, warmup=3):
             "per_projection_tflops": per}
 
 
+def measure_step(mnb, dev, spec, steps, warmup, seed_base=5000, local=0, clock_log=None,
+                 dist=None):
+    """One decode step recorded as a CUDA graph through the C ABI
+    (mnb_graph_build) and timed: device only (mnb_graph_run, clocks sampled
+    during the timed region) and end to end (mnb_graph_run_from_host: the
+    step's activation rows copied in from pinned host memory, its outputs
+    copied back, every step)."""
+    import torch
+    launches, A_all, Y_all, algo_bytes = build_decode_step(dev, seed_base, spec=spec)
+    graph = mnb.mnb_graph_build(step_ops(mnb, launches))
+    assert graph.calls == len(launches), (graph.calls, len(launches))
+    stream = torch.cuda.current_stream()
+    for _ in range(max(warmup, 3)):
+        graph.run()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local, clock_log)
+    if dist:
+        dist.barrier()
+    sampler.start()
+    time.sleep(0.3)
+    t, per = time_steps(graph.run, steps, stream)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    A_host = torch.empty(A_all.shape, dtype=A_all.dtype).pin_memory()
+    A_host.copy_(A_all.cpu())
+    Y_host = torch.empty(Y_all.shape, dtype=Y_all.dtype).pin_memory()
+    e2e_step = lambda: graph.run_from_host(A_host, A_all, Y_all, Y_host)
+    for _ in range(3):
+        e2e_step()
+    t_e2e, _ = time_steps(e2e_step, steps, stream)
+    return dict(launches=launches, A_all=A_all, Y_all=Y_all, algo_bytes=algo_bytes,
+                graph=graph, t=t, per=per, t_e2e=t_e2e, clocks=clocks,
+                h2d=A_all.numel() * A_all.element_size(),
+                d2h=Y_all.numel() * Y_all.element_size())
+
+
+def clocked(local, fn):
+    """fn() with the SM clocks sampled while it runs: (result, clocks)."""
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    try:
+        out = fn()
+    finally:
+        clocks = sampler.stop()
+    return out, clocks
+
+
+def single_gemv(mnb, dev, reps=30):
+    """The single GEMV workload (A fp32 [1, 1024], B [3072, 1024] bs 32, fp32
+    scales, no zero points, no bias): device time per launch with L2 flushed
+    before each launch (cold) and back to back with the 1.98 MB weight left in
+    L2 (hot)."""
+    import torch
+    from int4_weight_only_matmulnbits_gb300.workloads import make_problem
+    prob = make_problem(1, 3072, 1024, 32, dtype=torch.float32, seed=0)
+    w = mnb.mnb_prepack(prob.B.to(dev), prob.scales.to(dev), None, 3072, 1024, 32)
+    A = prob.A.to(dev)
+    Y = torch.empty(1, 3072, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    fn = lambda: mnb.mnb_matmul(A, w, None, out=Y, workspace=None)
+    cold = _cold_launch_us(fn, reps, flush)
+    # Hot: 20 back-to-back launches replayed from one CUDA graph, so that no
+    # host gap sits between them.
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(20):
+            fn()
+    for _ in range(3):
+        g.replay()
+    t, per = time_steps(g.replay, reps, torch.cuda.current_stream())
+    hot = statistics.median(per) * 1e6 / 20
+    return prob, {"cold_us": cold, "hot_us": hot, "algorithmic_bytes": prob.algorithmic_bytes()}
+
+
+def crossover(mnb, dev, flush):
+    """Condensed GEMV / tensor-core crossover: device time per launch (L2
+    flushed, median of 5) of both kernels and of the dispatch, on gate
+    2560->9728 and down 9728->2560, bf16 A, bs 128, no zero points."""
+    import torch
+    rows = []
+    for name, N, K in (("gate", 9728, 2560), ("down", 2560, 9728)):
+        w, _ = _weights(dev, N, K, 128, torch.bfloat16, False, 21)
+        for M in (1, 8, 16, 32, 64, 256):
+            A = torch.randn(M, K, device=dev).to(torch.bfloat16)
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            row = {"shape": name, "M": M}
+            for path in ("gemv", "gemm", "auto"):
+                try:
+                    mnb.mnb_matmul(A, w, None, out=Y, path=path, workspace=None)
+                except mnb.MnbError:
+                    continue
+                row[path + "_us"] = round(_cold_launch_us(
+                    lambda: mnb.mnb_matmul(A, w, None, out=Y, path=path, workspace=None), 5,
+                    flush), 2)
+            rows.append(row)
+    return rows
+
+
 def run_gpu(args, rank, world, dist):
     import torch
 
@@ -373,57 +568,12 @@ def run_gpu(args, rank, world, dist):
     dev = torch.device("cuda", local)
     mnb.build_library()
     mnb.load()
-    hbm_peak, _, _, peak_kind = peaks()
+    hbm_peak, bf16_peak, _, peak_kind = peaks()
 
-    launches, A_all, Y_all, algo_bytes = build_decode_step(dev)
-    stream = torch.cuda.Stream()
-    torch.cuda.synchronize()
-
-    def step_eager():
-        for name, ws, A, Ys in launches:
-            run_launch(mnb, name, ws, A, Ys)
-
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step_eager()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step_eager()
-    torch.cuda.synchronize()
-    launches_per_step = len(launches)
-
-    warmup = max(args.warmup, 3)
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-
-    sampler = ClockSampler(local, args.clock_log)
-    if dist:
-        dist.barrier()
-    sampler.start()
-    time.sleep(0.3)
-    torch.cuda.synchronize()
-    t = time_region(graph.replay, args.steps, torch.cuda.current_stream())
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-
-    # end to end: host activations in, host results out, every step
-    A_host = torch.empty(A_all.shape, dtype=A_all.dtype).pin_memory()
-    A_host.copy_(A_all.cpu())
-    Y_host = torch.empty(Y_all.shape, dtype=Y_all.dtype).pin_memory()
+    m = measure_step(mnb, dev, STEP_4B, args.steps, args.warmup, local=local,
+                     clock_log=args.clock_log, dist=dist)
+    launches, algo_bytes, graph = m["launches"], m["algo_bytes"], m["graph"]
     cur = torch.cuda.current_stream()
-
-    def step_e2e():
-        A_all.copy_(A_host, non_blocking=True)
-        graph.replay()
-        Y_host.copy_(Y_all, non_blocking=True)
-
-    for _ in range(3):
-        step_e2e()
-    t_e2e = time_region(step_e2e, args.steps, cur)
 
     # The same step as one persistent launch (mnb_chain_run), for comparison;
     # not the headline: the graph of launches is faster on this workload.
@@ -432,7 +582,7 @@ def run_gpu(args, rank, world, dist):
         chain.run()
     t_chain = time_region(chain.run, args.steps, cur)
 
-    ts = torch.tensor([t, t_e2e, t_chain], device=dev, dtype=torch.float64)
+    ts = torch.tensor([m["t"], m["t_e2e"], t_chain], device=dev, dtype=torch.float64)
     if dist:
         dist.all_reduce(ts, op=dist.ReduceOp.MAX)
     t, t_e2e, t_chain = ts.tolist()
@@ -442,27 +592,29 @@ def run_gpu(args, rank, world, dist):
     value = algo_bytes * args.steps * world / t / 1e9
     e2e = algo_bytes * args.steps * world / t_e2e / 1e9
     per_gpu = algo_bytes * args.steps / t / 1e9
-
-    prefill = None if args.skip_prefill else prefill_measure(dev)
-    fusions = lm_head_fusions(mnb, launches[-1], dev)
+    per = [x * 1e3 for x in m["per"]]
+    warmup = max(args.warmup, 3)
+    extras = world == 1 and not args.skip_extras
     cpu = None
     if world == 1 and not args.skip_cpu:
-        nbytes, secs, desc = oracle_sample(args.cpu_budget)
-        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": desc}
+        cpu = cpu_leg(args.cpu_budget)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup,
-        "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+        "ms_per_step": 1e3 * t / args.steps,
+        "ms_per_step_p10": pct(per, 10), "ms_per_step_p50": pct(per, 50),
+        "ms_per_step_p90": pct(per, 90), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "block_size": 128, "a_dtype": "bf16",
                    "weights_per_step": sum(len(ws) for _, ws, _, _ in launches),
-                   "launches_per_step": launches_per_step,
+                   "launches_per_step": len(launches),
                    "algorithmic_bytes_per_step": algo_bytes,
                    "l2": "inputs larger than L2 (2.08 GB per step vs 129 MB)",
-                   "launch": "one CUDA graph per step: per layer fused qkv, o, gated-MLP "
-                             "gate+up (SiLU(gate)*up), down, then lm_head (145 launches), "
-                             "programmatic dependent launch",
+                   "launch": "one CUDA graph per step recorded by the library "
+                             "(mnb_graph_build, run with mnb_graph_run): per layer fused "
+                             "qkv, o, gated-MLP gate+up (SiLU(gate)*up), down, then lm_head "
+                             f"({graph.calls} calls, {graph.kernels} kernels), programmatic "
+                             "dependent launch",
                    "parallelism": f"replicas x{world}"},
         "hbm_fraction": per_gpu / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": hbm_peak,
@@ -471,22 +623,91 @@ def run_gpu(args, rank, world, dist):
                      "kernel": "gemv_kernel (every launch of the step)",
                      "achieved_basis": "algorithmic bytes of the step / device time of the "
                                        "step (= bytes per launch / mean launch time)",
-                     "algorithmic_bytes_per_launch": algo_bytes / launches_per_step,
+                     "algorithmic_bytes_per_launch": algo_bytes / len(launches),
                      "traffic_basis": "ncu dram read+write per launch, mean over the "
-                                      "step's 145 launches; null if the kernel changed"},
-        "e2e": {"value": e2e, "unit": "GB/s",
-                "h2d_bytes_per_step": A_all.numel() * A_all.element_size(),
-                "d2h_bytes_per_step": Y_all.numel() * Y_all.element_size()},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
-        "prefill": prefill,
-        "lm_head_fusions": fusions,
+                                      "step's launches; null if the kernel changed"},
+        "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"],
+                "api": "mnb_graph_run_from_host (C ABI): pinned host activations in, the "
+                       "step, outputs back to pinned host memory, on one stream"},
+        "gpu_launches": graph.kernels * args.steps,
+        "clocks": m["clocks"],
+        "cpu_baseline": cpu,
         "decode_chain": {"value": algo_bytes * args.steps / t_chain / 1e9, "unit": "GB/s",
                          "ms_per_step": 1e3 * t_chain / args.steps, "launches_per_step": 1,
                          "note": "the same step and dependencies as one persistent "
                                  "cooperative launch (mnb_chain_run)"},
-        "cpu_baseline": cpu,
     }
+    if extras:
+        line["lm_head_fusions"] = lm_head_fusions(mnb, launches[-1], dev)
+        del chain, m, launches, graph
+        torch.cuda.empty_cache()
+        flops_peak = {"bound": "tensor", "peak": bf16_peak, "unit": "TFLOP/s",
+                      "peak_kind": peak_kind + " bf16 burst (cuBLAS)"}
+        for key, M in (("prefill", 2048), ("prefill_m512", 512)):
+            pf, clk = clocked(local, lambda: prefill_measure(dev, M=M))
+            if pf is not None:
+                pf["roofline"] = dict(flops_peak, achieved=pf["value"],
+                                      frac=pf["value"] / bf16_peak, traffic=None,
+                                      kernel="gemm_kernel / gemm_sk_kernel (7 shapes)")
+                pf["clocks"] = clk
+                pf["workload"] = (f"Qwen3-4B prefill projections, M={M}, bf16 A, bs 128, "
+                                  "zero points, fp32 bias, each shape timed alone")
+                pf["cpu_baseline"] = None if args.skip_cpu else dict(
+                    cpu_leg(3.0, seed_base=3500),
+                    note="the oracle's GB/s on decode-step projections; its prefill rate "
+                         "is the same dot products (not run again at M rows)")
+            line[key] = pf
+        m6 = measure_step(mnb, dev, STEP_0P6B, args.steps, warmup, seed_base=7000,
+                          local=local)
+        b6 = m6["algo_bytes"]
+        g6 = b6 * args.steps / m6["t"] / 1e9
+        line["decode_step_qwen3_0p6b"] = {
+            "workload": "Qwen3-0.6B decode step projections, M=1, fp32 A, bs 32, uint4 zero "
+                        "points, fp32 scales (28 layers + lm_head)",
+            "value": g6, "unit": "GB/s", "ms_per_step": 1e3 * m6["t"] / args.steps,
+            "ms_per_step_p10": pct([x * 1e3 for x in m6["per"]], 10),
+            "ms_per_step_p90": pct([x * 1e3 for x in m6["per"]], 90),
+            "algorithmic_bytes_per_step": b6, "launches_per_step": len(m6["launches"]),
+            "e2e": {"value": b6 * args.steps / m6["t_e2e"] / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": m6["h2d"], "d2h_bytes_per_step": m6["d2h"]},
+            "roofline": {"bound": "hbm", "achieved": g6, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": g6 / hbm_peak, "traffic": None, "peak_kind": peak_kind},
+            "clocks": m6["clocks"],
+            "cpu_baseline": None if args.skip_cpu else cpu_leg(3.0, STEP_0P6B, 3700),
+        }
+        del m6
+        torch.cuda.empty_cache()
+        prob1, s1 = single_gemv(mnb, dev)
+        nb1 = s1["algorithmic_bytes"]
+        cold_gbs = nb1 / s1["cold_us"] / 1e3
+        t0 = time.perf_counter()
+        import oracle
+        oracle.load()
+        reps = 0
+        while time.perf_counter() - t0 < 2.0:
+            oracle.matmulnbits(prob1.A, prob1.B, prob1.scales, None, None, N=3072, K=1024,
+                               block_size=32)
+            reps += 1
+        o_s = (time.perf_counter() - t0) / reps
+        line["single_gemv"] = {
+            "workload": "single MatMulNBits GEMV, A fp32 [1,1024], B [3072,1024] bs 32, fp32 "
+                        "scales, no zero points, no bias, seed 0",
+            "cold_us": s1["cold_us"], "hot_us": s1["hot_us"], "algorithmic_bytes": nb1,
+            "value": cold_gbs, "unit": "GB/s (cold L2)", "hot_GBps": nb1 / s1["hot_us"] / 1e3,
+            "roofline": {"bound": "hbm", "achieved": cold_gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": cold_gbs / hbm_peak, "traffic": None,
+                         "peak_kind": peak_kind,
+                         "note": "cold: L2 flushed before every launch; hot (weight in L2) "
+                                 "is not bounded by HBM"},
+            "cpu_baseline": {"value": nb1 / o_s / 1e9, "unit": "GB/s", "cores": 1,
+                             "cpu": cpu_model(), "kind": "oracle",
+                             "sample": f"the whole GEMV, {reps} runs"},
+        }
+        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+        cross, clk = clocked(local, lambda: crossover(mnb, dev, flush))
+        line["crossover"] = {"unit": "us per launch, L2 flushed, median of 5", "rows": cross,
+                             "clocks": clk}
     print(json.dumps(line), flush=True)
 
 
@@ -613,11 +834,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
-    ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--clock-log", default=None,
                     help="file for the raw nvidia-smi clock samples of the timed region "
                          "(default: a private temporary file)")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="only the headline decode step (no prefill, Qwen3-0.6B step, single "
+                         "GEMV or crossover keys)")
     ap.add_argument("--case", default=None, choices=sorted(CASES) + ["step", "sweep"],
                     help="run one kernel shape (or one eager decode step per --steps, or "
                          "the GEMV/GEMM crossover sweep) instead of the benchmark")

@@ -53,7 +53,9 @@ typedef enum {
   MNB_ERR_ALIAS = -6,       /* the output overlaps an input               */
   MNB_ERR_CUDA = -7,        /* a CUDA launch or copy failed               */
   MNB_ERR_UNSUPPORTED = -8, /* valid request the library cannot serve     */
-  MNB_ERR_DEVICE = -9       /* current device is not an sm_103 GPU        */
+  MNB_ERR_DEVICE = -9,      /* current device is not an sm_103 GPU        */
+  MNB_ERR_LAYOUT = -10      /* a packed weight does not match the call, or
+                               the library holds no header for it         */
 } mnb_status;
 
 typedef enum { MNB_F32 = 0, MNB_BF16 = 1 } mnb_dtype;
@@ -79,13 +81,81 @@ MNB_API const char *mnb_last_error_string(void);
 MNB_API int mnb_version(void);
 
 /*
+ * Packed-weight header (page "Qwen3 CPU Inference Critical Path", section
+ * "Prepared weight-only plan": the plan captures K, N, the nibble order and
+ * the block size, and packed weights are reused by every token).
+ *
+ * Every prepack call writes one into the last MNB_PACKED_HEADER_BYTES bytes
+ * of packed_b, so a packed weight saved with its three buffers carries its
+ * own description, and records it on the host, keyed by packed_b's device
+ * address. Every call that reads a packed weight (the matmul entry points,
+ * mnb_unprepack, mnb_chain_build, mnb_chain_run_noalloc) first compares the
+ * header recorded for its packed_b with the call's N, K, block_size, scale
+ * dtype, zero-point presence (a zero_points pointer given or not) and code
+ * form, on the host, after the argument checks and before anything is
+ * enqueued: a mismatch, or a packed_b for which the library holds no
+ * header, returns MNB_ERR_LAYOUT with the differing field in
+ * mnb_last_error_string(). A weight restored from storage into new device
+ * buffers is made known with mnb_packed_read_header + mnb_packed_register.
+ */
+#define MNB_PACKED_MAGIC 0x4B43415034424E4DULL /* the bytes "MNB4PACK" */
+#define MNB_PACKED_VERSION 1u
+#define MNB_PACKED_HEADER_BYTES 256
+
+typedef enum {
+  MNB_CODES_AFFINE = 0,  /* w = (q - z) * s: mnb_prepack, mnb_prepack_qdq */
+  MNB_CODES_CODEBOOK = 1 /* w = code[q] * absmax: mnb_prepack_bnb4        */
+} mnb_codes;
+
+typedef struct {
+  uint64_t magic;          /* MNB_PACKED_MAGIC                              */
+  uint32_t version;        /* MNB_PACKED_VERSION                            */
+  uint32_t codes;          /* mnb_codes                                     */
+  int64_t N, K;
+  int32_t block_size;
+  int32_t scale_dtype;     /* mnb_dtype of the scales (absmax)              */
+  int32_t has_zero_points; /* 0 or 1                                        */
+  int32_t reserved;        /* 0                                             */
+  uint64_t packed_b_bytes, packed_scales_bytes, packed_zp_bytes;
+  uint64_t check;          /* FNV-1a 64 of the 72 bytes before this field   */
+} mnb_packed_header;
+
+/* The header a prepack call writes for these arguments (pure host
+ * arithmetic). Errors: MNB_ERR_NULL, MNB_ERR_SHAPE, MNB_ERR_BLOCKSIZE,
+ * MNB_ERR_DTYPE, MNB_ERR_UNSUPPORTED (codes not an mnb_codes value, or a
+ * code-book weight with zero points). */
+MNB_API mnb_status mnb_packed_header_make(int64_t N, int64_t K, int block_size,
+                                          mnb_dtype scale_dtype, int has_zero_points,
+                                          int codes, mnb_packed_header *out);
+
+/* Records `header` (HOST) for the packed weight whose codes start at
+ * packed_b (DEVICE address; not dereferenced), replacing any earlier record
+ * for that address. Errors: MNB_ERR_NULL, MNB_ERR_LAYOUT (wrong magic or
+ * version, a check that does not match, or fields no prepack call writes). */
+MNB_API mnb_status mnb_packed_register(const void *packed_b, const mnb_packed_header *header);
+
+/* Copies the header stored in the last MNB_PACKED_HEADER_BYTES bytes of
+ * packed_b (DEVICE, packed_b_bytes long) into *out (HOST) and validates it
+ * as mnb_packed_register does; waits for the copy (synchronous with respect
+ * to the host, ordered on `stream`). Nothing is recorded. Errors:
+ * MNB_ERR_NULL, MNB_ERR_SHAPE (packed_b_bytes too small or not the size the
+ * header gives), MNB_ERR_LAYOUT, MNB_ERR_DEVICE, MNB_ERR_CUDA. */
+MNB_API mnb_status mnb_packed_read_header(const void *packed_b, size_t packed_b_bytes,
+                                          mnb_packed_header *out, mnb_stream_t stream);
+
+/* Drops the record for packed_b (before its buffer is freed or reused for
+ * something else). MNB_OK whether or not there was one; MNB_ERR_NULL. */
+MNB_API mnb_status mnb_packed_forget(const void *packed_b);
+
+/*
  * Sizes in bytes of the three prepacked buffers for an N x K weight
  * (section "Prepared weight-only plan": packed constant storage aligned for
  * the selected kernel). HOST outputs; zp_bytes is 0 when has_zero_points is
  * 0. The packed layout pads N up to a multiple of 16 and K up to a multiple
  * of 64 with zero codes; for N % 16 == 0 and K % 64 == 0 the packed codes
- * take exactly the N*K/2 bytes of the input. Zero points take 4 bits per
- * (row, block), with rows padded to 16 and blocks to an even count.
+ * take exactly the N*K/2 bytes of the input, and packed_b holds them
+ * followed by the MNB_PACKED_HEADER_BYTES-byte header. Zero points take 4
+ * bits per (row, block), with rows padded to 16 and blocks to an even count.
  * Errors: MNB_ERR_NULL (an output pointer), MNB_ERR_SHAPE (N or K < 1),
  * MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE.
  */
@@ -113,7 +183,9 @@ MNB_API mnb_status mnb_prepacked_sizes(int64_t N, int64_t K, int block_size,
  * The re-layout is lossless for every code with k < K; the storage padding
  * nibbles past K in the last block are not kept. Inputs need only byte
  * (B, zero_points) or element (scales) alignment. The last kernel it
- * enqueues is empty (see mnb_set_programmatic_launch).
+ * enqueues writes the packed-weight header into packed_b and nothing else
+ * (see mnb_set_programmatic_launch); the header is also recorded on the
+ * host for packed_b (affine codes).
  * Errors: MNB_ERR_NULL, MNB_ERR_SHAPE, MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE,
  * MNB_ERR_ALIGN (a packed output not 16-byte aligned), MNB_ERR_ALIAS (an
  * output overlaps an input or another output), MNB_ERR_CUDA.
@@ -186,8 +258,11 @@ MNB_API mnb_status mnb_unprepack(const void *packed_b,
  * Accumulation is fp32. Results are bitwise reproducible for a given device,
  * shape and path (every split-K reduction runs in a fixed order).
  * Errors: MNB_ERR_NULL, MNB_ERR_SHAPE, MNB_ERR_BLOCKSIZE, MNB_ERR_DTYPE,
- * MNB_ERR_ALIGN, MNB_ERR_ALIAS, MNB_ERR_UNSUPPORTED (no kernel for this
- * combination), MNB_ERR_DEVICE, MNB_ERR_CUDA.
+ * MNB_ERR_ALIGN, MNB_ERR_ALIAS, MNB_ERR_LAYOUT (the header recorded for
+ * packed_b differs from N, K, block_size, scale_dtype, zero-point presence
+ * or the affine code form, or there is none), MNB_ERR_UNSUPPORTED (no kernel
+ * for this combination), MNB_ERR_DEVICE, MNB_ERR_CUDA. Every other call that
+ * reads a packed weight checks its header the same way.
  */
 MNB_API mnb_status mnb_matmul(const void *A, const void *packed_b,
                               const void *scales, const void *zero_points,
@@ -373,6 +448,21 @@ MNB_API void mnb_set_programmatic_launch(int enable);
  * them. Errors: MNB_ERR_NULL, MNB_ERR_CUDA.
  */
 MNB_API mnb_status mnb_fault_status(unsigned int *fault_bits);
+
+/*
+ * Test-only failure injection for the decode kernel (off by default), so that
+ * the bounded waits above can be exercised without faulting a GPU: in every
+ * decode-kernel launch made after this call whose CTAs work without a
+ * cluster, CTA 0's producer issues weight stages 0 .. stop_stage - 1 and then
+ * stops. Its consumers, having consumed every copy issued, wait for stage
+ * stop_stage, give up after wait_limit iterations, record fault bit 1 and
+ * end the launch (the CTA's outputs are then wrong; nothing is left in flight
+ * and the context stays usable). wait_limit also caps every other wait of
+ * those launches (0: the normal cap). stop_stage < 0 and wait_limit 0 turn
+ * the injection off. Process-wide; launches recorded into a CUDA graph keep
+ * the values of their recording.
+ */
+MNB_API void mnb_test_wait_fault(int stop_stage, unsigned int wait_limit);
 
 /*
  * Projection of an RMS-normalized row, optionally followed by greedy ArgMax
@@ -571,6 +661,58 @@ MNB_API mnb_status mnb_chain_run_noalloc(const mnb_chain_op *ops, int32_t n_ops,
                                          int64_t M, int block_size,
                                          mnb_dtype a_dtype, mnb_dtype scale_dtype,
                                          mnb_stream_t stream);
+
+/*
+ * A sequence of projections as one CUDA graph: the GPU form of the page's
+ * session executor around one operator call per projection (page "Qwen3 CPU
+ * Inference Critical Path", section "Prepared weight-only plan"). The library
+ * records its own launches for the whole sequence once and then runs the
+ * sequence with one graph launch per step; no counterpart exists in the
+ * pages for the graph itself.
+ *
+ * mnb_graph_build: ops is a HOST array of n_ops (1..65536) descriptors, run
+ * in array order (deps is ignored: each op starts after the one before it
+ * on the stream). Consecutive ops without an up weight that read the same A
+ * with the same K form one fused-N call (mnb_matmul_grouped, up to 4 ops,
+ * M <= 16); an op with an up weight is one gated-MLP call
+ * (mnb_matmul_gate_up); any other op is one mnb_matmul call. Every call is
+ * validated as that entry point validates it (headers included) while it is
+ * recorded; the first failure ends the build with that call's status and
+ * message. The graph keeps the descriptors' device pointers: the buffers
+ * must stay allocated, and their contents are read (A, weights) and
+ * written (Y) each time the graph runs. The graph belongs to the device
+ * current at build time; the build records on a private stream and runs
+ * nothing. Host memory only (the graph objects); the library allocates no
+ * device memory.
+ * Errors: MNB_ERR_NULL, MNB_ERR_SHAPE, the recorded calls' errors,
+ * MNB_ERR_CUDA (capture or instantiation failed).
+ */
+typedef struct mnb_graph_st *mnb_graph;
+MNB_API mnb_status mnb_graph_build(const mnb_chain_op *ops, int32_t n_ops, int64_t M,
+                                   int block_size, mnb_dtype a_dtype, mnb_dtype scale_dtype,
+                                   mnb_graph *out);
+
+/* Library calls recorded and kernel nodes in the graph (HOST outputs, each
+ * may be NULL). Errors: MNB_ERR_NULL. */
+MNB_API mnb_status mnb_graph_info(mnb_graph graph, int32_t *calls, int32_t *kernels);
+
+/* One run of the graph on `stream` (asynchronous). Errors: MNB_ERR_NULL,
+ * MNB_ERR_DEVICE (another device is current), MNB_ERR_CUDA. */
+MNB_API mnb_status mnb_graph_run(mnb_graph graph, mnb_stream_t stream);
+
+/* One run framed by host copies, all on `stream`: in_bytes from in_host
+ * (HOST) to in_dev (DEVICE), the graph, then out_bytes from out_dev (DEVICE)
+ * to out_host (HOST). Page-locked host buffers make the copies asynchronous;
+ * the host buffers must stay valid until the stream reaches the end of the
+ * run. A zero byte count skips that copy. Errors: as mnb_graph_run;
+ * MNB_ERR_NULL for a missing buffer of a copy. */
+MNB_API mnb_status mnb_graph_run_from_host(mnb_graph graph, const void *in_host,
+                                           void *in_dev, size_t in_bytes,
+                                           const void *out_dev, void *out_host,
+                                           size_t out_bytes, mnb_stream_t stream);
+
+/* Frees the graph (host objects). Errors: MNB_ERR_NULL. */
+MNB_API mnb_status mnb_graph_destroy(mnb_graph graph);
 
 #ifdef __cplusplus
 }

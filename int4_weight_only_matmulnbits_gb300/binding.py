@@ -26,6 +26,10 @@ MNB_ERR_ALIAS = -6
 MNB_ERR_CUDA = -7
 MNB_ERR_UNSUPPORTED = -8
 MNB_ERR_DEVICE = -9
+MNB_ERR_LAYOUT = -10
+MNB_CODES_AFFINE, MNB_CODES_CODEBOOK = 0, 1
+MNB_PACKED_MAGIC = 0x4B43415034424E4D
+MNB_PACKED_HEADER_BYTES = 256
 MNB_F32, MNB_BF16 = 0, 1
 MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_streamk": 3}
 
@@ -36,7 +40,10 @@ EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
            "mnb_set_programmatic_launch", "mnb_fault_status", "mnb_matmul_grouped",
            "mnb_prepack_qdq", "mnb_matmul_gate_up", "mnb_chain_build", "mnb_chain_run", "mnb_chain_run_noalloc",
            "mnb_matmul_rmsnorm", "mnb_prepack_bnb4", "mnb_matmul_bnb4",
-           "mnb_matmul_workspace_size", "mnb_matmul_ws", "mnb_matmul_plan")
+           "mnb_matmul_workspace_size", "mnb_matmul_ws", "mnb_matmul_plan",
+           "mnb_packed_header_make", "mnb_packed_register", "mnb_packed_read_header",
+           "mnb_packed_forget", "mnb_graph_build", "mnb_graph_info", "mnb_graph_run",
+           "mnb_graph_run_from_host", "mnb_graph_destroy", "mnb_test_wait_fault")
 
 _lock = threading.Lock()
 _lib = None
@@ -49,6 +56,16 @@ class PlanInfoC(ctypes.Structure):
                 ("stream_k", ctypes.c_int32), ("tf32", ctypes.c_int32),
                 ("tma_store", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("ctas", ctypes.c_int64)]
+
+
+class PackedHeaderC(ctypes.Structure):
+    """mnb_packed_header (include/mnb.h)."""
+    _fields_ = [("magic", ctypes.c_uint64), ("version", ctypes.c_uint32),
+                ("codes", ctypes.c_uint32), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("block_size", ctypes.c_int32), ("scale_dtype", ctypes.c_int32),
+                ("has_zero_points", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("packed_b_bytes", ctypes.c_uint64), ("packed_scales_bytes", ctypes.c_uint64),
+                ("packed_zp_bytes", ctypes.c_uint64), ("check", ctypes.c_uint64)]
 
 
 class ChainOpC(ctypes.Structure):
@@ -152,6 +169,29 @@ def load(build_if_missing: bool = False):
         lib.mnb_matmul_rmsnorm.argtypes = [p, i32, p, ctypes.c_float, p, p, p, p, i64, i64,
                                            i64, i32, p, p, i32, i32, p]
         lib.mnb_matmul_rmsnorm.restype = i32
+        lib.mnb_packed_header_make.argtypes = [i64, i64, i32, i32, i32, i32,
+                                               ctypes.POINTER(PackedHeaderC)]
+        lib.mnb_packed_header_make.restype = i32
+        lib.mnb_packed_register.argtypes = [p, ctypes.POINTER(PackedHeaderC)]
+        lib.mnb_packed_register.restype = i32
+        lib.mnb_packed_read_header.argtypes = [p, sz, ctypes.POINTER(PackedHeaderC), p]
+        lib.mnb_packed_read_header.restype = i32
+        lib.mnb_packed_forget.argtypes = [p]
+        lib.mnb_packed_forget.restype = i32
+        lib.mnb_graph_build.argtypes = [ctypes.POINTER(ChainOpC), i32, i64, i32, i32, i32,
+                                        ctypes.POINTER(p)]
+        lib.mnb_graph_build.restype = i32
+        lib.mnb_graph_info.argtypes = [p, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int32)]
+        lib.mnb_graph_info.restype = i32
+        lib.mnb_graph_run.argtypes = [p, p]
+        lib.mnb_graph_run.restype = i32
+        lib.mnb_graph_run_from_host.argtypes = [p, p, p, sz, p, p, sz, p]
+        lib.mnb_graph_run_from_host.restype = i32
+        lib.mnb_test_wait_fault.argtypes = [i32, ctypes.c_uint]
+        lib.mnb_test_wait_fault.restype = None
+        lib.mnb_graph_destroy.argtypes = [p]
+        lib.mnb_graph_destroy.restype = i32
         lib.mnb_prepack_bnb4.argtypes = [p, p, i64, i64, i32, i32, p, p, p]
         lib.mnb_prepack_bnb4.restype = i32
         lib.mnb_matmul_bnb4.argtypes = [p, p, p, p, p, i64, i64, i64, i32, p, i32, i32, p]
@@ -212,6 +252,12 @@ def mnb_set_programmatic_launch(enable: bool) -> None:
     load().mnb_set_programmatic_launch(1 if enable else 0)
 
 
+def mnb_test_wait_fault(stop_stage: int = -1, wait_limit: int = 0) -> None:
+    """Test-only failure injection in the decode kernel (see include/mnb.h);
+    the defaults turn it off."""
+    load().mnb_test_wait_fault(stop_stage, wait_limit)
+
+
 def mnb_fault_status() -> int:
     """Fault bits recorded by kernels whose bounded waits ran out (cleared)."""
     v = ctypes.c_uint()
@@ -268,6 +314,37 @@ def mnb_prepack_qdq(B_qdq: torch.Tensor, scales: torch.Tensor,
                                   _ptr(packed_s), _ptr(packed_z), _stream(stream)),
            "mnb_prepack_qdq")
     return PackedWeight(packed_b, packed_s, packed_z, N, K, block_size, scales.dtype)
+
+
+def mnb_packed_header_make(N: int, K: int, block_size: int, scale_dtype: torch.dtype,
+                           has_zero_points: bool, codes: int = MNB_CODES_AFFINE) -> PackedHeaderC:
+    """The header a prepack call writes for these arguments (host only)."""
+    h = PackedHeaderC()
+    _check(load().mnb_packed_header_make(N, K, block_size, _dtype_code(scale_dtype),
+                                         int(has_zero_points), codes, ctypes.byref(h)),
+           "mnb_packed_header_make")
+    return h
+
+
+def mnb_packed_read_header(w: PackedWeight | torch.Tensor, *, stream=None) -> PackedHeaderC:
+    """The header stored at the end of a packed_b buffer (read from the device)."""
+    pb = w.packed_b if isinstance(w, PackedWeight) else w
+    h = PackedHeaderC()
+    _check(load().mnb_packed_read_header(_ptr(pb), pb.numel() * pb.element_size(),
+                                         ctypes.byref(h), _stream(stream)),
+           "mnb_packed_read_header")
+    return h
+
+
+def mnb_packed_register(packed_b: torch.Tensor | int, header: PackedHeaderC) -> None:
+    """Record `header` for the packed weight at packed_b (a restored weight)."""
+    ptr = ctypes.c_void_p(packed_b) if isinstance(packed_b, int) else _ptr(packed_b)
+    _check(load().mnb_packed_register(ptr, ctypes.byref(header)), "mnb_packed_register")
+
+
+def mnb_packed_forget(packed_b: torch.Tensor | int) -> None:
+    ptr = ctypes.c_void_p(packed_b) if isinstance(packed_b, int) else _ptr(packed_b)
+    _check(load().mnb_packed_forget(ptr), "mnb_packed_forget")
 
 
 def mnb_unprepack(w: PackedWeight, *, stream=None):
@@ -513,6 +590,55 @@ def mnb_chain_run(chain: MnbChain, *, stream=None) -> None:
     """Run every op of a built chain in one cooperative launch on `stream`."""
     _check(load().mnb_chain_run(ctypes.c_void_p(chain.plan.data_ptr()), ctypes.byref(chain.info),
                                 _stream(stream)), "mnb_chain_run")
+
+
+class MnbGraph:
+    """A sequence of projections recorded as one CUDA graph by the library
+    (mnb_graph_build). Holds references to every tensor of its ops; the graph
+    reads their current contents each run."""
+
+    def __init__(self, ops: list, handle: int):
+        self.ops = list(ops)
+        self._handle = ctypes.c_void_p(handle)
+        calls, kernels = ctypes.c_int32(), ctypes.c_int32()
+        _check(load().mnb_graph_info(self._handle, ctypes.byref(calls), ctypes.byref(kernels)),
+               "mnb_graph_info")
+        self.calls, self.kernels = calls.value, kernels.value
+
+    def run(self, stream=None) -> None:
+        _check(load().mnb_graph_run(self._handle, _stream(stream)), "mnb_graph_run")
+
+    def run_from_host(self, in_host: torch.Tensor | None, in_dev: torch.Tensor | None,
+                      out_dev: torch.Tensor | None, out_host: torch.Tensor | None,
+                      stream=None) -> None:
+        """Copy in_host -> in_dev, run, copy out_dev -> out_host (one stream)."""
+        nb = lambda t: 0 if t is None else t.numel() * t.element_size()
+        if nb(in_host) != nb(in_dev) or nb(out_dev) != nb(out_host):
+            raise ValueError("host and device buffers of a copy must have the same size")
+        _check(load().mnb_graph_run_from_host(self._handle, _ptr(in_host), _ptr(in_dev),
+                                              nb(in_dev), _ptr(out_dev), _ptr(out_host),
+                                              nb(out_dev), _stream(stream)),
+               "mnb_graph_run_from_host")
+
+    def __del__(self):
+        if getattr(self, "_handle", None) and self._handle.value and _lib is not None:
+            _lib.mnb_graph_destroy(self._handle)
+            self._handle = None
+
+
+def mnb_graph_build(ops: list) -> MnbGraph:
+    """Record the projections `ops` (ChainOp; run in list order, deps ignored)
+    as one CUDA graph on the current device: consecutive ops reading the same
+    activations fuse into one grouped call, gated pairs run as one call."""
+    if not ops:
+        raise ValueError("empty sequence")
+    arr, M = _chain_structs(ops)
+    w0 = ops[0].weight
+    h = ctypes.c_void_p()
+    _check(load().mnb_graph_build(arr, len(ops), M, w0.block_size, _dtype_code(ops[0].A.dtype),
+                                  _dtype_code(w0.scale_dtype), ctypes.byref(h)),
+           "mnb_graph_build")
+    return MnbGraph(ops, h.value)
 
 
 def mnb_chain_run_noalloc(ops: list, *, stream=None) -> None:

@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/mnb.h"
@@ -48,11 +49,16 @@ struct Sizes {
   size_t b, s, z;
 };
 
+// Bytes of the packed codes; packed_b holds them, then the header.
+size_t codes_bytes(int64_t N, int64_t K) {
+  return size_t(ceil_div(N, kTileN)) * ceil_div(K, kChunkK) * kChunkBytes;
+}
+
 Sizes packed_sizes(int64_t N, int64_t K, int bs, int scale_dtype, bool zp) {
-  const int64_t N16 = ceil_div(N, kTileN), K64 = ceil_div(K, kChunkK);
+  const int64_t N16 = ceil_div(N, kTileN);
   const int64_t nb = ceil_div(K, bs);
   Sizes s;
-  s.b = size_t(N16) * K64 * kChunkBytes;
+  s.b = codes_bytes(N, K) + MNB_PACKED_HEADER_BYTES;
   s.s = size_t(N16) * nb * kTileN * dtype_size(scale_dtype);
   s.z = zp ? size_t(N16) * ceil_div(nb, 2) * 2 * 8 : 0;
   return s;
@@ -68,6 +74,111 @@ mnb_status check_shape(int64_t N, int64_t K, int bs, int scale_dtype) {
   if (!valid_block_size(bs)) return MNB_ERR_BLOCKSIZE;
   if (!valid_dtype(scale_dtype)) return MNB_ERR_DTYPE;
   return MNB_OK;
+}
+
+// ---- packed-weight headers and their host-side records ---------------------
+
+static_assert(sizeof(mnb_packed_header) == 80, "mnb_packed_header layout");
+static_assert(sizeof(mnb_packed_header) <= MNB_PACKED_HEADER_BYTES, "header room");
+
+uint64_t header_check(const mnb_packed_header &h) {
+  const unsigned char *b = reinterpret_cast<const unsigned char *>(&h);
+  uint64_t x = 1469598103934665603ull;  // FNV-1a 64
+  for (size_t i = 0; i < offsetof(mnb_packed_header, check); ++i) {
+    x ^= b[i];
+    x *= 1099511628211ull;
+  }
+  return x;
+}
+
+mnb_packed_header make_header(int64_t N, int64_t K, int bs, int scale_dtype, bool zp,
+                              int codes) {
+  mnb_packed_header h;
+  std::memset(&h, 0, sizeof h);
+  h.magic = MNB_PACKED_MAGIC;
+  h.version = MNB_PACKED_VERSION;
+  h.codes = static_cast<uint32_t>(codes);
+  h.N = N;
+  h.K = K;
+  h.block_size = bs;
+  h.scale_dtype = scale_dtype;
+  h.has_zero_points = zp ? 1 : 0;
+  const Sizes z = packed_sizes(N, K, bs, scale_dtype, zp);
+  h.packed_b_bytes = z.b;
+  h.packed_scales_bytes = z.s;
+  h.packed_zp_bytes = z.z;
+  h.check = header_check(h);
+  return h;
+}
+
+// A header some prepack call could have written, with a matching check.
+mnb_status header_valid(const mnb_packed_header &h) {
+  if (h.magic != MNB_PACKED_MAGIC || h.version != MNB_PACKED_VERSION ||
+      h.check != header_check(h)) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "not a packed-weight header of this library (magic, version or check)");
+    return MNB_ERR_LAYOUT;
+  }
+  const bool ok_codes = h.codes == MNB_CODES_AFFINE ||
+                        (h.codes == MNB_CODES_CODEBOOK && h.has_zero_points == 0);
+  if (!ok_codes || (h.has_zero_points != 0 && h.has_zero_points != 1) || h.reserved != 0 ||
+      check_shape(h.N, h.K, h.block_size, h.scale_dtype) != MNB_OK) {
+    std::snprintf(g_last_error, sizeof g_last_error, "packed-weight header with invalid fields");
+    return MNB_ERR_LAYOUT;
+  }
+  const Sizes z = packed_sizes(h.N, h.K, h.block_size, h.scale_dtype, h.has_zero_points != 0);
+  if (h.packed_b_bytes != z.b || h.packed_scales_bytes != z.s || h.packed_zp_bytes != z.z) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "packed-weight header sizes do not match its shape");
+    return MNB_ERR_LAYOUT;
+  }
+  return MNB_OK;
+}
+
+std::mutex g_headers_mu;
+std::unordered_map<uintptr_t, mnb_packed_header> g_headers;
+
+void record_header(const void *packed_b, const mnb_packed_header &h) {
+  std::lock_guard<std::mutex> lock(g_headers_mu);
+  g_headers[reinterpret_cast<uintptr_t>(packed_b)] = h;
+}
+
+const char *dtype_name(int d) { return d == MNB_F32 ? "fp32" : "bf16"; }
+
+// The header recorded for packed_b against what a call passes.
+mnb_status check_layout(const void *packed_b, int64_t N, int64_t K, int bs, int scale_dtype,
+                        bool zp, int codes) {
+  mnb_packed_header h;
+  {
+    std::lock_guard<std::mutex> lock(g_headers_mu);
+    const auto it = g_headers.find(reinterpret_cast<uintptr_t>(packed_b));
+    if (it == g_headers.end()) {
+      std::snprintf(g_last_error, sizeof g_last_error,
+                    "no packed-weight header is recorded for %p: pack it with a prepack "
+                    "call, or register the header stored with it",
+                    packed_b);
+      return MNB_ERR_LAYOUT;
+    }
+    h = it->second;
+  }
+  const char *field = h.N != N                             ? "N"
+                      : h.K != K                           ? "K"
+                      : h.block_size != bs                 ? "block_size"
+                      : h.scale_dtype != scale_dtype       ? "scale dtype"
+                      : (h.has_zero_points != 0) != zp     ? "zero-point presence"
+                      : static_cast<int>(h.codes) != codes ? "code form"
+                                                           : nullptr;
+  if (!field) return MNB_OK;
+  std::snprintf(g_last_error, sizeof g_last_error,
+                "packed weight %p differs in %s: packed as N=%lld K=%lld bs=%d scales %s, "
+                "%s zero points, %s codes; called with N=%lld K=%lld bs=%d scales %s, %s "
+                "zero points, %s codes",
+                packed_b, field, (long long)h.N, (long long)h.K, h.block_size,
+                dtype_name(h.scale_dtype), h.has_zero_points ? "with" : "no",
+                h.codes == MNB_CODES_AFFINE ? "affine" : "code-book", (long long)N,
+                (long long)K, bs, dtype_name(scale_dtype), zp ? "with" : "no",
+                codes == MNB_CODES_AFFINE ? "affine" : "code-book");
+  return MNB_ERR_LAYOUT;
 }
 
 mnb_status check_device() {
@@ -129,13 +240,25 @@ mnb_status validate_matmul_args(const void *A, const void *packed_b,
   return MNB_OK;
 }
 
+// Argument checks and the packed weight's recorded header (host only).
+mnb_status validate_matmul_host(const void *A, const void *packed_b, const void *scales,
+                                const void *zero_points, const float *bias, int64_t M,
+                                int64_t N, int64_t K, int block_size, const void *Y,
+                                int a_dtype, int scale_dtype, int path,
+                                int codes = MNB_CODES_AFFINE) {
+  const mnb_status st = validate_matmul_args(A, packed_b, scales, zero_points, bias, M, N, K,
+                                             block_size, Y, a_dtype, scale_dtype, path);
+  if (st != MNB_OK) return st;
+  return check_layout(packed_b, N, K, block_size, scale_dtype, zero_points != nullptr, codes);
+}
+
 mnb_status validate_matmul(const void *A, const void *packed_b,
                            const void *scales, const void *zero_points,
                            const float *bias, int64_t M, int64_t N, int64_t K,
                            int block_size, const void *Y, int a_dtype,
-                           int scale_dtype, int path) {
-  const mnb_status st = validate_matmul_args(A, packed_b, scales, zero_points, bias, M, N,
-                                             K, block_size, Y, a_dtype, scale_dtype, path);
+                           int scale_dtype, int path, int codes = MNB_CODES_AFFINE) {
+  const mnb_status st = validate_matmul_host(A, packed_b, scales, zero_points, bias, M, N, K,
+                                             block_size, Y, a_dtype, scale_dtype, path, codes);
   return st != MNB_OK ? st : check_device();
 }
 
@@ -254,6 +377,8 @@ const char *mnb_status_string(int status) {
     case MNB_ERR_UNSUPPORTED:
       return "MNB_ERR_UNSUPPORTED: no kernel serves this combination";
     case MNB_ERR_DEVICE: return "MNB_ERR_DEVICE: current device is not sm_103";
+    case MNB_ERR_LAYOUT:
+      return "MNB_ERR_LAYOUT: the packed weight does not match the call, or has no header";
     default: return "unknown mnb_status";
   }
 }
@@ -263,6 +388,10 @@ const char *mnb_last_error_string(void) { return g_last_error; }
 int mnb_version(void) { return (1 << 16) | 0; }
 
 void mnb_set_programmatic_launch(int enable) { g_pdl.store(enable ? 1 : 0); }
+
+void mnb_test_wait_fault(int stop_stage, unsigned int wait_limit) {
+  gemv_set_wait_fault(stop_stage, wait_limit);
+}
 
 mnb_status mnb_fault_status(unsigned int *fault_bits) {
   if (!fault_bits) return MNB_ERR_NULL;
@@ -274,6 +403,58 @@ mnb_status mnb_fault_status(unsigned int *fault_bits) {
   if (e == cudaSuccess) e = chain_take_fault(&c);
   if (e != cudaSuccess) return cuda_fail(e, "mnb_fault_status");
   *fault_bits = a | b | c;
+  return MNB_OK;
+}
+
+mnb_status mnb_packed_header_make(int64_t N, int64_t K, int block_size, mnb_dtype scale_dtype,
+                                  int has_zero_points, int codes, mnb_packed_header *out) {
+  if (!out) return MNB_ERR_NULL;
+  const mnb_status st = check_shape(N, K, block_size, scale_dtype);
+  if (st != MNB_OK) return st;
+  if ((codes != MNB_CODES_AFFINE && codes != MNB_CODES_CODEBOOK) ||
+      (codes == MNB_CODES_CODEBOOK && has_zero_points))
+    return MNB_ERR_UNSUPPORTED;
+  *out = make_header(N, K, block_size, scale_dtype, has_zero_points != 0, codes);
+  return MNB_OK;
+}
+
+mnb_status mnb_packed_register(const void *packed_b, const mnb_packed_header *header) {
+  if (!packed_b || !header) return MNB_ERR_NULL;
+  const mnb_status st = header_valid(*header);
+  if (st != MNB_OK) return st;
+  record_header(packed_b, *header);
+  return MNB_OK;
+}
+
+mnb_status mnb_packed_read_header(const void *packed_b, size_t packed_b_bytes,
+                                  mnb_packed_header *out, mnb_stream_t stream) {
+  if (!packed_b || !out) return MNB_ERR_NULL;
+  if (packed_b_bytes < MNB_PACKED_HEADER_BYTES) return MNB_ERR_SHAPE;
+  mnb_status st = check_device();
+  if (st != MNB_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mnb_packed_header h;
+  cudaError_t e = cudaMemcpyAsync(
+      &h, static_cast<const char *>(packed_b) + (packed_b_bytes - MNB_PACKED_HEADER_BYTES),
+      sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "mnb_packed_read_header");
+  st = header_valid(h);
+  if (st != MNB_OK) return st;
+  if (h.packed_b_bytes != packed_b_bytes) {
+    std::snprintf(g_last_error, sizeof g_last_error,
+                  "the header gives packed_b %llu bytes, the call %llu",
+                  (unsigned long long)h.packed_b_bytes, (unsigned long long)packed_b_bytes);
+    return MNB_ERR_SHAPE;
+  }
+  *out = h;
+  return MNB_OK;
+}
+
+mnb_status mnb_packed_forget(const void *packed_b) {
+  if (!packed_b) return MNB_ERR_NULL;
+  std::lock_guard<std::mutex> lock(g_headers_mu);
+  g_headers.erase(reinterpret_cast<uintptr_t>(packed_b));
   return MNB_OK;
 }
 
@@ -320,8 +501,12 @@ mnb_status mnb_prepack(const uint8_t *B, const void *scales,
   if (st != MNB_OK) return st;
   PrepackArgs a{B, scales, zero_points, N, K, block_size,
                 scale_dtype == MNB_F32, packed_b, packed_scales, packed_zp};
+  a.header = make_header(N, K, block_size, scale_dtype, zero_points != nullptr,
+                         MNB_CODES_AFFINE);
+  a.header_dst = static_cast<char *>(packed_b) + codes_bytes(N, K);
   const cudaError_t e = launch_prepack(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mnb_prepack");
+  record_header(packed_b, a.header);
   return MNB_OK;
 }
 
@@ -350,8 +535,11 @@ mnb_status mnb_prepack_qdq(const uint8_t *B_qdq, const void *scales,
   PrepackArgs a{B_qdq, scales, zero_points, N, K, block_size,
                 scale_dtype == MNB_F32, packed_b, packed_scales, packed_zp};
   a.qdq_axis = axis;
+  a.header = make_header(N, K, block_size, scale_dtype, true, MNB_CODES_AFFINE);
+  a.header_dst = static_cast<char *>(packed_b) + codes_bytes(N, K);
   const cudaError_t e = launch_prepack(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mnb_prepack_qdq");
+  record_header(packed_b, a.header);
   return MNB_OK;
 }
 
@@ -377,6 +565,11 @@ mnb_status mnb_unprepack(const void *packed_b, const void *packed_scales,
                            size_t(N) * nb * dtype_size(scale_dtype),
                            packed_zp ? size_t(N) * ((nb + 1) / 2) : 0};
   st = check_outputs_disjoint(outs, out_n, ins, in_n);
+  if (st != MNB_OK) return st;
+  st = check_layout(packed_b, N, K, block_size, scale_dtype, packed_zp != nullptr,
+                    MNB_CODES_AFFINE);
+  if (st == MNB_ERR_LAYOUT && packed_zp == nullptr)  // the bitsandbytes-style plan
+    st = check_layout(packed_b, N, K, block_size, scale_dtype, false, MNB_CODES_CODEBOOK);
   if (st != MNB_OK) return st;
   st = check_device();
   if (st != MNB_OK) return st;
@@ -477,6 +670,9 @@ mnb_status mnb_matmul_ws(const void *A, const void *packed_b, const void *scales
     for (int j = 0; j < 6; ++j)
       if (overlap(workspace, workspace_bytes, others[j], on[j])) return MNB_ERR_ALIAS;
   }
+  st = check_layout(packed_b, N, K, block_size, scale_dtype, zero_points != nullptr,
+                    MNB_CODES_AFFINE);
+  if (st != MNB_OK) return st;
   st = check_device();
   if (st != MNB_OK) return st;
   return run_matmul(A, packed_b, scales, zero_points, bias, M, N, K, block_size, Y,
@@ -507,7 +703,7 @@ mnb_status mnb_matmul_grouped(const void *A, int count,
   const bool has_zp = zero_points && zero_points[0];
   for (int i = 0; i < count; ++i) {
     if (zero_points && ((zero_points[i] != nullptr) != has_zp)) return MNB_ERR_NULL;
-    const mnb_status st = validate_matmul(
+    const mnb_status st = validate_matmul_host(
         A, packed_b[i], scales[i], has_zp ? zero_points[i] : nullptr,
         bias ? bias[i] : nullptr, M, N[i], K, block_size, Y[i], a_dtype,
         scale_dtype, MNB_PATH_AUTO);
@@ -524,6 +720,7 @@ mnb_status mnb_matmul_grouped(const void *A, int count,
         if (overlap(Y[i], size_t(M) * N[i] * es, others[k], on[k])) return MNB_ERR_ALIAS;
     }
   }
+  if (const mnb_status st = check_device(); st != MNB_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (M > kGemvMaxM) {
     for (int i = 0; i < count; ++i) {
@@ -573,11 +770,13 @@ mnb_status mnb_matmul_gate_up(const void *A, const void *packed_gate,
                               int block_size, void *Y, mnb_dtype a_dtype,
                               mnb_dtype scale_dtype, mnb_stream_t stream) {
   if ((zp_gate != nullptr) != (zp_up != nullptr)) return MNB_ERR_NULL;
-  mnb_status st = validate_matmul(A, packed_gate, scales_gate, zp_gate, bias_gate, M, N, K,
-                                  block_size, Y, a_dtype, scale_dtype, MNB_PATH_AUTO);
+  mnb_status st = validate_matmul_host(A, packed_gate, scales_gate, zp_gate, bias_gate, M, N,
+                                       K, block_size, Y, a_dtype, scale_dtype, MNB_PATH_AUTO);
   if (st != MNB_OK) return st;
-  st = validate_matmul(A, packed_up, scales_up, zp_up, bias_up, M, N, K, block_size, Y,
-                       a_dtype, scale_dtype, MNB_PATH_AUTO);
+  st = validate_matmul_host(A, packed_up, scales_up, zp_up, bias_up, M, N, K, block_size, Y,
+                            a_dtype, scale_dtype, MNB_PATH_AUTO);
+  if (st != MNB_OK) return st;
+  st = check_device();
   if (st != MNB_OK) return st;
   const size_t es = dtype_size(a_dtype);
   GroupArgs g{};
@@ -689,6 +888,9 @@ mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
     if (overlap(Y, y_bytes, ins[j], in_n[j]) || overlap(argmax, k_bytes, ins[j], in_n[j]))
       return MNB_ERR_ALIAS;
   if (overlap(Y, y_bytes, argmax, k_bytes)) return MNB_ERR_ALIAS;
+  st = check_layout(packed_b, N, K, block_size, scale_dtype, zero_points != nullptr,
+                    MNB_CODES_AFFINE);
+  if (st != MNB_OK) return st;
   st = check_device();
   if (st != MNB_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -760,8 +962,11 @@ mnb_status mnb_prepack_bnb4(const uint8_t *B, const void *absmax, int64_t N, int
   PrepackArgs a{B, absmax, nullptr, N, K, block_size, absmax_dtype == MNB_F32, packed_b,
                 packed_scales, nullptr};
   a.bnb4 = true;
+  a.header = make_header(N, K, block_size, absmax_dtype, false, MNB_CODES_CODEBOOK);
+  a.header_dst = static_cast<char *>(packed_b) + codes_bytes(N, K);
   const cudaError_t e = launch_prepack(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mnb_prepack_bnb4");
+  record_header(packed_b, a.header);
   return MNB_OK;
 }
 
@@ -772,7 +977,8 @@ mnb_status mnb_matmul_bnb4(const void *A, const void *packed_b, const void *pack
   if (!code) return MNB_ERR_NULL;
   if (!aligned(code, 4)) return MNB_ERR_ALIGN;
   mnb_status st = validate_matmul(A, packed_b, packed_scales, nullptr, bias, M, N, K,
-                                  block_size, Y, a_dtype, absmax_dtype, MNB_PATH_AUTO);
+                                  block_size, Y, a_dtype, absmax_dtype, MNB_PATH_AUTO,
+                                  MNB_CODES_CODEBOOK);
   if (st != MNB_OK) return st;
   if (overlap(Y, size_t(M) * N * dtype_size(a_dtype), code, 64)) return MNB_ERR_ALIAS;
   const size_t es = dtype_size(a_dtype);
@@ -883,6 +1089,16 @@ mnb_status mnb_chain_build(const mnb_chain_op *ops, int32_t n_ops, int64_t M,
           overlap(a.y, a.ny, rg[i].y, rg[i].ny))
         return MNB_ERR_ALIAS;
     }
+  }
+  // The weights' headers, after the argument and hazard checks.
+  for (int j = 0; j < n_ops; ++j) {
+    const mnb_chain_op &o = ops[j];
+    mnb_status ls = check_layout(o.packed_b, o.N, o.K, block_size, scale_dtype, has_zp,
+                                 MNB_CODES_AFFINE);
+    if (ls == MNB_OK && o.packed_b_up)
+      ls = check_layout(o.packed_b_up, o.N, o.K, block_size, scale_dtype, has_zp,
+                        MNB_CODES_AFFINE);
+    if (ls != MNB_OK) return ls;
   }
   mnb_status st = check_device();
   if (st != MNB_OK) return st;

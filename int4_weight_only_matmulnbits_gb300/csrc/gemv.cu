@@ -86,6 +86,10 @@ struct GemvParams {
   int cpw, scs;              // chunks per warp and stage; chunks per stage and tile (ksw*cpw)
   int krp, sg;               // staged activation row stride, block sums per row
   int nst, stage_bytes, stage_tx;  // ring depth, stage stride, bytes per stage
+  // Failure-detection test (mnb_test_wait_fault): every wait's iteration cap,
+  // and the stage at which CTA 0's producer stops issuing (-1: never).
+  uint32_t wait_limit;
+  int stop_stage;
   // RMS-normalized activations (the fusion "RMSNorm into packed projection
   // input"): the staged row is A * gamma and every output is scaled by
   // r[m] = 1 / sqrt(mean_k A[m,k]^2 + eps). norm = 0: plain A.
@@ -293,8 +297,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       const int tile0 = (gi - p.tg_begin[q]) * p.tpc;
       for (int j = 0; j < p.R && ok; ++j) {
         if (!a_issued && issued == kPrefetchStages) issue_a();
+        // Test-only stop (launches without a cluster): the stage is never
+        // issued, so CTA 0's consumers give up waiting for it; every copy
+        // issued before it is consumed first, so none is left in flight.
+        if (issued == p.stop_stage && blockIdx.x == 0 && p.cluster == 1) {
+          ok = false;
+          break;
+        }
         ++issued;
-        if (wrapped && !mbar_wait(empty + slot, phase ^ 1)) {
+        if (wrapped && !mbar_wait(empty + slot, phase ^ 1, p.wait_limit)) {
           if (lane == 0) record_fault(&g_fault_gemv, kFaultGemvWait);
           ok = false;
           break;
@@ -399,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       const int n = p.K - k0 < kr ? static_cast<int>(p.K - k0) : kr;
       for (int e = n + tid; e < kr; e += kConsumers)
         for (int m = 0; m < p.M; ++m) sA[m * p.krp + e] = 0;
-      if (!mbar_wait(abar, 0)) {
+      if (!mbar_wait(abar, 0, p.wait_limit)) {
         record_fault(&g_fault_gemv, kFaultGemvWait);
         fault = true;
       }
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
       for (int j = 0; j < p.R && !fault; ++j) {
-        if (!mbar_wait(full + slot, phase)) {
+        if (!mbar_wait(full + slot, phase, p.wait_limit)) {
           record_fault(&g_fault_gemv, kFaultGemvWait);
           fault = true;
           break;
@@ -965,6 +976,14 @@ cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int scs, GemvParams 
 
 }  // namespace
 
+std::atomic<int> g_test_stop_stage{-1};
+std::atomic<uint32_t> g_test_wait_limit{0};
+
+void gemv_set_wait_fault(int stop_stage, uint32_t wait_limit) {
+  g_test_stop_stage.store(stop_stage < 0 ? -1 : stop_stage);
+  g_test_wait_limit.store(wait_limit);
+}
+
 cudaError_t gemv_take_fault(unsigned int *out) {
   unsigned int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(out, g_fault_gemv, sizeof(unsigned int));
@@ -1039,6 +1058,9 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   p.R = best.R;
   p.cpw = best.cpw;
   p.scs = best.ksw * best.cpw;
+  const uint32_t wl = g_test_wait_limit.load();
+  p.wait_limit = wl ? wl : kWaitLimit;
+  p.stop_stage = g_test_stop_stage.load();
 
   // Persistent grid: every tile group gets a CTA (cluster) when they fit in
   // the CTAs resident at once; otherwise CTAs walk the groups.

@@ -10,6 +10,8 @@
 #include <atomic>
 #include <vector>
 
+#include "../../include/mnb.h"
+
 namespace mnb {
 
 // Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
@@ -41,6 +43,10 @@ struct PrepackArgs {
   // The bitsandbytes-style storage (flattened N x K codes, first of a pair
   // high; absmax [N * K / bs] read as [N, nb] scales, K a multiple of bs).
   bool bnb4 = false;
+  // The packed-weight header, written by the last kernel to header_dst (the
+  // end of packed_b).
+  mnb_packed_header header{};
+  void *header_dst = nullptr;
 };
 
 struct UnprepackArgs {
@@ -90,6 +96,8 @@ GemmPlanInfo gemm_plan_info(const MatmulArgs &a, int sms);
 size_t gemm_workspace_bytes();
 
 cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream);
+// Test-only failure injection for the decode kernel (mnb_test_wait_fault).
+void gemv_set_wait_fault(int stop_stage, uint32_t wait_limit);
 cudaError_t launch_unprepack(const UnprepackArgs &a, cudaStream_t stream);
 
 // Up to kMaxGroup weights that share one activation matrix A (fused-N

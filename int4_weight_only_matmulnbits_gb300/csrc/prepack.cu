@@ -195,12 +195,23 @@ __global__ void unpack_zp_kernel(const uint64_t *__restrict__ packed,
   }
 }
 
-// Launched last by mnb_prepack. Matmul kernels launched with programmatic
-// dependent launch may start loading their packed weights as soon as the
-// kernel before them on the stream begins to exit; ending the prepack with
-// this empty kernel puts a full kernel boundary between the writes of the
-// packed weights and any such early load.
-__global__ void prepack_fence_kernel() {}
+// Launched last by every prepack call: writes the packed-weight header at
+// the end of packed_b. Matmul kernels launched with programmatic dependent
+// launch may start loading their packed weights as soon as the kernel before
+// them on the stream begins to exit; ending the prepack with this kernel,
+// which writes nothing the matmul kernels read, puts a full kernel boundary
+// between the writes of the packed weights and any such early load.
+// The header fills the first 80 of its 256 bytes; the rest are zeros, so
+// the packed bytes of a weight are fully determined by its contents.
+__global__ void prepack_fence_kernel(const mnb_packed_header h, uint64_t *dst) {
+  static_assert(sizeof(mnb_packed_header) % 8 == 0 && MNB_PACKED_HEADER_BYTES == 32 * 8,
+                "one 8-byte word per thread");
+  const int i = threadIdx.x;
+  if (!dst || i >= 32) return;
+  uint64_t w = 0;
+  if (i < static_cast<int>(sizeof(h) / 8)) w = reinterpret_cast<const uint64_t *>(&h)[i];
+  dst[i] = w;
+}
 
 inline unsigned grid_for(int64_t total) {
   int64_t blocks = ceil_div(total, 256);
@@ -243,7 +254,7 @@ cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream) {
   else if (a.zp != nullptr)
     pack_zp_kernel<<<grid_for(N16 * nbz), 256, 0, stream>>>(
         NBitsZp{a.zp, nb}, static_cast<uint64_t *>(a.packed_zp), a.N, nb, nbz, N16 * nbz);
-  prepack_fence_kernel<<<1, 32, 0, stream>>>();
+  prepack_fence_kernel<<<1, 32, 0, stream>>>(a.header, static_cast<uint64_t *>(a.header_dst));
   return cudaGetLastError();
 }
 

@@ -1,6 +1,8 @@
 """C-ABI checks that need no GPU: the library loads, exports every entry
 point include/mnb.h declares, and rejects invalid arguments on the host
-before touching a device."""
+before touching a device, including a packed weight whose recorded header
+does not match the call (fake device addresses: the header records are
+host-side, so registering one needs no device)."""
 import ctypes
 import os
 import re
@@ -42,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert mnb.mnb_version() >> 16 == 1
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         assert mnb.status_string(code).startswith("MNB_")
     assert "unknown" in mnb.status_string(42)
 
@@ -53,7 +55,7 @@ def test_version_and_status_strings(lib):
 def test_prepacked_sizes(lib, N, K, bs, zp, dt):
     b, s, z = mnb.mnb_prepacked_sizes(N, K, bs, dt, zp)
     n16, k64, nb = -(-N // 16), -(-K // 64), -(-K // bs)
-    assert b == n16 * k64 * 512
+    assert b == n16 * k64 * 512 + 256  # the codes, then the packed-weight header
     assert s == n16 * nb * 16 * (4 if dt == torch.float32 else 2)
     assert z == (n16 * (-(-nb // 2) * 2) * 8 if zp else 0)
 
@@ -175,6 +177,14 @@ def _build(lib, arr, n=None, M=1, bs=32, a_t=1, s_t=1, plan=None, plan_bytes=0):
 NO_DEVICE = (-7, -9)  # validation passed; the call then needs a device
 
 
+def _register(lib, ptr, N, K, bs, s_t, zp, codes=0):
+    """Records, for a fake device address, the header a prepack call would write."""
+    h = binding.PackedHeaderC()
+    assert lib.mnb_packed_header_make(N, K, bs, s_t, int(zp), codes, ctypes.byref(h)) == 0
+    assert lib.mnb_packed_register(ctypes.c_void_p(ptr), ctypes.byref(h)) == 0
+    return h
+
+
 def test_chain_build_rejects_invalid_arguments_on_host(lib):
     assert lib.mnb_chain_build(None, 1, 1, 32, 1, 1, None, 0, None, None) == -1
     assert _build(lib, _chain_ops(2), n=0) == -2
@@ -194,6 +204,8 @@ def test_chain_build_rejects_invalid_arguments_on_host(lib):
 
 
 def test_chain_build_checks_hazards_on_host(lib):
+    for j in range(3):
+        _register(lib, ((j + 1) << 24) + (2 << 20), 16, 64, 32, 1, False)
     y0 = (1 << 24) + (1 << 20)
     a0 = 1 << 24
     # op 1 reads op 0's output: needs the dependency
@@ -249,7 +261,9 @@ def test_matmul_rmsnorm_rejects_invalid_arguments_on_host(lib):
     assert call(Y=v(1 << 16)) == -6            # Y over A
     assert call(am=v((1 << 22) + 8)) == -6     # argmax over Y
     assert call(gamma=v(1 << 22)) == -6        # Y over gamma
+    _register(lib, 1 << 20, 16, 64, 32, 1, False)
     assert call(nrm=0, gamma=v(1 << 22)) in (-7, -9)  # gamma unused without normalize
+    assert call(bs=64) == -10                  # packed with block_size 32
 
 
 def test_bnb4_rejects_invalid_arguments_on_host(lib):
@@ -290,7 +304,109 @@ def test_matmul_ws_checks_its_workspace_on_host(lib):
     assert _call_matmul_ws(lib, far, 1 << 20, path=4) == -8
     # A valid request reaches the device query, which fails without a GPU
     # (MNB_ERR_CUDA, or MNB_ERR_DEVICE for another architecture).
+    assert _call_matmul_ws(lib, far, 1 << 20, packed_b=1 << 12) == -10  # no header recorded
     import torch
+    _register(lib, 256, 16, 64, 32, 1, False)
     if not torch.cuda.is_available():
         assert _call_matmul_ws(lib, far, 1 << 20) in (-7, -9)
         assert lib.mnb_matmul_workspace_size() == 0
+
+
+# --- packed-weight headers -------------------------------------------------------
+
+def test_packed_header_fields(lib):
+    h = _register(lib, 1 << 32, 3072, 1024, 32, 0, True)
+    assert h.magic == binding.MNB_PACKED_MAGIC and h.version == 1 and h.codes == 0
+    assert (h.N, h.K, h.block_size, h.scale_dtype, h.has_zero_points) == (3072, 1024, 32, 0, 1)
+    sizes = mnb.mnb_prepacked_sizes(3072, 1024, 32, torch.float32, True)
+    assert (h.packed_b_bytes, h.packed_scales_bytes, h.packed_zp_bytes) == sizes
+    assert bytes(h)[:8] == b"MNB4PACK"
+    h2 = binding.PackedHeaderC()
+    # a code-book weight carries no zero points; unknown code forms are refused
+    assert lib.mnb_packed_header_make(16, 64, 32, 0, 1, 1, ctypes.byref(h2)) == -8
+    assert lib.mnb_packed_header_make(16, 64, 32, 0, 0, 2, ctypes.byref(h2)) == -8
+    assert lib.mnb_packed_header_make(16, 64, 24, 0, 0, 0, ctypes.byref(h2)) == -3
+    assert lib.mnb_packed_header_make(16, 64, 32, 0, 0, 0, None) == -1
+
+
+def test_register_refuses_a_damaged_header(lib):
+    h = binding.PackedHeaderC()
+    assert lib.mnb_packed_header_make(160, 640, 64, 1, 0, 0, ctypes.byref(h)) == 0
+    ptr = ctypes.c_void_p(3 << 32)
+    for field, value in (("magic", 1), ("version", 2), ("N", 161), ("check", h.check ^ 1),
+                         ("packed_b_bytes", h.packed_b_bytes + 16)):
+        bad = binding.PackedHeaderC.from_buffer_copy(h)
+        setattr(bad, field, value)
+        assert lib.mnb_packed_register(ptr, ctypes.byref(bad)) == -10, field
+    assert lib.mnb_packed_register(None, ctypes.byref(h)) == -1
+    assert lib.mnb_packed_register(ptr, None) == -1
+
+
+@pytest.mark.parametrize("kw", [dict(N=32), dict(K=128), dict(bs=64), dict(s_t=0),
+                                dict(zp=1 << 23)])
+def test_matmul_refuses_a_layout_mismatch_before_any_launch(lib, kw):
+    """A weight packed with N=16, K=64, bs=32, bf16 scales and no zero points,
+    called with one of those changed: MNB_ERR_LAYOUT, nothing enqueued (the
+    same call with the recorded layout goes on to the device query)."""
+    pb = 5 << 32
+    _register(lib, pb, 16, 64, 32, 1, False)
+    base = dict(packed_b=pb, scales=(5 << 32) + (1 << 20), A=6 << 32, Y=7 << 32, a_t=1, s_t=1)
+    assert _call_matmul(lib, **base) in NO_DEVICE
+    base.update(kw)
+    assert _call_matmul(lib, **base) == -10
+    assert "differs in" in lib.mnb_last_error_string().decode()
+
+
+def test_layout_checks_cover_every_reader_of_a_packed_weight(lib):
+    v = ctypes.c_void_p
+    pb, ps = 9 << 32, (9 << 32) + (1 << 20)
+    A, Y = v(10 << 32), v(11 << 32)
+    _register(lib, pb, 16, 64, 32, 1, False)
+    # unknown packed_b, and a forgotten one
+    assert _call_matmul(lib, packed_b=12 << 32, scales=ps, A=10 << 32, Y=11 << 32, a_t=1,
+                        s_t=1) == -10
+    assert lib.mnb_packed_forget(v(pb)) == 0
+    assert _call_matmul(lib, packed_b=pb, scales=ps, A=10 << 32, Y=11 << 32, a_t=1,
+                        s_t=1) == -10
+    _register(lib, pb, 16, 64, 32, 1, False)
+    # grouped (second weight's K differs), gated pair (up unknown)
+    arr = (ctypes.c_void_p * 2)(pb, pb)
+    sc = (ctypes.c_void_p * 2)(ps, ps)
+    ns = (ctypes.c_int64 * 2)(16, 16)
+    ys = (ctypes.c_void_p * 2)(11 << 32, (11 << 32) + (1 << 20))
+    assert lib.mnb_matmul_grouped(A, 2, arr, sc, None, None, ns, ys, 1, 64, 32, 1, 1,
+                                  None) in NO_DEVICE
+    assert lib.mnb_matmul_grouped(A, 2, arr, sc, None, None, ns, ys, 1, 128, 32, 1, 1,
+                                  None) == -10
+    assert lib.mnb_matmul_gate_up(A, v(pb), v(ps), None, None, v(13 << 32), v(ps), None,
+                                  None, 1, 16, 64, 32, Y, 1, 1, None) == -10
+    # the code-book form is not the affine one, either way round
+    assert lib.mnb_matmul_bnb4(A, v(pb), v(ps), v(14 << 32), None, 1, 16, 64, 32, Y, 1, 1,
+                               None) == -10
+    _register(lib, 15 << 32, 16, 64, 32, 1, False, codes=1)
+    assert lib.mnb_matmul_bnb4(A, v(15 << 32), v(ps), v(14 << 32), None, 1, 16, 64, 32, Y,
+                               1, 1, None) in NO_DEVICE
+    assert _call_matmul(lib, packed_b=15 << 32, scales=ps, A=10 << 32, Y=11 << 32, a_t=1,
+                        s_t=1) == -10
+    # unprepack, and a chain op whose weight has zero points it was not packed with
+    assert lib.mnb_unprepack(v(pb), v(ps), None, 16, 64, 64, 1, v(16 << 32), v(17 << 32),
+                             None, None) == -10
+    ops = _chain_ops(1, over={0: {"packed_b": pb, "packed_scales": ps}})
+    assert _build(lib, ops) in NO_DEVICE
+    assert _build(lib, ops, bs=64) == -10
+
+
+def test_graph_calls_reject_invalid_arguments_on_host(lib):
+    v = ctypes.c_void_p
+    h = v()
+    assert lib.mnb_graph_build(None, 1, 1, 32, 1, 1, ctypes.byref(h)) == -1
+    assert lib.mnb_graph_build(_chain_ops(1), 1, 1, 32, 1, 1, None) == -1
+    assert lib.mnb_graph_build(_chain_ops(1), 0, 1, 32, 1, 1, ctypes.byref(h)) == -2
+    assert lib.mnb_graph_build(_chain_ops(1), 1, 0, 32, 1, 1, ctypes.byref(h)) == -2
+    assert lib.mnb_graph_build(_chain_ops(2, over={1: {"Y": None}}), 2, 1, 32, 1, 1,
+                               ctypes.byref(h)) == -1
+    assert not h.value  # nothing built
+    for fn in (lib.mnb_graph_run, lib.mnb_graph_destroy):
+        assert (fn(None, None) if fn is lib.mnb_graph_run else fn(None)) == -1
+    assert lib.mnb_graph_info(None, None, None) == -1
+    assert lib.mnb_graph_run_from_host(None, None, None, 0, None, None, 0, None) == -1

@@ -1,10 +1,13 @@
 """Parity of the decode step exactly as the benchmark times it: the Qwen3-4B
 batch-1 step (M = 1, bf16, bs 128, no zero points; 253 weights, 2.08 GB)
-captured as one CUDA graph of 145 programmatically dependent launches (fused
-q/k/v, o, the gated-MLP pair, down, then lm_head), replayed, and checked
-against the oracle on the raw inputs of selected launches (drawn by the same
-seeded device generator as the benchmark, copied to the host). Small
-projections are checked in full, lm_head on seeded columns."""
+recorded by the library as one CUDA graph of 145 programmatically dependent
+calls (mnb_graph_build: fused q/k/v, o, the gated-MLP pair, down, then
+lm_head), run with mnb_graph_run, and checked against the oracle on the raw
+inputs of selected launches (drawn by the same seeded device generator as
+the benchmark, copied to the host). Small projections are checked in full,
+lm_head on seeded columns. The run framed by host copies
+(mnb_graph_run_from_host, the benchmark's end-to-end form) returns the same
+outputs."""
 import numpy as np
 import pytest
 import torch
@@ -29,19 +32,18 @@ def dev():
 
 def test_decode_step_graph_matches_oracle(dev):
     launches, A_all, Y_all, _, kept = bench.build_decode_step(dev, keep=KEEP)
-    stream = torch.cuda.Stream()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            for name, ws, A, Ys in launches:
-                bench.run_launch(mnb, name, ws, A, Ys)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for name, ws, A, Ys in launches:
-            bench.run_launch(mnb, name, ws, A, Ys)
+    graph = mnb.mnb_graph_build(bench.step_ops(mnb, launches))
+    assert (graph.calls, graph.kernels) == (145, 145)
     Y_all.fill_(float("nan"))
-    graph.replay()
+    graph.run()
     torch.cuda.synchronize()
+    Y_first = Y_all.clone()
+    A_host = A_all.cpu().pin_memory()
+    Y_host = torch.full(Y_all.shape, float("nan"), dtype=Y_all.dtype).pin_memory()
+    Y_all.fill_(float("nan"))
+    graph.run_from_host(A_host, A_all, Y_all, Y_host)
+    torch.cuda.synchronize()
+    assert torch.equal(Y_host, Y_first.cpu())
     outs = {name: Ys for name, _, _, Ys in launches}
     rng = np.random.default_rng(5)
     for name in KEEP:
