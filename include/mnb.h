@@ -477,18 +477,23 @@ MNB_API void mnb_test_wait_fault(int stop_stage, unsigned int wait_limit);
  *   Y[m,n]  = sum_k a'[m,k] * dequant(B)[n,k] + bias[n]
  *   argmax[m] = the smallest n with the largest Y[m,n]
  *
- * in one decode-kernel launch (plus a one-thread-per-row finishing kernel
- * for the ArgMax). gamma: fp32 [K] DEVICE or NULL (1); the sum of squares
- * and the scale are fp32; a normalized bf16 row is rounded to bf16 once
- * before the products (as the unfused graph rounds the normalization's
- * output). Y [M, N] in A's dtype, or NULL when only argmax is wanted (the
- * logits are then never written). argmax: int64 [M] DEVICE or NULL; the
- * comparison uses the fp32 value of each output before it is rounded to
- * A's dtype. M <= 16 (the decode path). Other arguments as mnb_matmul.
+ * in one decode-kernel launch for M <= 16 (plus a one-block finishing kernel
+ * for the ArgMax). Prefill rows (M > 16, bf16 activations whose rows TMA
+ * can stage, no ArgMax) run the tensor-core kernel in one launch: each
+ * staged A tile is multiplied by gamma in place and every output row scaled
+ * by its r[m], summed over the whole K (no K split); other rows (fp32, rows
+ * not 16-byte aligned, or with the ArgMax) run the decode kernel over
+ * 16-row slices, each normalizing its own rows. gamma: fp32 [K] DEVICE or
+ * NULL (1); the sum of squares and the scale are fp32; a normalized bf16
+ * row is rounded to bf16 once before the products (as the unfused graph
+ * rounds the normalization's output). Y [M, N] in A's dtype, or NULL when
+ * only argmax is wanted (the logits are then never written). argmax: int64
+ * [M] DEVICE or NULL; the comparison uses the fp32 value of each output
+ * before it is rounded to A's dtype. Other arguments as mnb_matmul.
  * Errors: as mnb_matmul; MNB_ERR_NULL if Y and argmax are both NULL;
  * MNB_ERR_SHAPE for normalize not 0/1 or a negative or non-finite epsilon;
  * MNB_ERR_ALIGN for gamma (4 bytes) or argmax (8 bytes); MNB_ERR_ALIAS if Y
- * or argmax overlaps an input or each other; MNB_ERR_UNSUPPORTED for M > 16.
+ * or argmax overlaps an input or each other.
  */
 MNB_API mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
                                       float epsilon, const void *packed_b,

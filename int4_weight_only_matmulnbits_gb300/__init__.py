@@ -12,7 +12,8 @@ from .binding import (EXPORTS, MNB_CODES_AFFINE, MNB_CODES_CODEBOOK, ChainOp, Mn
                       mnb_matmul_rmsnorm, mnb_matmul_workspace, mnb_packed_forget,
                       mnb_packed_header_make, mnb_packed_read_header, mnb_packed_register,
                       mnb_prepack, mnb_prepack_bnb4, mnb_prepack_qdq, mnb_prepacked_sizes,
-                      mnb_set_programmatic_launch, mnb_unprepack, mnb_version, status_string)
+                      mnb_set_programmatic_launch, mnb_test_wait_fault, mnb_unprepack,
+                      mnb_version, status_string)
 from ._build import build_library
 
 __all__ = ["EXPORTS", "MNB_CODES_AFFINE", "MNB_CODES_CODEBOOK", "ChainOp", "MnbChain",
@@ -23,4 +24,5 @@ __all__ = ["EXPORTS", "MNB_CODES_AFFINE", "MNB_CODES_CODEBOOK", "ChainOp", "MnbC
            "mnb_matmul_workspace", "mnb_packed_forget", "mnb_packed_header_make",
            "mnb_packed_read_header", "mnb_packed_register", "mnb_prepack", "mnb_prepack_bnb4",
            "mnb_prepack_qdq", "mnb_prepacked_sizes", "mnb_set_programmatic_launch",
+           "mnb_test_wait_fault",
            "mnb_unprepack", "mnb_version", "status_string"]

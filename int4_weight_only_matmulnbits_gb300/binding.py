@@ -659,8 +659,9 @@ def mnb_matmul_rmsnorm(A: torch.Tensor, w: PackedWeight, bias: torch.Tensor | No
                        normalize: bool = True, logits: bool = True, argmax: bool = False,
                        out: torch.Tensor | None = None, stream=None):
     """Y = rmsnorm(A; gamma, eps) @ dequant(w)^T + bias (normalize=False: plain
-    A), and optionally the greedy ArgMax of each row, in one decode launch
-    (M <= 16). Returns (Y or None, argmax int64 [M] or None)."""
+    A), and optionally the greedy ArgMax of each row: one decode launch for
+    M <= 16, the tensor-core kernel for bf16 prefill rows, 16-row decode
+    slices otherwise. Returns (Y or None, argmax int64 [M] or None)."""
     if A.dim() != 2 or A.shape[1] != w.K or not A.is_cuda or not A.is_contiguous():
         raise ValueError(f"A must be a contiguous CUDA [M, {w.K}] tensor")
     for name, t in (("bias", bias), ("gamma", gamma)):

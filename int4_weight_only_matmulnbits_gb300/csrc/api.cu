@@ -873,12 +873,6 @@ mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
       (bias && !aligned(bias, 4)) || (gamma && !aligned(gamma, 4)) ||
       (argmax && !aligned(argmax, 8)))
     return MNB_ERR_ALIGN;
-  if (M > kGemvMaxM) {
-    std::snprintf(g_last_error, sizeof g_last_error,
-                  "mnb_matmul_rmsnorm serves the decode path, M <= %d (M=%lld)", kGemvMaxM,
-                  (long long)M);
-    return MNB_ERR_UNSUPPORTED;
-  }
   const Sizes in = packed_sizes(N, K, block_size, scale_dtype, zero_points != nullptr);
   const void *ins[6] = {A, packed_b, scales, zero_points, bias, normalize ? gamma : nullptr};
   const size_t in_n[6] = {size_t(M) * K * es, in.b, in.s, in.z, bias ? size_t(N) * 4 : 0,
@@ -895,20 +889,34 @@ mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
   if (st != MNB_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
+  if (M > kGemvMaxM && !argmax && Y) {
+    // Prefill rows: the tensor-core kernel normalizes each staged A tile
+    // and scales its output rows, when it can stage these activations.
+    MatmulArgs t{A, packed_b, scales, zero_points, bias, Y, M, N, K, block_size,
+                 a_dtype == MNB_F32, scale_dtype == MNB_F32, g_pdl.load() != 0};
+    t.norm = normalize != 0;
+    t.gamma = normalize ? gamma : nullptr;
+    t.eps = epsilon;
+    if (!t.a_f32 && gemm_supports(t)) {
+      e = launch_gemm(t, s);
+      if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_rmsnorm");
+      return MNB_OK;
+    }
+  }
   if (argmax)
     e = launch_argmax_init(reinterpret_cast<unsigned long long *>(argmax), static_cast<int>(M),
                            s);
   if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_rmsnorm (ArgMax keys)");
+  // The decode kernel, over 16-row slices beyond 16 rows (fp32 rows, rows the
+  // tensor core cannot stage, or with the ArgMax): each slice normalizes
+  // its own rows over the whole of K.
   GroupArgs g{};
-  g.A = A;
   g.count = 1;
   g.packed_b[0] = packed_b;
   g.scales[0] = scales;
   g.zp[0] = zero_points;
   g.bias[0] = bias;
-  g.Y[0] = Y;
   g.N[0] = N;
-  g.M = M;
   g.K = K;
   g.bs = block_size;
   g.a_f32 = a_dtype == MNB_F32;
@@ -918,8 +926,13 @@ mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float *gamma,
   g.norm = normalize != 0;
   g.gamma = normalize ? gamma : nullptr;
   g.eps = epsilon;
-  g.amax = reinterpret_cast<unsigned long long *>(argmax);
-  e = launch_gemv_group(g, s);
+  for (int64_t m0 = 0; m0 < M && e == cudaSuccess; m0 += kGemvMaxM) {
+    g.M = std::min<int64_t>(kGemvMaxM, M - m0);
+    g.A = static_cast<const char *>(A) + size_t(m0) * K * es;
+    g.Y[0] = Y ? static_cast<char *>(Y) + size_t(m0) * N * es : nullptr;
+    g.amax = argmax ? reinterpret_cast<unsigned long long *>(argmax) + m0 : nullptr;
+    e = launch_gemv_group(g, s);
+  }
   if (e == cudaErrorNotSupported) {
     std::snprintf(g_last_error, sizeof g_last_error, "no kernel for M=%lld N=%lld K=%lld bs=%d",
                   (long long)M, (long long)N, (long long)K, block_size);

@@ -93,6 +93,14 @@ struct GemmParams {
   int sc_bytes, zp_bytes;  // per stage
   int ksplit, kps;  // CTAs splitting K (cluster along z), k stages per CTA
   int paired;       // gate (tiles 0-3 of the B tile) and up (tiles 4-7)
+  // RMS-normalized activations (the fusion "RMSNorm into packed projection
+  // input"): the staged A tile becomes A * gamma (rounded to bf16 once) and
+  // each output row is scaled by r[m] = 1 / sqrt(mean_k A[m,k]^2 + eps),
+  // summed over the whole row from the staged tiles (needs ksplit == 1).
+  int norm;
+  const float *gamma;  // [K] or null (1)
+  float eps;
+  int K;
   int sc_up, zp_up;  // paired: byte offsets of the up halves in a stage's scales / zero points
 };
 
@@ -419,6 +427,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
         }
       }
     }
+    // RMS normalization: thread e of the dequantisation warps takes A row
+    // nrow of the tile (two threads a row for 128-row tiles), chunks nc0 ..
+    // nc0 + kNormChunks - 1 of every stage.
+    constexpr int kNormChunks = MH == 1 ? 4 : 8;
+    const int ne = tid - 64;
+    const int nrow = MH == 1 ? (ne >> 1) : ne, nc0 = MH == 1 ? (ne & 1) * 4 : 0;
+    float nss = 0.f;
     for (int i = 0; i < nk; ++i) {
       const int s = i % kWStages, bslot = i % kBStages, kb = kb0 + i;
       if (!mbar_wait(wfull + s, (i / kWStages) & 1) ||
@@ -462,6 +477,37 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
           zc1[bi] = (0x4300u | ((zw.y >> (4 * g)) & 15)) * 0x10001u;
         }
       }
+      if (p.norm) {
+        // The stage's A tile (swizzled rows of 128 bytes): this thread's row
+        // and chunks, sum of squares of the raw values, then A * gamma in
+        // place.
+        const int sa = i % kAStages;
+        if (!mbar_wait(afull + sa, (i / kAStages) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          fault = true;
+          break;
+        }
+        unsigned char *arow = smem + S::kA + sa * S::kATileBytes + nrow * 128;
+#pragma unroll
+        for (int c = nc0; c < nc0 + kNormChunks; ++c) {
+          uint4 *q = reinterpret_cast<uint4 *>(arow + ((c ^ (nrow & 7)) * 16));
+          const uint4 x = *q;
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t o[4];
+          const int k0 = kb * kBK + 8 * c;
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float a0 = bf16_bits_to_f32(w[e2] & 0xFFFFu), a1 = bf16_bits_to_f32(w[e2] >> 16);
+            nss = fmaf(a0, a0, nss);
+            nss = fmaf(a1, a1, nss);
+            const int k = k0 + 2 * e2;
+            const float g0 = p.gamma ? (k < p.K ? __ldg(p.gamma + k) : 0.f) : 1.f;
+            const float g1 = p.gamma ? (k + 1 < p.K ? __ldg(p.gamma + k + 1) : 0.f) : 1.f;
+            o[e2] = bf16_bits(a0 * g0) | (bf16_bits(a1 * g1) << 16);
+          }
+          *q = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
       const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + tile * kChunkBytes + lane * 16);
       const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
@@ -498,7 +544,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
       record_fault(&g_fault_gemm, kFaultGemmWait);
       fault = true;
     }
-    named_barrier_sync(kBarEpi, 32 * kDqWarps);  // bias staged
+    // r[m] of every row of the tile, in the B slot the MMAs have drained.
+    float *sNorm = reinterpret_cast<float *>(smem + S::kB);
+    if (p.norm) {
+      const float ss = MH == 1 ? nss + __shfl_xor_sync(0xffffffffu, nss, 1) : nss;
+      if (!fault && (MH == 2 || (ne & 1) == 0))
+        sNorm[nrow] = 1.f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
+    }
+    named_barrier_sync(kBarEpi, 32 * kDqWarps);  // bias and r staged
     if (!fault && MH == 1 && p.ksplit > 1) {
       // Park the accumulator, column-major [col][row], in the drained
       // operand rings.
@@ -568,8 +621,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
           float v[32];
           tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + h * kBN + c * 32, v);
           float o[32];
+          const float rn = p.norm ? sNorm[row] : 1.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[out_col(i)] = v[i] + sBias[c * 32 + out_col(i)];
+          for (int i = 0; i < 32; ++i) o[out_col(i)] = v[i] * rn + sBias[c * 32 + out_col(i)];
           unsigned char *box = stage + (c >> 1) * kBoxBytes + row * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -611,8 +665,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
             const int n0 = n_base + c * 32;
             uint16_t *yrow = static_cast<uint16_t *>(p.Y) + static_cast<int64_t>(m) * p.N;
             float o[32];
+            const float rn = p.norm ? sNorm[h * kBH + quarter * 32 + lane] : 1.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[out_col(i)] = v[i] + sBias[c * 32 + out_col(i)];
+            for (int i = 0; i < 32; ++i) o[out_col(i)] = v[i] * rn + sBias[c * 32 + out_col(i)];
             if (n0 + 32 <= p.N && p.y_vec) {
 #pragma unroll
               for (int i = 0; i < 32; i += 8) {
@@ -1744,6 +1799,10 @@ cudaError_t launch_gemm_tf32(const MatmulArgs &a, cudaStream_t stream) {
   const int ksplit = plan_gemm_tf32(a, sm_count());
   p.ksplit = ksplit;
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
+  p.norm = a.norm ? 1 : 0;
+  p.K = static_cast<int>(a.K);
+  p.gamma = a.gamma;
+  p.eps = a.eps;
   const dim3 grid(static_cast<unsigned>(ceil_div(a.N, int64_t(kBN))),
                   static_cast<unsigned>(ceil_div(a.M, int64_t(kBH))),
                   static_cast<unsigned>(ksplit));
@@ -1776,7 +1835,8 @@ GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
   {
     bool have = false;
     for (int h = 1; h <= 2; ++h)
-      for (int c = 1; c <= (h == 1 ? (a.paired ? 4 : 8) : 1); c *= 2) {
+      // A normalized row needs its whole K in one CTA: no K split.
+      for (int c = 1; c <= (h == 1 ? (a.norm ? 1 : a.paired ? 4 : 8) : 1); c *= 2) {
         const int64_t kps = ceil_div(int64_t(K64), int64_t(c));
         if (c > 1 && (kps < 4 || (c - 1) * kps >= int64_t(K64))) continue;
         const int64_t ctas = ceil_div(a.M, int64_t(kBH) * h) * ceil_div(a.N, cols) * c;
@@ -1803,7 +1863,7 @@ GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
   // for each further tile a CTA's range touches. It wins where whole tiles
   // leave half the CTA slots idle for long (down and o projections with
   // M >= 2048, 4096) and loses where tiles are few or short.
-  if (a.ws && !a.paired && a.ws_bytes > kSkCountBytes) {
+  if (a.ws && !a.paired && !a.norm && a.ws_bytes > kSkCountBytes) {
     const int64_t tiles_n = ceil_div(a.N, int64_t(kBN));
     const int64_t units = ceil_div(a.M, int64_t(2 * kBH)) * tiles_n * int64_t(K64);
     const int64_t room = static_cast<int64_t>((a.ws_bytes - kSkCountBytes) / kSkCtaBytes);
@@ -1828,7 +1888,8 @@ GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
 
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   if (!gemm_supports(a)) return cudaErrorNotSupported;
-  if (a.sk_only && (a.a_f32 || a.paired || !a.ws)) return cudaErrorNotSupported;
+  if (a.sk_only && (a.a_f32 || a.paired || a.norm || !a.ws)) return cudaErrorNotSupported;
+  if (a.norm && (a.a_f32 || a.paired)) return cudaErrorNotSupported;
   if (a.a_f32) return launch_gemm_tf32(a, stream);
   GemmParams p{};
   const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
@@ -1909,6 +1970,10 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
   p.ksplit = ksplit;
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
+  p.norm = a.norm ? 1 : 0;
+  p.K = static_cast<int>(a.K);
+  p.gamma = a.gamma;
+  p.eps = a.eps;
   // TMA stores of the output tile: single weight, no K split, rows of Y a
   // multiple of 16 bytes from a 16-byte aligned base.
   if (!sk && !a.paired && ksplit == 1 && (a.N % 8) == 0 &&

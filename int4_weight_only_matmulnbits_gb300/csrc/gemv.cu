@@ -764,16 +764,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 // atomic only after its dependency wait, i.e. after this kernel.
 __global__ void argmax_init_kernel(unsigned long long *amax, int M) {
   grid_dependents_launch();
-  if (static_cast<int>(threadIdx.x) < M) amax[threadIdx.x] = 0ull;
+  for (int m = threadIdx.x; m < M; m += blockDim.x) amax[m] = 0ull;
 }
 
-// Turns the ArgMax keys into indices in place (one thread per row); launched
-// as a programmatic dependent of the decode kernel, it is resident before
-// that kernel ends and waits for its results.
+// Turns the ArgMax keys into indices in place (a thread per row, striding
+// over the rows); launched as a programmatic dependent of the decode kernel,
+// it is resident before that kernel ends and waits for its results.
 __global__ void argmax_finalize_kernel(unsigned long long *amax, int M) {
   grid_dependency_wait();
-  const int m = threadIdx.x;
-  if (m < M) {
+  for (int m = threadIdx.x; m < M; m += blockDim.x) {
     const unsigned long long key = amax[m];
     amax[m] = static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(key));
   }
@@ -1074,7 +1073,7 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
 }
 
 cudaError_t launch_argmax_init(unsigned long long *amax, int M, cudaStream_t stream) {
-  argmax_init_kernel<<<1, 32, 0, stream>>>(amax, M);
+  argmax_init_kernel<<<1, 256, 0, stream>>>(amax, M);
   return cudaGetLastError();
 }
 
@@ -1082,7 +1081,7 @@ cudaError_t launch_argmax_finalize(unsigned long long *amax, int M, bool pdl,
                                    cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, 1, 1);
-  cfg.blockDim = dim3(32, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

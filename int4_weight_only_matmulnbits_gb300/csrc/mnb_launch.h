@@ -78,6 +78,11 @@ struct MatmulArgs {
   void *ws = nullptr;
   size_t ws_bytes = 0;
   bool sk_only = false;  // the stream-K schedule or cudaErrorNotSupported
+  // RMS-normalized activations (bf16, single weight, tensor-core kernel):
+  // A * gamma staged, outputs scaled by 1 / sqrt(mean A^2 + eps).
+  bool norm = false;
+  const float *gamma = nullptr;
+  float eps = 0.f;
 };
 
 // What launch_gemm would launch for a product on a GPU with `sms` SMs (host

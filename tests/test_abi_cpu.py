@@ -257,7 +257,6 @@ def test_matmul_rmsnorm_rejects_invalid_arguments_on_host(lib):
     assert call(a_t=5) == -4
     assert call(gamma=v((1 << 17) + 2)) == -5
     assert call(am=v((1 << 23) + 4)) == -5
-    assert call(M=17) == -8
     assert call(Y=v(1 << 16)) == -6            # Y over A
     assert call(am=v((1 << 22) + 8)) == -6     # argmax over Y
     assert call(gamma=v(1 << 22)) == -6        # Y over gamma

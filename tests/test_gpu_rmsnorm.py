@@ -149,8 +149,39 @@ def test_qwen3_4b_final_norm_lm_head_argmax(dev):
     check_logits(Y[:, cols], R[:, cols], mag[:, cols], "lm_head logits")
 
 
-def test_decode_path_only(dev):
-    prob = make_problem(17, 16, 64, 32, dtype=torch.bfloat16, seed=1)
-    with pytest.raises(mnb.MnbError) as e:
-        run(prob, dev, None)
-    assert e.value.status == -8
+@pytest.mark.parametrize("M", [17, 512, 2048])
+def test_prefill_rows_on_the_tensor_core_kernel(dev, M):
+    """M > 16 with bf16 rows TMA can stage: the tensor-core kernel normalizes
+    each staged A tile (A * gamma, rounded to bf16 once) and scales each
+    output row by r[m] over the whole K. Qwen3-4B-like K (2560, bs 128, zero
+    points, bias); seeded rows beyond 64 rows, every column."""
+    N, K = 1536, 2560
+    prob = make_problem(M, N, K, 128, dtype=torch.bfloat16, zero_points=True, bias=True,
+                        seed=M, scale_range=(0.002, 0.01))
+    gamma = torch.rand(K, generator=torch.Generator().manual_seed(M)) * 1.5 + 0.25
+    Y, _ = run(prob, dev, gamma)
+    rows = None if M <= 64 else np.sort(np.random.default_rng(M).choice(M, 48, replace=False))
+    R, mag = reference(prob, gamma, rows=rows)
+    check_logits(Y if rows is None else Y[rows], R, mag, f"prefill M{M}")
+
+
+@pytest.mark.parametrize("case", ["tails", "fp32", "argmax", "no_gamma", "plain"])
+def test_prefill_rows_other_forms(dev, case):
+    """Ragged tiles on the tensor-core kernel (M 300, N 1000, K 704); and the
+    forms served by 16-row decode slices: fp32 rows, rows TMA cannot stage
+    (K % 8 != 0) with the ArgMax; gamma absent; normalize = 0."""
+    M, N, K, dt = 300, 1000, 704, torch.bfloat16
+    if case == "fp32":
+        dt = torch.float32
+    if case == "argmax":
+        K = 700
+    prob = make_problem(M, N, K, 64, dtype=dt, zero_points=True, bias=True, seed=len(case))
+    gamma = None if case == "no_gamma" else (
+        torch.rand(K, generator=torch.Generator().manual_seed(5)) * 1.5 + 0.25)
+    normalize = case != "plain"
+    Y, idx = run(prob, dev, gamma, normalize=normalize, argmax=case == "argmax")
+    rows = np.sort(np.random.default_rng(3).choice(M, 40, replace=False))
+    R, mag = reference(prob, gamma, normalize=normalize, rows=rows)
+    check_logits(Y[rows], R, mag, f"prefill {case}")
+    if case == "argmax":
+        check_argmax(idx[rows], R, bound(R, mag, dt), Y[rows], "prefill argmax")
