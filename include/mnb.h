@@ -451,18 +451,20 @@ MNB_API mnb_status mnb_fault_status(unsigned int *fault_bits);
 
 /*
  * Test-only failure injection for the decode kernel (off by default), so that
- * the bounded waits above can be exercised without faulting a GPU: in every
- * decode-kernel launch made after this call whose CTAs work without a
- * cluster, CTA 0's producer issues weight stages 0 .. stop_stage - 1 and then
- * stops. Its consumers, having consumed every copy issued, wait for stage
- * stop_stage, give up after wait_limit iterations, record fault bit 1 and
- * end the launch (the CTA's outputs are then wrong; nothing is left in flight
- * and the context stays usable). wait_limit also caps every other wait of
- * those launches (0: the normal cap). stop_stage < 0 and wait_limit 0 turn
- * the injection off. Process-wide; launches recorded into a CUDA graph keep
- * the values of their recording.
+ * the bounded waits above can be exercised without faulting a GPU. While
+ * stop_stage >= 0, decode-kernel launches of one configuration (bf16
+ * activations and scales, block_size 128, no zero points, M <= 8) whose
+ * CTAs work without a cluster run a separate instantiation of the kernel
+ * whose waits give up after 2^16 iterations and whose CTA 0 producer issues
+ * weight stages 0 .. stop_stage - 1 and then stops. CTA 0's consumers, having
+ * consumed every copy issued, wait for stage stop_stage, give up, record
+ * fault bit 1 and end the launch (the CTA's outputs are then wrong; nothing
+ * is left in flight and the context stays usable). Every other launch, and
+ * every launch while stop_stage < 0, is unaffected (the normal kernels hold
+ * none of this). Process-wide; launches recorded into a CUDA graph keep the
+ * setting of their recording.
  */
-MNB_API void mnb_test_wait_fault(int stop_stage, unsigned int wait_limit);
+MNB_API void mnb_test_wait_fault(int stop_stage);
 
 /*
  * Projection of an RMS-normalized row, optionally followed by greedy ArgMax

@@ -188,7 +188,7 @@ def load(build_if_missing: bool = False):
         lib.mnb_graph_run.restype = i32
         lib.mnb_graph_run_from_host.argtypes = [p, p, p, sz, p, p, sz, p]
         lib.mnb_graph_run_from_host.restype = i32
-        lib.mnb_test_wait_fault.argtypes = [i32, ctypes.c_uint]
+        lib.mnb_test_wait_fault.argtypes = [i32]
         lib.mnb_test_wait_fault.restype = None
         lib.mnb_graph_destroy.argtypes = [p]
         lib.mnb_graph_destroy.restype = i32
@@ -252,10 +252,10 @@ def mnb_set_programmatic_launch(enable: bool) -> None:
     load().mnb_set_programmatic_launch(1 if enable else 0)
 
 
-def mnb_test_wait_fault(stop_stage: int = -1, wait_limit: int = 0) -> None:
+def mnb_test_wait_fault(stop_stage: int = -1) -> None:
     """Test-only failure injection in the decode kernel (see include/mnb.h);
-    the defaults turn it off."""
-    load().mnb_test_wait_fault(stop_stage, wait_limit)
+    the default turns it off."""
+    load().mnb_test_wait_fault(stop_stage)
 
 
 def mnb_fault_status() -> int:

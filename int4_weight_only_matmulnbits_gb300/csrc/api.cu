@@ -389,9 +389,7 @@ int mnb_version(void) { return (1 << 16) | 0; }
 
 void mnb_set_programmatic_launch(int enable) { g_pdl.store(enable ? 1 : 0); }
 
-void mnb_test_wait_fault(int stop_stage, unsigned int wait_limit) {
-  gemv_set_wait_fault(stop_stage, wait_limit);
-}
+void mnb_test_wait_fault(int stop_stage) { gemv_set_wait_fault(stop_stage); }
 
 mnb_status mnb_fault_status(unsigned int *fault_bits) {
   if (!fault_bits) return MNB_ERR_NULL;

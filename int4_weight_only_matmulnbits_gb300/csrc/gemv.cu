@@ -86,9 +86,8 @@ struct GemvParams {
   int cpw, scs;              // chunks per warp and stage; chunks per stage and tile (ksw*cpw)
   int krp, sg;               // staged activation row stride, block sums per row
   int nst, stage_bytes, stage_tx;  // ring depth, stage stride, bytes per stage
-  // Failure-detection test (mnb_test_wait_fault): every wait's iteration cap,
-  // and the stage at which CTA 0's producer stops issuing (-1: never).
-  uint32_t wait_limit;
+  // Failure-detection test (mnb_test_wait_fault; the PROBE instantiation
+  // only): the stage at which CTA 0's producer stops issuing.
   int stop_stage;
   // RMS-normalized activations (the fusion "RMSNorm into packed projection
   // input"): the staged row is A * gamma and every output is scaled by
@@ -221,9 +220,12 @@ __device__ __forceinline__ void store_gate_up(const GemvParams &p, int m, int n,
         static_cast<uint16_t>(bf16_bits(v));
 }
 
-template <int MT, int BS, bool HAS_ZP, bool SF32, bool CODE>
+// PROBE: the failure-detection test's instantiation (a short wait cap and a
+// producer that stops); every other launch compiles without it.
+template <int MT, int BS, bool HAS_ZP, bool SF32, bool CODE, bool PROBE = false>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     gemv_kernel(const __grid_constant__ GemvParams p) {
+  constexpr uint32_t kLimit = PROBE ? (1u << 16) : kWaitLimit;
   using G = BlockGeom<BS>;
   constexpr int kEs = SF32 ? 4 : 2;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -300,12 +302,12 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         // Test-only stop (launches without a cluster): the stage is never
         // issued, so CTA 0's consumers give up waiting for it; every copy
         // issued before it is consumed first, so none is left in flight.
-        if (issued == p.stop_stage && blockIdx.x == 0 && p.cluster == 1) {
+        if (PROBE && issued == p.stop_stage && blockIdx.x == 0 && p.cluster == 1) {
           ok = false;
           break;
         }
         ++issued;
-        if (wrapped && !mbar_wait(empty + slot, phase ^ 1, p.wait_limit)) {
+        if (wrapped && !mbar_wait_n<kLimit>(empty + slot, phase ^ 1)) {
           if (lane == 0) record_fault(&g_fault_gemv, kFaultGemvWait);
           ok = false;
           break;
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       const int n = p.K - k0 < kr ? static_cast<int>(p.K - k0) : kr;
       for (int e = n + tid; e < kr; e += kConsumers)
         for (int m = 0; m < p.M; ++m) sA[m * p.krp + e] = 0;
-      if (!mbar_wait(abar, 0, p.wait_limit)) {
+      if (!mbar_wait_n<kLimit>(abar, 0)) {
         record_fault(&g_fault_gemv, kFaultGemvWait);
         fault = true;
       }
@@ -535,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
       for (int j = 0; j < p.R && !fault; ++j) {
-        if (!mbar_wait(full + slot, phase, p.wait_limit)) {
+        if (!mbar_wait_n<kLimit>(full + slot, phase)) {
           record_fault(&g_fault_gemv, kFaultGemvWait);
           fault = true;
           break;
@@ -876,10 +878,10 @@ bool layout_for(const GroupArgs &a, int ksw, int cluster, int cpw, Choice &ch) {
   return true;
 }
 
-template <int MT, int BS, bool HAS_ZP, bool SF32, bool CODE = false>
+template <int MT, int BS, bool HAS_ZP, bool SF32, bool CODE = false, bool PROBE = false>
 cudaError_t launch_one(const GemvParams &p, const Choice &ch, int grid, bool pdl,
                        cudaStream_t stream) {
-  auto kernel = gemv_kernel<MT, BS, HAS_ZP, SF32, CODE>;
+  auto kernel = gemv_kernel<MT, BS, HAS_ZP, SF32, CODE, PROBE>;
   static std::atomic<unsigned long long> configured{0};
   if (const cudaError_t e = ensure_smem_limit(kernel, kSmemMax, configured); e != cudaSuccess)
     return e;
@@ -976,12 +978,8 @@ cudaError_t weight_maps(const GroupArgs &a, int i, int tpc, int scs, GemvParams 
 }  // namespace
 
 std::atomic<int> g_test_stop_stage{-1};
-std::atomic<uint32_t> g_test_wait_limit{0};
 
-void gemv_set_wait_fault(int stop_stage, uint32_t wait_limit) {
-  g_test_stop_stage.store(stop_stage < 0 ? -1 : stop_stage);
-  g_test_wait_limit.store(wait_limit);
-}
+void gemv_set_wait_fault(int stop_stage) { g_test_stop_stage.store(stop_stage < 0 ? -1 : stop_stage); }
 
 cudaError_t gemv_take_fault(unsigned int *out) {
   unsigned int zero = 0;
@@ -1057,8 +1055,6 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   p.R = best.R;
   p.cpw = best.cpw;
   p.scs = best.ksw * best.cpw;
-  const uint32_t wl = g_test_wait_limit.load();
-  p.wait_limit = wl ? wl : kWaitLimit;
   p.stop_stage = g_test_stop_stage.load();
 
   // Persistent grid: every tile group gets a CTA (cluster) when they fit in
@@ -1068,6 +1064,8 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream) {
   const int64_t clusters = tg < resident ? tg : resident;
   const int grid = static_cast<int>(clusters) * best.cluster;
 
+  if (p.stop_stage >= 0 && MT == 1 && a.bs == 128 && !a.has_zp && !a.scale_f32 && !a.code)
+    return launch_one<1, 128, false, false, false, true>(p, best, grid, a.pdl, stream);
   return MT == 2 ? launch_bs<2>(p, best, grid, a.bs, a.has_zp, a.scale_f32, a.pdl, stream)
                  : launch_bs<1>(p, best, grid, a.bs, a.has_zp, a.scale_f32, a.pdl, stream);
 }

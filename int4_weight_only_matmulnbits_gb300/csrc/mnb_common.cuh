@@ -173,12 +173,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait; returns false if the cap (kWaitLimit unless given) was reached.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          uint32_t limit = kWaitLimit) {
-  for (uint32_t i = 0; i < limit; ++i)
+// Bounded wait; returns false if the cap was reached.
+template <uint32_t kLimit = kWaitLimit>
+__device__ __forceinline__ bool mbar_wait_n(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  return mbar_wait_n<kWaitLimit>(bar, parity);
 }
 
 // 1-D bulk copy global -> this CTA's shared memory, completing on bar.

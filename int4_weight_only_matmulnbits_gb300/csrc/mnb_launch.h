@@ -102,7 +102,7 @@ size_t gemm_workspace_bytes();
 
 cudaError_t launch_prepack(const PrepackArgs &a, cudaStream_t stream);
 // Test-only failure injection for the decode kernel (mnb_test_wait_fault).
-void gemv_set_wait_fault(int stop_stage, uint32_t wait_limit);
+void gemv_set_wait_fault(int stop_stage);
 cudaError_t launch_unprepack(const UnprepackArgs &a, cudaStream_t stream);
 
 // Up to kMaxGroup weights that share one activation matrix A (fused-N
