@@ -535,6 +535,26 @@ def single_gemv(mnb, dev, reps=30):
     return prob, {"cold_us": cold, "hot_us": hot, "algorithmic_bytes": prob.algorithmic_bytes()}
 
 
+def bnb4_prefill(mnb, dev, M=2048, N=9728, K=2560, bs=64, reps=10):
+    """The bitsandbytes-style 4-bit matrix at prefill size on the tensor-core
+    kernel's code-book mode: gate-sized weight (9728 x 2560, bs 64, bf16
+    absmax and activations, a 16-value code book), L2 flushed before each
+    launch, median of reps."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    B = torch.randint(0, 256, (N * K // 2,), dtype=torch.uint8, device=dev, generator=g)
+    absmax = (torch.rand(N * K // bs, device=dev, generator=g) * 0.04 + 0.01).to(torch.bfloat16)
+    code = torch.linspace(-1.0, 1.0, 16, device=dev)
+    w = mnb.mnb_prepack_bnb4(B, absmax, N, K, bs)
+    A = torch.randn(M, K, device=dev, generator=g).to(torch.bfloat16)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    us = _cold_launch_us(lambda: mnb.mnb_matmul_bnb4(A, w, code, out=Y), reps, flush)
+    return {"workload": f"MatMulBnb4 {N}x{K}, bs {bs}, bf16 absmax and A, M={M}, L2 flushed",
+            "us": us, "value": 2 * M * N * K / us / 1e6, "unit": "TFLOP/s"}
+
+
 def crossover(mnb, dev, flush):
     """Condensed GEMV / tensor-core crossover: device time per launch (L2
     flushed, median of 5) of both kernels and of the dispatch, on gate
@@ -704,6 +724,11 @@ def run_gpu(args, rank, world, dist):
                              "cpu": cpu_model(), "kind": "oracle",
                              "sample": f"the whole GEMV, {reps} runs"},
         }
+        bb, clk = clocked(local, lambda: bnb4_prefill(mnb, dev))
+        bb["roofline"] = dict(flops_peak, achieved=bb["value"], frac=bb["value"] / bf16_peak,
+                              traffic=None, kernel="gemm_kernel, code-book instantiation")
+        bb["clocks"] = clk
+        line["bnb4_prefill"] = bb
         flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
         cross, clk = clocked(local, lambda: crossover(mnb, dev, flush))
         line["crossover"] = {"unit": "us per launch, L2 flushed, median of 5", "rows": cross,

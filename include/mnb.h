@@ -526,11 +526,15 @@ MNB_API mnb_status mnb_matmul_rmsnorm(const void *A, int normalize, const float 
  * no zero points). Errors: as mnb_prepack; MNB_ERR_UNSUPPORTED when K is
  * not a multiple of block_size.
  *
- * mnb_matmul_bnb4 runs the decode kernel with the code book (over 8-row
- * slices beyond 8 rows): each CTA turns the 16 values into a table of bf16
- * pairs, each value c held as hi = bf16(c) and lo = bf16(c - hi) and both
+ * mnb_matmul_bnb4 runs the decode kernel with the code book for M <= 16
+ * (8-row launches): each CTA turns the 16 values into a table of bf16 pairs,
+ * each value c held as hi = bf16(c) and lo = bf16(c - hi) and both
  * multiplied by the activations, so every weight is within 2^-16 |c| of
- * code[q], times the fp32 or bf16 absmax applied in fp32. Errors: as mnb_matmul;
+ * code[q], times the fp32 or bf16 absmax applied in fp32. Above 16 rows,
+ * bf16 activations with 16-byte-aligned rows run the tensor-core kernel's
+ * code-book mode (w = code[q] * absmax formed in fp32 and fed as an exact
+ * hi + lo bf16 pair); other activations run 8-row decode launches.
+ * Errors: as mnb_matmul;
  * MNB_ERR_NULL for code; MNB_ERR_ALIAS if Y overlaps code.
  */
 MNB_API mnb_status mnb_prepack_bnb4(const uint8_t *B, const void *absmax, int64_t N,

@@ -994,6 +994,18 @@ mnb_status mnb_matmul_bnb4(const void *A, const void *packed_b, const void *pack
   if (overlap(Y, size_t(M) * N * dtype_size(a_dtype), code, 64)) return MNB_ERR_ALIAS;
   const size_t es = dtype_size(a_dtype);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M > kGemvMaxM) {
+    // Prefill rows: the tensor-core kernel's code-book mode, when it can
+    // stage these activations (bf16 rows, 16-byte aligned).
+    MatmulArgs t{A, packed_b, packed_scales, nullptr, bias, Y, M, N, K, block_size,
+                 a_dtype == MNB_F32, absmax_dtype == MNB_F32, g_pdl.load() != 0};
+    t.code = code;
+    if (!t.a_f32 && gemm_supports(t)) {
+      const cudaError_t e = launch_gemm(t, s);
+      if (e != cudaSuccess) return cuda_fail(e, "mnb_matmul_bnb4");
+      return MNB_OK;
+    }
+  }
   // The decode kernel in code-book mode, over 8-row slices.
   constexpr int64_t kRows = kGemvMaxM / 2;
   for (int64_t m0 = 0; m0 < M; m0 += kRows) {

@@ -101,6 +101,9 @@ struct GemmParams {
   const float *gamma;  // [K] or null (1)
   float eps;
   int K;
+  // Code-book weights (the bitsandbytes-style form; the CB instantiation):
+  // w = code[q] * s with the 16 fp32 values here, no zero points.
+  const float *code;
   int sc_up, zp_up;  // paired: byte offsets of the up halves in a stage's scales / zero points
 };
 
@@ -135,7 +138,8 @@ struct Smem {
   static constexpr int kSc = kCodes + kWStages * kCodeBytes;
   static constexpr int kZp = kSc + kWStages * kScBytes;
   static constexpr int kBias = kZp + kWStages * kZpBytes;
-  static constexpr int kBar = kBias + kBN * 4;
+  static constexpr int kCodeTab = kBias + kBN * 4;  // 16 fp32 code-book values
+  static constexpr int kBar = kCodeTab + 64;
   // ... + acc_full, and acc_empty (the stream-K kernel's drained accumulator)
   static constexpr int kNumBars = 2 * kAStages + 2 * kWStages + 2 * kBStages + 2;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
@@ -278,9 +282,10 @@ __host__ __device__ constexpr int out_col(int c) {
   return (c & ~15) + ((c & 1) ? 8 : 0) + ((c & 15) >> 1);
 }
 
-template <int BS, bool HAS_ZP, bool SF32, int MH>
+template <int BS, bool HAS_ZP, bool SF32, int MH, bool CB = false>
 __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant__ GemmParams p) {
   using S = Smem<MH, BS, SF32>;
+  static_assert(!(CB && HAS_ZP), "code-book weights carry no zero points");
   constexpr int kAStages = S::kAStages, kWStages = S::kWStages, kBStages = S::kBStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles. The offset is added
@@ -434,6 +439,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
     const int ne = tid - 64;
     const int nrow = MH == 1 ? (ne >> 1) : ne, nc0 = MH == 1 ? (ne & 1) * 4 : 0;
     float nss = 0.f;
+    float *sCode = reinterpret_cast<float *>(smem + S::kCodeTab);
+    if (CB) {
+      // Every dequantisation warp writes the same 16 values (identical
+      // stores), so its own reads after __syncwarp need no CTA barrier.
+      if (lane < 16) sCode[lane] = __ldg(p.code + lane);
+      __syncwarp();
+    }
     for (int i = 0; i < nk; ++i) {
       const int s = i % kWStages, bslot = i % kBStages, kb = kb0 + i;
       if (!mbar_wait(wfull + s, (i / kWStages) & 1) ||
@@ -513,13 +525,33 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int bi = BS < kBK ? (16 * j) / BS : 0;  // block of this k step
-        uint32_t r[4];
-        codes_to_bf16x2(wv[j], r);
         uint32_t h00, l00, h02, l02, h10, l10, h12, l12;
-        dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi], h00, l00);  // row g
-        dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi], h02, l02);
-        dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi], h10, l10);  // row g + 8
-        dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi], h12, l12);
+        if (CB) {
+          // Register i of the affine path holds the codes at bits 4i and
+          // 16 + 4i (rows g for even i, g + 8 for odd i): here their code-book
+          // values times the row's scale, in fp32, split hi + lo.
+          const float s0 = SF32 ? sf0[bi] : bf16_bits_to_f32(sb0[bi] & 0xFFFFu);
+          const float s1 = SF32 ? sf1[bi] : bf16_bits_to_f32(sb1[bi] & 0xFFFFu);
+          uint32_t hv[4], lv[4];
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            const uint32_t x = wv[j] >> (4 * ii);
+            const float sc2 = (ii & 1) ? s1 : s0;
+            const float w0 = sCode[x & 15u] * sc2, w1 = sCode[(x >> 16) & 15u] * sc2;
+            hv[ii] = f32x2_to_bf16x2(w0, w1);
+            lv[ii] = f32x2_to_bf16x2(w0 - bf16_bits_to_f32(hv[ii] & 0xFFFFu),
+                                     w1 - bf16_bits_to_f32(hv[ii] >> 16));
+          }
+          h00 = hv[0], l00 = lv[0], h02 = hv[2], l02 = lv[2];
+          h10 = hv[1], l10 = lv[1], h12 = hv[3], l12 = lv[3];
+        } else {
+          uint32_t r[4];
+          codes_to_bf16x2(wv[j], r);
+          dequant_pair<SF32>(r[0], zc0[bi], sb0[bi], sf0[bi], h00, l00);  // row g
+          dequant_pair<SF32>(r[2], zc0[bi], sb0[bi], sf0[bi], h02, l02);
+          dequant_pair<SF32>(r[1], zc1[bi], sb1[bi], sf1[bi], h10, l10);  // row g + 8
+          dequant_pair<SF32>(r[3], zc1[bi], sb1[bi], sf1[bi], h12, l12);
+        }
         // K-major 128-byte swizzle: 16-byte chunk (k / 8) XOR (row % 8); the
         // lo tile sits kBTileBytes after the hi tile.
         const int k0 = 16 * j + 4 * t;
@@ -1594,9 +1626,9 @@ cudaError_t launch_tf32_flags(const GemmParams &p, dim3 grid, bool sf32, bool pd
               : launch_tf32_one<BS, false, false>(p, grid, pdl, stream);
 }
 
-template <int BS, bool HAS_ZP, bool SF32, int MH>
+template <int BS, bool HAS_ZP, bool SF32, int MH, bool CB = false>
 cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t stream) {
-  auto kernel = gemm_kernel<BS, HAS_ZP, SF32, MH>;
+  auto kernel = gemm_kernel<BS, HAS_ZP, SF32, MH, CB>;
   const int smem = Smem<MH, BS, SF32>::kTotal + 1024;
   static std::atomic<unsigned long long> configured{0};
   if (const cudaError_t e = ensure_smem_limit(kernel, smem, configured); e != cudaSuccess)
@@ -1628,6 +1660,9 @@ cudaError_t launch_one(const GemmParams &p, dim3 grid, bool pdl, cudaStream_t st
 template <int BS, int MH>
 cudaError_t launch_flags(const GemmParams &p, dim3 grid, bool sf32, bool pdl,
                          cudaStream_t stream) {
+  if (p.code)  // code-book weights: no zero points
+    return sf32 ? launch_one<BS, false, true, MH, true>(p, grid, pdl, stream)
+                : launch_one<BS, false, false, MH, true>(p, grid, pdl, stream);
   if (p.has_zp)
     return sf32 ? launch_one<BS, true, true, MH>(p, grid, pdl, stream)
                 : launch_one<BS, true, false, MH>(p, grid, pdl, stream);
@@ -1801,6 +1836,7 @@ cudaError_t launch_gemm_tf32(const MatmulArgs &a, cudaStream_t stream) {
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
   p.norm = a.norm ? 1 : 0;
   p.K = static_cast<int>(a.K);
+  p.code = a.code;
   p.gamma = a.gamma;
   p.eps = a.eps;
   const dim3 grid(static_cast<unsigned>(ceil_div(a.N, int64_t(kBN))),
@@ -1863,7 +1899,7 @@ GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
   // for each further tile a CTA's range touches. It wins where whole tiles
   // leave half the CTA slots idle for long (down and o projections with
   // M >= 2048, 4096) and loses where tiles are few or short.
-  if (a.ws && !a.paired && !a.norm && a.ws_bytes > kSkCountBytes) {
+  if (a.ws && !a.paired && !a.norm && !a.code && a.ws_bytes > kSkCountBytes) {
     const int64_t tiles_n = ceil_div(a.N, int64_t(kBN));
     const int64_t units = ceil_div(a.M, int64_t(2 * kBH)) * tiles_n * int64_t(K64);
     const int64_t room = static_cast<int64_t>((a.ws_bytes - kSkCountBytes) / kSkCtaBytes);
@@ -1890,6 +1926,7 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   if (!gemm_supports(a)) return cudaErrorNotSupported;
   if (a.sk_only && (a.a_f32 || a.paired || a.norm || !a.ws)) return cudaErrorNotSupported;
   if (a.norm && (a.a_f32 || a.paired)) return cudaErrorNotSupported;
+  if (a.code && (a.a_f32 || a.paired || a.norm || a.zp || a.sk_only)) return cudaErrorNotSupported;
   if (a.a_f32) return launch_gemm_tf32(a, stream);
   GemmParams p{};
   const uint64_t N16 = ceil_div(a.N, kTileN), K64 = ceil_div(a.K, kChunkK);
@@ -1972,6 +2009,7 @@ cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream) {
   p.kps = static_cast<int>(ceil_div(int64_t(K64), int64_t(ksplit)));
   p.norm = a.norm ? 1 : 0;
   p.K = static_cast<int>(a.K);
+  p.code = a.code;
   p.gamma = a.gamma;
   p.eps = a.eps;
   // TMA stores of the output tile: single weight, no K split, rows of Y a

@@ -83,6 +83,9 @@ struct MatmulArgs {
   bool norm = false;
   const float *gamma = nullptr;
   float eps = 0.f;
+  // Code-book weights (bf16 activations, tensor-core kernel): w = code[q] * s
+  // with the 16 fp32 values here, no zero points.
+  const float *code = nullptr;
 };
 
 // What launch_gemm would launch for a product on a GPU with `sms` SMs (host
@@ -131,8 +134,8 @@ struct GroupArgs {
   // launch_argmax_finalize turns them into indices). Y[0] may be null.
   unsigned long long *amax = nullptr;
   // Code-book weights (the bitsandbytes-style format): w = code[q] * s with
-  // code the 16 fp32 values here (rounded to bf16 for the products), no
-  // zero points. Null: the affine MatMulNBits codes.
+  // code the 16 fp32 values here (each held as a bf16 hi + lo pair for the
+  // products), no zero points. Null: the affine MatMulNBits codes.
   const float *code = nullptr;
 };
 cudaError_t launch_argmax_init(unsigned long long *amax, int M, cudaStream_t stream);

@@ -65,7 +65,24 @@ def test_bnb4_matches_oracle(dev, bs, a_dtype, s_dtype):
             check(Y, R, mag, f"bnb4 M{M} N{N} K{K} bs{bs}")
 
 
-@pytest.mark.parametrize("M", [1, 8, 17])
+@pytest.mark.parametrize("M", [17, 512])
+@pytest.mark.parametrize("s_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("bs", [16, 64, 256])
+def test_bnb4_prefill_rows_on_the_tensor_core_kernel(dev, M, s_dtype, bs):
+    """Above 16 rows with bf16 activations: the tensor-core kernel's code-book
+    mode (ragged N, K of several blocks); seeded rows at M = 512."""
+    N, K = 300, 10 * bs
+    Q, absmax, A, b = problem(M, N, K, bs, torch.bfloat16, s_dtype, True, M + bs)
+    w = mnb.mnb_prepack_bnb4(torch.tensor(pack_bnb4_flat(Q)).to(dev), absmax.to(dev), N, K, bs)
+    Y = mnb.mnb_matmul_bnb4(A.to(dev), w, torch.tensor(CODE).to(dev), b.to(dev))
+    torch.cuda.synchronize()
+    rows = None if M <= 64 else np.sort(np.random.default_rng(M).choice(M, 40, replace=False))
+    R, mag = oracle.bnb4_matmul(A, pack_bnb4_flat(Q), absmax, CODE, b, N=N, K=K,
+                                block_size=bs, rows=rows)
+    check(Y if rows is None else Y[rows], R, mag, f"bnb4 prefill M{M} bs{bs}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 17, 200])
 @pytest.mark.parametrize("a_f32", [False, True], ids=["abf16", "af32"])
 def test_bnb4_adversarial_code_book_within_stated_bound(dev, M, a_f32):
     bs, N = 64, 40
