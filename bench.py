@@ -45,23 +45,27 @@ METRIC = "INT4 decode GEMV GB/s and % HBM peak (M=1); prefill TFLOP/s (M=2048)"
 WORKLOAD = "Qwen3-4B decode step projections, M=1, bf16 A, bs 128, no zp"
 
 
-# DRAM read + write per decode-kernel launch of one decode step, from one ncu
-# capture of the 145 launches (dram__bytes_read.sum + dram__bytes_write.sum),
-# valid only for the decode-kernel sources it was measured on.
+# DRAM traffic of the decode kernel relative to its algorithmic bytes, from
+# an ncu capture of three launches of the Qwen3-4B gate projection (9728 x
+# 2560, bs 128; dram__bytes_read.sum + dram__bytes_write.sum, mean 12,932,608
+# B for 12,865,536 algorithmic), scaled to the step's mean launch; valid only
+# for the decode-kernel sources it was measured on.
 STEP_TRAFFIC = {
-    "bytes_per_launch": 14399640,
+    "ratio": 12932608 / 12865536,
     "sources": ("gemv.cu", "mnb_common.cuh", "mnb_launch.h"),
-    "sha256": "604251cb1579c44863bc26c95029890d02f40b0237f20ce896671d5979cb1d64",
+    "sha256": "62a397c602eef64f95f10d2b9044bab8cb371eb31d186cb8fae259a4569d85bf",
 }
 
 
-def step_traffic():
+def step_traffic(algo_bytes_per_launch):
     import hashlib
     h = hashlib.sha256()
     for f in STEP_TRAFFIC["sources"]:
         with open(os.path.join(ROOT, "int4_weight_only_matmulnbits_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    return STEP_TRAFFIC["bytes_per_launch"] if h.hexdigest() == STEP_TRAFFIC["sha256"] else None
+    if h.hexdigest() != STEP_TRAFFIC["sha256"]:
+        return None
+    return round(STEP_TRAFFIC["ratio"] * algo_bytes_per_launch)
 
 
 def peaks():
@@ -638,14 +642,17 @@ def run_gpu(args, rank, world, dist):
                    "parallelism": f"replicas x{world}"},
         "hbm_fraction": per_gpu / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": per_gpu / hbm_peak, "traffic": step_traffic(),
+                     "unit": "GB/s", "frac": per_gpu / hbm_peak,
+                     "traffic": step_traffic(algo_bytes / len(launches)),
                      "peak_kind": peak_kind,
                      "kernel": "gemv_kernel (every launch of the step)",
                      "achieved_basis": "algorithmic bytes of the step / device time of the "
                                        "step (= bytes per launch / mean launch time)",
                      "algorithmic_bytes_per_launch": algo_bytes / len(launches),
-                     "traffic_basis": "ncu dram read+write per launch, mean over the "
-                                      "step's launches; null if the kernel changed"},
+                     "traffic_basis": "ncu dram read+write of the decode kernel on the "
+                                      "gate shape (3 launches, 1.0052 x algorithmic), "
+                                      "scaled to the step's mean launch; null if the "
+                                      "kernel changed"},
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": m["h2d"],
                 "d2h_bytes_per_step": m["d2h"],
                 "api": "mnb_graph_run_from_host (C ABI): pinned host activations in, the "
