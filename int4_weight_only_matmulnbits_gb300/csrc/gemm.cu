@@ -94,9 +94,10 @@ struct GemmParams {
   int ksplit, kps;  // CTAs splitting K (cluster along z), k stages per CTA
   int paired;       // gate (tiles 0-3 of the B tile) and up (tiles 4-7)
   // RMS-normalized activations (the fusion "RMSNorm into packed projection
-  // input"): the staged A tile becomes A * gamma (rounded to bf16 once) and
-  // each output row is scaled by r[m] = 1 / sqrt(mean_k A[m,k]^2 + eps),
-  // summed over the whole row from the staged tiles (needs ksplit == 1).
+  // input"): gamma[k] multiplies the dequantised weights (in fp32, before the
+  // hi + lo split) and each output row is scaled by r[m] = 1 / sqrt(mean_k
+  // A[m,k]^2 + eps), summed over the whole row from the staged tiles (needs
+  // ksplit == 1).
   int norm;
   const float *gamma;  // [K] or null (1)
   float eps;
@@ -313,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
   if (tid == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(afull + i, 1);
-      mbar_init(aempty + i, 1);
+      // Normalized rows: the dequantisation warps' sum-of-squares pass reads
+      // the A tile too, and arrives when done.
+      mbar_init(aempty + i, p.norm ? 1 + kDqWarps : 1);
     }
     for (int i = 0; i < kWStages; ++i) {
       mbar_init(wfull + i, 1);
@@ -489,36 +492,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
           zc1[bi] = (0x4300u | ((zw.y >> (4 * g)) & 15)) * 0x10001u;
         }
       }
+      // Normalized rows: gamma of this lane's 16 k positions of the stage
+      // (k = 16 j + 4 t + e), folded into the weights below.
+      float gm[4][4];
       if (p.norm) {
-        // The stage's A tile (swizzled rows of 128 bytes): this thread's row
-        // and chunks, sum of squares of the raw values, then A * gamma in
-        // place.
-        const int sa = i % kAStages;
-        if (!mbar_wait(afull + sa, (i / kAStages) & 1)) {
-          record_fault(&g_fault_gemm, kFaultGemmWait);
-          fault = true;
-          break;
-        }
-        unsigned char *arow = smem + S::kA + sa * S::kATileBytes + nrow * 128;
 #pragma unroll
-        for (int c = nc0; c < nc0 + kNormChunks; ++c) {
-          uint4 *q = reinterpret_cast<uint4 *>(arow + ((c ^ (nrow & 7)) * 16));
-          const uint4 x = *q;
-          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-          uint32_t o[4];
-          const int k0 = kb * kBK + 8 * c;
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const float a0 = bf16_bits_to_f32(w[e2] & 0xFFFFu), a1 = bf16_bits_to_f32(w[e2] >> 16);
-            nss = fmaf(a0, a0, nss);
-            nss = fmaf(a1, a1, nss);
-            const int k = k0 + 2 * e2;
-            const float g0 = p.gamma ? (k < p.K ? __ldg(p.gamma + k) : 0.f) : 1.f;
-            const float g1 = p.gamma ? (k + 1 < p.K ? __ldg(p.gamma + k + 1) : 0.f) : 1.f;
-            o[e2] = bf16_bits(a0 * g0) | (bf16_bits(a1 * g1) << 16);
+          for (int e = 0; e < 4; ++e) {
+            const int k = kb * kBK + 16 * j + 4 * t + e;
+            gm[j][e] = p.gamma ? (k < p.K ? __ldg(p.gamma + k) : 0.f) : 1.f;
           }
-          *q = make_uint4(o[0], o[1], o[2], o[3]);
-        }
       }
       const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + tile * kChunkBytes + lane * 16);
       const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -538,6 +522,27 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
             const uint32_t x = wv[j] >> (4 * ii);
             const float sc2 = (ii & 1) ? s1 : s0;
             const float w0 = sCode[x & 15u] * sc2, w1 = sCode[(x >> 16) & 15u] * sc2;
+            hv[ii] = f32x2_to_bf16x2(w0, w1);
+            lv[ii] = f32x2_to_bf16x2(w0 - bf16_bits_to_f32(hv[ii] & 0xFFFFu),
+                                     w1 - bf16_bits_to_f32(hv[ii] >> 16));
+          }
+          h00 = hv[0], l00 = lv[0], h02 = hv[2], l02 = lv[2];
+          h10 = hv[1], l10 = lv[1], h12 = hv[3], l12 = lv[3];
+        } else if (p.norm) {
+          // (q - z) * s * gamma[k] in fp32, split hi + lo (within 2^-16):
+          // gamma rides on the weights, so the A tile stays as staged.
+          uint32_t r[4];
+          codes_to_bf16x2(wv[j], r);
+          const float s0 = SF32 ? sf0[bi] : bf16_bits_to_f32(sb0[bi] & 0xFFFFu);
+          const float s1 = SF32 ? sf1[bi] : bf16_bits_to_f32(sb1[bi] & 0xFFFFu);
+          uint32_t hv[4], lv[4];
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii) {
+            const uint32_t dq = bf16x2_sub(r[ii], (ii & 1) ? zc1[bi] : zc0[bi]);
+            const float sc2 = (ii & 1) ? s1 : s0;
+            const int e0 = (ii >> 1) * 2;  // registers 0, 1: k steps e 0, 1; 2, 3: e 2, 3
+            const float w0 = bf16_bits_to_f32(dq & 0xFFFFu) * sc2 * gm[j][e0];
+            const float w1 = bf16_bits_to_f32(dq >> 16) * sc2 * gm[j][e0 + 1];
             hv[ii] = f32x2_to_bf16x2(w0, w1);
             lv[ii] = f32x2_to_bf16x2(w0 - bf16_bits_to_f32(hv[ii] & 0xFFFFu),
                                      w1 - bf16_bits_to_f32(hv[ii] >> 16));
@@ -568,6 +573,31 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const __grid_constant
       if (lane == 0) {
         mbar_arrive(bfull + bslot);
         mbar_arrive(wempty + s);  // this warp is done with the stage's weights
+      }
+      if (p.norm) {
+        // Sum of squares of this thread's row and chunks of the stage's A
+        // tile (swizzled rows of 128 bytes), read only, beside the MMAs that
+        // read the same tile; then this warp lets the slot go.
+        const int sa = i % kAStages;
+        if (!mbar_wait(afull + sa, (i / kAStages) & 1)) {
+          record_fault(&g_fault_gemm, kFaultGemmWait);
+          fault = true;
+          break;
+        }
+        const unsigned char *arow = smem + S::kA + sa * S::kATileBytes + nrow * 128;
+#pragma unroll
+        for (int c = nc0; c < nc0 + kNormChunks; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(arow + ((c ^ (nrow & 7)) * 16));
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float a0 = bf16_bits_to_f32(w[e2] & 0xFFFFu), a1 = bf16_bits_to_f32(w[e2] >> 16);
+            nss = fmaf(a0, a0, nss);
+            nss = fmaf(a1, a1, nss);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aempty + sa);
       }
     }
 
