@@ -655,7 +655,9 @@ MNB_API mnb_status mnb_chain_run(const void *plan, const mnb_chain_info *info,
  * of a caller buffer; the library allocates no device memory. Each call
  * plans again (host work), copies the plan into the array, waits on the
  * host until that copy has finished on `stream` (so every call
- * synchronises `stream`), then launches; the copy also clears the
+ * synchronises `stream` and none can be recorded by a stream capture: a
+ * capturing stream cannot be synchronised, and the capture would be
+ * invalidated), then launches; the copy also clears the
  * completion counters the launch starts from. A chain whose plan exceeds
  * the array is rejected with MNB_ERR_UNSUPPORTED and a message giving both
  * sizes (the Qwen3-4B decode step needs about 0.6 MB).
@@ -664,9 +666,8 @@ MNB_API mnb_status mnb_chain_run(const void *plan, const mnb_chain_info *info,
  * (two streams, or two host threads) race and must be serialised by the
  * caller. The first call on a device looks up the array's device address
  * (once per device, with that device current) and keeps it for the life of
- * the process; make that first call before any stream capture, and do not
- * use this entry point on a device after cudaDeviceReset (the kept address
- * would no longer map the array).
+ * the process; do not use this entry point on a device after
+ * cudaDeviceReset (the kept address would no longer map the array).
  */
 MNB_API mnb_status mnb_chain_run_noalloc(const mnb_chain_op *ops, int32_t n_ops,
                                          int64_t M, int block_size,
