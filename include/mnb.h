@@ -65,9 +65,13 @@ typedef enum {
   MNB_PATH_AUTO = 0, /* small-M kernel for M <= 16, tensor-core GEMM above */
   MNB_PATH_GEMV = 1, /* split-K decode kernel (M <= 16)                    */
   MNB_PATH_GEMM = 2, /* TMA + tcgen05/TMEM prefill kernel (any M)          */
-  MNB_PATH_GEMM_STREAMK = 3 /* the same kernel's stream-K schedule: bf16
+  MNB_PATH_GEMM_STREAMK = 3, /* the same kernel's stream-K schedule: bf16
                                activations, a single weight and a workspace
                                (mnb_matmul_ws), else MNB_ERR_UNSUPPORTED     */
+  MNB_PATH_GEMM_PAIR = 4 /* persistent CTA-pair tensor-core kernel
+                            (tcgen05.mma.cta_group::2, 256-row tiles): bf16
+                            activations and a single weight, else
+                            MNB_ERR_UNSUPPORTED                           */
 } mnb_path;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -344,7 +348,8 @@ typedef struct {
   int32_t stream_k;  /* 1: the stream-K schedule                             */
   int32_t tf32;      /* 1: the tf32 kernel (fp32 activations)                */
   int32_t tma_store; /* 1: the output tile goes out through TMA stores      */
-  int32_t reserved;  /* 0                                                    */
+  int32_t pair_cols; /* persistent CTA-pair kernel: output columns per
+                        256-row tile (128 .. 256); 0: another kernel        */
   int64_t ctas;      /* CTAs of the tensor-core launch                       */
 } mnb_matmul_plan_info;
 
@@ -443,7 +448,7 @@ MNB_API void mnb_set_programmatic_launch(int enable);
  * runs out records a bit in a device fault word, abandons its tile and
  * exits instead of hanging. This call waits for the current device to be
  * idle, returns the fault bits seen since the last call in *fault_bits
- * (HOST; 0 = none; 1 = decode kernel, 2 = tensor-core kernel, 4 = decode
+ * (HOST; 0 = none; 1 = decode kernel, 2 = a tensor-core kernel, 4 = decode
  * chain) and clears
  * them. Errors: MNB_ERR_NULL, MNB_ERR_CUDA.
  */

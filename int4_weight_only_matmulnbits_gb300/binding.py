@@ -31,7 +31,7 @@ MNB_CODES_AFFINE, MNB_CODES_CODEBOOK = 0, 1
 MNB_PACKED_MAGIC = 0x4B43415034424E4D
 MNB_PACKED_HEADER_BYTES = 256
 MNB_F32, MNB_BF16 = 0, 1
-MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_streamk": 3}
+MNB_PATH = {"auto": 0, "gemv": 1, "gemm": 2, "gemm_streamk": 3, "gemm_pair": 4}
 
 # Every entry point include/mnb.h declares.
 EXPORTS = ("mnb_status_string", "mnb_last_error_string", "mnb_version",
@@ -54,7 +54,7 @@ class PlanInfoC(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("m_slices", ctypes.c_int32),
                 ("tile_rows", ctypes.c_int32), ("k_split", ctypes.c_int32),
                 ("stream_k", ctypes.c_int32), ("tf32", ctypes.c_int32),
-                ("tma_store", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("tma_store", ctypes.c_int32), ("pair_cols", ctypes.c_int32),
                 ("ctas", ctypes.c_int64)]
 
 
@@ -369,7 +369,9 @@ def mnb_matmul_plan(M: int, N: int, K: int, block_size: int, *,
                     sm_count: int = 0) -> dict:
     """What mnb_matmul(..., workspace) would launch (host arithmetic only):
     {"path": "gemv" | "gemm", "m_slices", "tile_rows", "k_split", "stream_k",
-    "tf32", "tma_store", "ctas"}. sm_count 0 asks the current device."""
+    "tf32", "tma_store", "pair_cols", "ctas"}; pair_cols > 0 names the
+    persistent CTA-pair kernel and its tile width. sm_count 0 asks the current
+    device."""
     info = PlanInfoC()
     sd = a_dtype if scale_dtype is None else scale_dtype
     _check(load().mnb_matmul_plan(M, N, K, block_size, _dtype_code(a_dtype), _dtype_code(sd),
@@ -378,7 +380,7 @@ def mnb_matmul_plan(M: int, N: int, K: int, block_size: int, *,
     return {"path": "gemv" if info.path == MNB_PATH["gemv"] else "gemm",
             "m_slices": info.m_slices, "tile_rows": info.tile_rows,
             "k_split": info.k_split, "stream_k": bool(info.stream_k), "tf32": bool(info.tf32),
-            "tma_store": bool(info.tma_store), "ctas": info.ctas}
+            "tma_store": bool(info.tma_store), "pair_cols": info.pair_cols, "ctas": info.ctas}
 
 
 def mnb_matmul_workspace(device=None) -> torch.Tensor:

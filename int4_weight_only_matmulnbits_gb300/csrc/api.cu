@@ -222,7 +222,7 @@ mnb_status validate_matmul_args(const void *A, const void *packed_b,
   if (st != MNB_OK) return st;
   if (!valid_dtype(a_dtype)) return MNB_ERR_DTYPE;
   if (path != MNB_PATH_AUTO && path != MNB_PATH_GEMV && path != MNB_PATH_GEMM &&
-      path != MNB_PATH_GEMM_STREAMK)
+      path != MNB_PATH_GEMM_STREAMK && path != MNB_PATH_GEMM_PAIR)
     return MNB_ERR_UNSUPPORTED;
   if (path == MNB_PATH_GEMV && M > kGemvMaxM) return MNB_ERR_UNSUPPORTED;
   const size_t es = dtype_size(a_dtype);
@@ -275,6 +275,8 @@ mnb_status run_matmul(const void *A, const void *packed_b, const void *scales,
   cudaError_t e;
   if (path == MNB_PATH_GEMV || (path == MNB_PATH_AUTO && M <= kGemvMaxM)) {
     e = launch_gemv(a, stream);
+  } else if (path == MNB_PATH_GEMM_PAIR) {
+    e = launch_gemm_pair(a, stream);
   } else if (path == MNB_PATH_GEMM || path == MNB_PATH_GEMM_STREAMK || gemm_supports(a)) {
     e = launch_gemm(a, stream);
   } else {
@@ -397,10 +399,11 @@ mnb_status mnb_fault_status(unsigned int *fault_bits) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = gemv_take_fault(&a);
   if (e == cudaSuccess) e = gemm_take_fault(&b);
-  unsigned int c = 0;
+  unsigned int c = 0, d = 0;
   if (e == cudaSuccess) e = chain_take_fault(&c);
+  if (e == cudaSuccess) e = pair_take_fault(&d);
   if (e != cudaSuccess) return cuda_fail(e, "mnb_fault_status");
-  *fault_bits = a | b | c;
+  *fault_bits = a | b | c | d;
   return MNB_OK;
 }
 
@@ -605,7 +608,7 @@ mnb_status mnb_matmul_plan(int64_t M, int64_t N, int64_t K, int block_size,
   if (st != MNB_OK) return st;
   if (!valid_dtype(a_dtype)) return MNB_ERR_DTYPE;
   if (path != MNB_PATH_AUTO && path != MNB_PATH_GEMV && path != MNB_PATH_GEMM &&
-      path != MNB_PATH_GEMM_STREAMK)
+      path != MNB_PATH_GEMM_STREAMK && path != MNB_PATH_GEMM_PAIR)
     return MNB_ERR_UNSUPPORTED;
   if (path == MNB_PATH_GEMV && M > kGemvMaxM) return MNB_ERR_UNSUPPORTED;
   int sms = sm_count_in;
@@ -626,6 +629,15 @@ mnb_status mnb_matmul_plan(int64_t M, int64_t N, int64_t K, int block_size,
   mnb_matmul_plan_info r{};
   if (path == MNB_PATH_GEMV || (path == MNB_PATH_AUTO && M <= kGemvMaxM)) {
     r.path = MNB_PATH_GEMV;
+  } else if (path == MNB_PATH_GEMM_PAIR) {
+    if (!pair_supports(a)) return MNB_ERR_UNSUPPORTED;
+    const PairPlan pp = plan_pair(a, sm_count_in > 0 ? sms / 2 : pair_slots());
+    if (pp.nt == 0) return MNB_ERR_UNSUPPORTED;
+    r.path = MNB_PATH_GEMM;
+    r.tile_rows = 256;
+    r.k_split = 1;
+    r.pair_cols = 32 * pp.nt;
+    r.ctas = 2 * int64_t(pp.pairs);
   } else if (path == MNB_PATH_GEMM || path == MNB_PATH_GEMM_STREAMK || gemm_supports(a)) {
     if (!gemm_supports(a) || (a.sk_only && (a.a_f32 || !a.ws))) return MNB_ERR_UNSUPPORTED;
     const GemmPlanInfo g = gemm_plan_info(a, sms);

@@ -153,6 +153,21 @@ cudaError_t launch_gemv_group(const GroupArgs &a, cudaStream_t stream);
 bool gemm_supports(const MatmulArgs &a);
 cudaError_t launch_gemm(const MatmulArgs &a, cudaStream_t stream);
 
+// Persistent CTA-pair tensor-core kernel (gemm_pair.cu): bf16 activations,
+// single affine weights (no gated pair, normalization or code book).
+struct PairPlan {
+  int nt = 0;         // 16-row weight tiles per CTA (tile columns 32 nt); 0: none
+  int pairs = 0;      // CTA pairs launched
+  int64_t tiles = 0;  // 256-row output tiles
+};
+bool pair_supports(const MatmulArgs &a);
+// The tile width and grid for `pairs` resident CTA pairs (host arithmetic).
+PairPlan plan_pair(const MatmulArgs &a, int pairs);
+// CTA pairs the current device holds at once (0 if the query fails).
+int pair_slots();
+cudaError_t launch_gemm_pair(const MatmulArgs &a, cudaStream_t stream);
+cudaError_t pair_take_fault(unsigned int *out);
+
 // Decode chain (chain.cu): ops validated by the C ABI.
 constexpr int kChainMaxDeps = 4;
 constexpr int kChainMaxOps = 4096;

@@ -300,7 +300,7 @@ def test_matmul_ws_checks_its_workspace_on_host(lib):
     assert _call_matmul_ws(lib, 256, 1 << 16) == -6          # covers B and the scales
     assert _call_matmul_ws(lib, (1 << 20) - 256, 512) == -6  # covers the start of Y
     assert _call_matmul_ws(lib, far, 1 << 20, A=None) == -1
-    assert _call_matmul_ws(lib, far, 1 << 20, path=4) == -8
+    assert _call_matmul_ws(lib, far, 1 << 20, path=5) == -8
     # A valid request reaches the device query, which fails without a GPU
     # (MNB_ERR_CUDA, or MNB_ERR_DEVICE for another architecture).
     assert _call_matmul_ws(lib, far, 1 << 20, packed_b=1 << 12) == -10  # no header recorded

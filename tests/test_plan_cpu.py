@@ -108,3 +108,24 @@ def test_argument_errors(lib):
     if not torch.cuda.is_available():  # sm_count 0 asks the device
         assert lib.mnb_matmul_plan(64, 256, 256, 128, 1, 1, 0, 0, 0, 0,
                                    ctypes.byref(info)) in (-7, -9)
+
+
+def test_pair_kernel_tile_widths_fill_the_pairs(lib):
+    """The CTA-pair kernel's tile width (32 nt columns, nt = 4..8 weight
+    tiles per CTA) for the Qwen3-4B shapes at M = 2048 on 76 pairs: the
+    fewest rounds of tiles times the work per tile."""
+    want = {1024: (128, 128), 2560: (160, 152), 4096: (224, 152), 9728: (256, 152)}
+    for N, (cols, ctas) in want.items():
+        r = plan(2048, N, 2560, path="gemm_pair", zero_points=True)
+        assert (r["path"], r["tile_rows"], r["k_split"]) == ("gemm", 256, 1)
+        assert (r["pair_cols"], r["ctas"]) == (cols, ctas), N
+    # A single tile: one pair; past the pairs, every pair is launched.
+    assert plan(17, 16, 264, path="gemm_pair")["ctas"] == 2
+    assert plan(8192, 151936, 2560, path="gemm_pair")["ctas"] == SMS
+
+
+def test_pair_kernel_refusals(lib):
+    with pytest.raises(mnb.MnbError) as e:
+        plan(2048, 2560, 2560, path="gemm_pair", a_dtype=torch.float32)
+    assert e.value.status == -8
+    assert plan(2048, 2560, 2560, path="gemm")["pair_cols"] == 0
