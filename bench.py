@@ -417,9 +417,10 @@ def lm_head_fusions(mnb, lm_launch, dev, steps=50):
     return out
 
 
-def prefill_measure(dev, steps=5, warmup=3, M=2048):
+def prefill_measure(dev, steps=10, warmup=3, M=2048, repeats=5, path="gemm"):
     """TFLOP/s of the tensor-core path at M rows over the seven Qwen3-4B
-    projection shapes (bf16 A, bs 128, zero points, bias), each timed alone;
+    projection shapes (bf16 A, bs 128, zero points, bias), each timed alone
+    as the median of `repeats` regions of `steps` back-to-back launches;
     None when the path is not available."""
     import torch
 
@@ -441,14 +442,16 @@ def prefill_measure(dev, steps=5, warmup=3, M=2048):
         w = mnb.mnb_prepack(B, S, Z, p.N, p.K, bs)
         Y = torch.empty(M, p.N, dtype=torch.bfloat16, device=dev)
         try:
-            mnb.mnb_matmul(A, w, bias, out=Y, path="gemm")
+            mnb.mnb_matmul(A, w, bias, out=Y, path=path)
         except mnb.MnbError as e:
             if e.status == -8:
                 return None
             raise
         for _ in range(warmup):
-            mnb.mnb_matmul(A, w, bias, out=Y, path="gemm")
-        t = time_region(lambda: mnb.mnb_matmul(A, w, bias, out=Y, path="gemm"), steps, stream)
+            mnb.mnb_matmul(A, w, bias, out=Y, path=path)
+        ts = sorted(time_region(lambda: mnb.mnb_matmul(A, w, bias, out=Y, path=path), steps,
+                                stream) for _ in range(repeats))
+        t = ts[len(ts) // 2]
         flops = 2 * M * p.N * p.K * steps
         per[p.name] = flops / t / 1e12
         total_flops += flops
@@ -685,6 +688,17 @@ def run_gpu(args, rank, world, dist):
                     note="the oracle's GB/s on decode-step projections; its prefill rate "
                          "is the same dot products (not run again at M rows)")
             line[key] = pf
+        # The persistent CTA-pair kernel (forced path; the dispatch keeps the
+        # tile-per-CTA kernel, which is faster on these shapes).
+        pp, clk = clocked(local, lambda: prefill_measure(dev, M=2048, path="gemm_pair"))
+        if pp is not None:
+            pp["roofline"] = dict(flops_peak, achieved=pp["value"],
+                                  frac=pp["value"] / bf16_peak, traffic=None,
+                                  kernel="gemm_pair_kernel (7 shapes)")
+            pp["clocks"] = clk
+            pp["workload"] = ("Qwen3-4B prefill projections, M=2048, as 'prefill', through "
+                              "mnb_matmul_path(..., MNB_PATH_GEMM_PAIR)")
+            line["prefill_cta_pair"] = pp
         m6 = measure_step(mnb, dev, STEP_0P6B, args.steps, warmup, seed_base=7000,
                           local=local)
         b6 = m6["algo_bytes"]
@@ -786,6 +800,7 @@ CASES = {
     "gemv_lm_head": (1, 151936, 2560, 128, "bf16", False, False, "auto"),
     "gemm_gate": (2048, 9728, 2560, 128, "bf16", True, True, "gemm"),
     "gemm_gate_f32": (2048, 9728, 2560, 128, "f32", True, True, "gemm"),
+    "gemm_pair_gate": (2048, 9728, 2560, 128, "bf16", True, True, "gemm_pair"),
 }
 
 
