@@ -1776,16 +1776,20 @@ cudaError_t launch_gemm_tf32(const MatmulArgs &a, cudaStream_t stream) {
 // Tile height, K split and schedule of the bf16 kernel for a product on a
 // GPU with `sms` SMs: pure host arithmetic, shared by the launch and by
 // mnb_matmul_plan.
+// Stage costs of the planner's model, us per 64-wide k stage of one CTA.
+constexpr double kStage128 = 1.17, kStage256 = 1.6;
+
 GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
   const uint64_t K64 = ceil_div(a.K, kChunkK);
   const int64_t cols = a.paired ? kBN / 2 : kBN;
   // Tile height (128 or 256 rows) and K split (cluster of 1..8 CTAs, 128-row
-  // tiles only) by a cost model fitted to GB300 measurements: a CTA spends
-  // about 0.72 us per 64-wide k stage with 128 rows and 0.95 us with 256
-  // rows (two CTAs share the SM's tensor core), plus a fixed cost that grows with the
-  // split (the partial tiles' reduction through distributed shared memory);
-  // CTAs run in rounds of what can be resident at once, clusters packing per
-  // GPC.
+  // tiles only) by a cost model fitted to GB300 measurements of the Qwen3-4B
+  // shapes at M = 512, 2048 and 4096 (each dequantised weight as a hi + lo
+  // pair, two MMAs per k step): a CTA spends about 1.17 us per 64-wide k
+  // stage with 128 rows and 1.6 us with 256 rows (two CTAs share the SM's
+  // tensor core), plus a fixed cost that grows with the split (the partial
+  // tiles' reduction through distributed shared memory); CTAs run in rounds
+  // of what can be resident at once, clusters packing per GPC.
   GemmPlan r;
   int &mh = r.mh, &ksplit = r.ksplit;
   double best = 0.0;
@@ -1802,7 +1806,7 @@ GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
         if (slots <= 0) continue;
         const double fixed = c == 1 ? 2.0 : c == 2 ? 4.0 : c == 4 ? 6.0 : 13.0;
         const double cost = double(ceil_div(ctas, slots)) *
-                            (double(kps) * (h == 2 ? 0.95 : 0.72) + fixed);
+                            (double(kps) * (h == 2 ? kStage256 : kStage128) + fixed);
         if (!have || cost < best - 1e-9) {
           best = cost;
           mh = h;
@@ -1830,7 +1834,8 @@ GemmPlan plan_gemm(const MatmulArgs &a, int sms) {
       const int64_t L = ceil_div(units, ctas);
       const int64_t segs = ceil_div(L - 1, int64_t(K64)) + 1;
       const int64_t parts = ceil_div(int64_t(K64), L);
-      const double cost = double(L) * 0.95 + 28.0 + double(segs - 1) + 2.5 * double(parts - 1);
+      const double cost =
+          double(L) * kStage256 + 28.0 + double(segs - 1) + 2.5 * double(parts - 1);
       if (a.sk_only || cost < best - 1e-9) {
         r.sk = true;
         r.sk_ctas = ctas;
