@@ -654,7 +654,9 @@ cudaError_t launch_gemm_pair(const MatmulArgs &a, cudaStream_t stream) {
   p.tiles = static_cast<int>(plan.tiles);
   p.y_vec = (a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.Y) % 16) == 0;
   p = pair_rings(p, a.bs, a.scale_f32, a.zp != nullptr);
-  if (p.a_stages < 4 || pair_smem_bytes(p) > kSmemBudget + 1024) return cudaErrorNotSupported;
+  if (p.a_stages < 4 || p.b_stages > kMaxBStages || p.w_stages > kMaxWStages ||
+      pair_smem_bytes(p) > kSmemBudget + 1024)
+    return cudaErrorNotSupported;
   switch (a.bs) {
     case 16: return pair_launch_flags<16>(p, plan.pairs, a.zp, a.scale_f32, a.pdl, stream);
     case 32: return pair_launch_flags<32>(p, plan.pairs, a.zp, a.scale_f32, a.pdl, stream);
