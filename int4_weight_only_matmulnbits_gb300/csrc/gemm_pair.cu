@@ -19,16 +19,17 @@
 //    pairs, tiles ordered M fastest so that concurrent pairs share weight
 //    columns in L2), with two TMEM accumulators (2 x 256 columns): the MMAs
 //    of the next tile run while the epilogue warps drain the last one.
-//  * Warp roles (24 warps per CTA): 0 A loads (TMA, 128-byte swizzle, a
-//    six-stage ring), 1 packed-weight loads (codes, scales, zero points, a
-//    four-stage ring), 2 the tensor memory and, in CTA 0, the MMAs, 3 in CTA
-//    1 the relay of its A stages, 4-7 the epilogue
-//    (one TMEM lane quarter each), 8 .. 23 the dequantisation in 16 / NT
-//    groups of NT warps, one 16-row weight tile per warp, group i taking the
-//    stages i, i + groups, ... (a warp's hand-off latency then spreads over
-//    several stages), into three B slots of hi and lo bf16 tiles (each
-//    weight w = hi + lo exactly for bf16 scales, within 2^-16 |w| for fp32
-//    scales; the two tiles go through two MMAs into one accumulator).
+//  * Warp roles (24 warps per CTA): 0 A loads (TMA, 128-byte swizzle), 1
+//    packed-weight loads (codes, scales, zero points), 2 the tensor memory
+//    and, in CTA 0, the MMAs, 3 in CTA 1 the relay of its A stages, 4-7 the
+//    epilogue (one TMEM lane quarter each), 8 .. 23 the dequantisation in
+//    16 / NT groups of NT warps, one 16-row weight tile per warp, group i
+//    taking the stages i, i + groups, ... (a warp's hand-off latency then
+//    spreads over several stages), into B slots of hi and lo bf16 tiles
+//    (each weight w = hi + lo exactly for bf16 scales, within 2^-16 |w| for
+//    fp32 scales; the two tiles go through two MMAs into one accumulator).
+//    The ring depths (A 4 to 9 stages, B and weights a multiple of the
+//    group count) are planned per launch by pair_rings.
 //  * Hand-offs across the pair go through CTA 0's mbarriers: both CTAs'
 //    dequantisation warps arrive on CTA 0's bfull, CTA 1's A relay (warp 3)
 //    on CTA 0's apeer once CTA 1's A stage has landed; the MMA completions
