@@ -47,13 +47,13 @@ WORKLOAD = "Qwen3-4B decode step projections, M=1, bf16 A, bs 128, no zp"
 
 # DRAM traffic of the decode kernel relative to its algorithmic bytes, from
 # an ncu capture of three launches of the Qwen3-4B gate projection (9728 x
-# 2560, bs 128; dram__bytes_read.sum + dram__bytes_write.sum, mean 12,932,608
-# B for 12,865,536 algorithmic), scaled to the step's mean launch; valid only
-# for the decode-kernel sources it was measured on.
+# 2560, bs 128; dram__bytes_read.sum + dram__bytes_write.sum, median
+# 12,930,048 B for 12,865,536 algorithmic), scaled to the step's mean launch;
+# valid only for the decode-kernel sources it was measured on.
 STEP_TRAFFIC = {
-    "ratio": 12932608 / 12865536,
+    "ratio": 12930048 / 12865536,
     "sources": ("gemv.cu", "mnb_common.cuh", "mnb_launch.h"),
-    "sha256": "62a397c602eef64f95f10d2b9044bab8cb371eb31d186cb8fae259a4569d85bf",
+    "sha256": "7e836f0e9ac4775f9e39585695f7020438442d61cdb344768b0f8165343b6d30",
 }
 
 
@@ -653,7 +653,7 @@ def run_gpu(args, rank, world, dist):
                                        "step (= bytes per launch / mean launch time)",
                      "algorithmic_bytes_per_launch": algo_bytes / len(launches),
                      "traffic_basis": "ncu dram read+write of the decode kernel on the "
-                                      "gate shape (3 launches, 1.0052 x algorithmic), "
+                                      "gate shape (3 launches, 1.0050 x algorithmic), "
                                       "scaled to the step's mean launch; null if the "
                                       "kernel changed"},
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": m["h2d"],
