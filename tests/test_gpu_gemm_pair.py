@@ -158,3 +158,24 @@ def test_pair_refusals(dev):
     assert e.value.status == -8
     with pytest.raises(mnb.MnbError):
         mnb.mnb_matmul_plan(64, 128, 256, 64, a_dtype=torch.float32, path="gemm_pair")
+
+
+@pytest.mark.parametrize("path", ["gemm", "gemm_pair"])
+def test_codes_equal_to_zero_point_give_bias_exactly(dev, path):
+    """Every code equal to its block's zero point makes every weight exactly
+    zero (hi = lo = 0 in both tensor-core kernels, no offset to cancel), so
+    Y is the bias rounded to bf16, bit for bit, on a ragged shape with
+    several tiles."""
+    M, N, K, bs = 300, 1000, 512, 32
+    prob = make_problem(M, N, K, bs, dtype=torch.bfloat16, zero_points=True, bias=True,
+                        seed=4)
+    nb = K // bs
+    Z = torch.randint(0, 16, (N, nb), generator=torch.Generator().manual_seed(2))
+    prob.zero_points = (Z[:, 0::2] | (Z[:, 1::2] << 4)).to(torch.uint8)
+    codes = Z.repeat_interleave(bs, dim=1)
+    prob.B = (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8).view(N, nb, bs // 2)
+    Y = run(prob, dev, path=path)
+    R, mag = ref(prob)
+    assert not mag.any()
+    want = prob.bias.to(torch.bfloat16).expand(M, N)
+    assert torch.equal(Y.cpu(), want)
