@@ -586,6 +586,22 @@ def crossover(mnb, dev, flush):
     return rows
 
 
+def max_over_ranks(values, dist, device=None):
+    """Element-wise maximum of a list of floats over all ranks (the slowest
+    rank's times); the list itself at N = 1."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_step, steps, world, seconds):
+    """Units per second processed by all ranks together (weak scaling: every
+    rank runs the same step), over the slowest rank's time, in units / 1e9."""
+    return units_per_step * steps * world / seconds / 1e9
+
+
 def run_gpu(args, rank, world, dist):
     import torch
 
@@ -609,16 +625,13 @@ def run_gpu(args, rank, world, dist):
         chain.run()
     t_chain = time_region(chain.run, args.steps, cur)
 
-    ts = torch.tensor([m["t"], m["t_e2e"], t_chain], device=dev, dtype=torch.float64)
-    if dist:
-        dist.all_reduce(ts, op=dist.ReduceOp.MAX)
-    t, t_e2e, t_chain = ts.tolist()
+    t, t_e2e, t_chain = max_over_ranks([m["t"], m["t_e2e"], t_chain], dist, device=dev)
 
     if rank != 0:
         return
-    value = algo_bytes * args.steps * world / t / 1e9
-    e2e = algo_bytes * args.steps * world / t_e2e / 1e9
-    per_gpu = algo_bytes * args.steps / t / 1e9
+    value = whole_job_rate(algo_bytes, args.steps, world, t)
+    e2e = whole_job_rate(algo_bytes, args.steps, world, t_e2e)
+    per_gpu = whole_job_rate(algo_bytes, args.steps, 1, t)
     per = [x * 1e3 for x in m["per"]]
     warmup = max(args.warmup, 3)
     extras = world == 1 and not args.skip_extras
